@@ -1,0 +1,43 @@
+"""Host logic of the seeded workload generators (no GPU, no method arithmetic)."""
+import torch
+
+from linear_attention_state_kda_gb300 import inputs
+
+
+def test_seeded_and_deterministic():
+    a = inputs.make_prefill([100, 28], 2, 16, 8, "bf16", seed=7)
+    b = inputs.make_prefill([100, 28], 2, 16, 8, "bf16", seed=7)
+    for x, y in zip([a.q, a.k, a.v, a.g, a.beta], [b.q, b.k, b.v, b.g, b.beta]):
+        assert torch.equal(x, y)
+    assert a.cu_seqlens.tolist() == [0, 100, 128]
+    assert a.q.dtype == torch.bfloat16 and a.g.dtype == torch.float32
+    assert (a.g <= 0).all() and (a.beta > 0).all() and (a.beta < 1).all()
+    kn = a.k.float().norm(dim=-1)
+    assert (kn - 1).abs().max() < 1e-2          # normalised in fp32 before the bf16 cast
+
+
+def test_decode_slots_unique():
+    d = inputs.make_decode(64, 2, 16, 16, 500, seed=3)
+    s = d.slot_ids.tolist()
+    assert len(set(s)) == len(s) and min(s) >= 0 and max(s) < 500
+
+
+def test_leveled_split_rule():
+    for length, n in [(131072, 16), (65536, 16), (32768, 8), (8192, 4)]:
+        segs = inputs.gang_split(length)
+        assert len(segs) == n, (length, segs)
+        assert sum(segs) == length
+        assert min(segs) >= inputs.SEGMENT_FLOOR
+        assert all(s % 64 == 0 for s in segs[:-1])
+        # deeper segments are not longer (leveling), up to the 64-token rounding
+        assert all(segs[i] + 64 >= segs[i + 1] for i in range(len(segs) - 2))
+    assert inputs.gang_split(8192) == [2048] * 4
+    segs = inputs.workload_segments("varlen_long")
+    assert sum(len(s) for s in segs) == 44
+    offs, seq = inputs.segment_offsets([131072, 65536, 32768, 8192], segs)
+    assert offs[-1].item() == 237568 and seq.tolist() == [0, 16, 32, 40, 44]
+
+
+def test_gang_split_too_short_is_one_segment():
+    assert inputs.gang_split(3000) == [3000]
+    assert inputs.gang_split(4096) == [2048, 2048]

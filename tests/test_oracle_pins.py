@@ -1,0 +1,291 @@
+"""Pins for the CPU oracle: each test checks it against something other than itself.
+
+The pages (pegainfer #970's KDA (M,D) packages and Blelloch prefix scan; kern #44's
+per-sequence KDA state; ATOM #2709's forked KDA state) print no worked example, so the
+oracle is fixed by the mathematics of the gated delta rule
+    S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T,   o_t = scale S_t^T q_t
+and of the package algebra (M2, D2) o (M1, D1) = (M2 M1, M2 D1 + D2):
+closed forms, exact rational arithmetic on tiny inputs, invariants, and brute force over
+every segmentation. Shapes use dk != dv so that a transposed operand cannot pass.
+"""
+import itertools
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.filterwarnings("ignore")
+
+
+def _rand_inputs(rng, T, H, dk, dv, beta_lo=0.0, beta_hi=1.0, g_scale=1.0, unit_k=True):
+    q = rng.standard_normal((T, H, dk))
+    k = rng.standard_normal((T, H, dk))
+    if unit_k:
+        k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, dv))
+    g = -np.log1p(np.exp(rng.standard_normal((T, H, dk)))) * g_scale
+    beta = rng.uniform(beta_lo, beta_hi, (T, H))
+    return q, k, v, g, beta
+
+
+# p1: beta = 0 leaves decay only: S_t = Diag(exp(sum_{i<=t} g_i)) S_0, o_t = scale S_t^T q_t.
+def test_p1_beta_zero_closed_form(oracle_mod):
+    rng = np.random.default_rng(1)
+    T, H, dk, dv = 9, 2, 3, 5
+    q, k, v, g, _ = _rand_inputs(rng, T, H, dk, dv)
+    beta = np.zeros((T, H))
+    S0 = rng.standard_normal((1, H, dk, dv))
+    o, fin = oracle_mod.forward(q, k, v, g, beta, init_state=S0, scale=0.7)
+    gam = np.cumsum(g, axis=0)  # [T, H, dk]
+    for h in range(H):
+        for t in range(T):
+            St = np.exp(gam[t, h])[:, None] * S0[0, h]
+            np.testing.assert_allclose(o[t, h], 0.7 * St.T @ q[t, h], rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(fin[0, h], np.exp(gam[-1, h])[:, None] * S0[0, h],
+                                   rtol=1e-12, atol=1e-14)
+
+
+# p2: a = 1, beta = 1, orthonormal keys overwrite exactly:
+#   S_T = S_0 - sum k_i k_i^T S_0 + sum k_i v_i^T, and reading with k_j returns v_j.
+def test_p2_orthonormal_overwrite(oracle_mod):
+    rng = np.random.default_rng(2)
+    T, H, dk, dv = 5, 1, 7, 4
+    Qm, _ = np.linalg.qr(rng.standard_normal((dk, dk)))
+    k = Qm[:T][:, None, :].copy()                    # orthonormal rows
+    v = rng.standard_normal((T, H, dv))
+    g = np.zeros((T, H, dk))
+    beta = np.ones((T, H))
+    S0 = rng.standard_normal((1, H, dk, dv))
+    # read each step with the key just written: must return that value
+    o, fin = oracle_mod.forward(k.copy(), k, v, g, beta, init_state=S0)
+    np.testing.assert_allclose(o[:, 0], v[:, 0], rtol=0, atol=1e-12)
+    K = k[:, 0]
+    expect = S0[0, 0] - K.T @ (K @ S0[0, 0]) + K.T @ v[:, 0]
+    np.testing.assert_allclose(fin[0, 0], expect, rtol=0, atol=1e-12)
+    # after all writes, reading with an earlier key returns its value (no interference)
+    q2 = np.repeat(k[:1], T, axis=0)
+    o2, _ = oracle_mod.forward(q2, k, v, g, beta, init_state=S0)
+    np.testing.assert_allclose(o2[-1, 0], v[0, 0], rtol=0, atol=1e-12)
+
+
+# p3: one token, written as explicit matrix products (I - b k k^T) Diag(a) S_0 + b k v^T.
+def test_p3_single_token_matrix_form(oracle_mod):
+    rng = np.random.default_rng(3)
+    H, dk, dv = 3, 4, 6
+    for trial in range(5):
+        q, k, v, g, beta = _rand_inputs(rng, 1, H, dk, dv, unit_k=(trial % 2 == 0))
+        S0 = rng.standard_normal((1, H, dk, dv))
+        o, fin = oracle_mod.forward(q, k, v, g, beta, init_state=S0, scale=1.3)
+        for h in range(H):
+            kk = k[0, h][:, None]
+            A = (np.eye(dk) - beta[0, h] * kk @ kk.T) @ np.diag(np.exp(g[0, h]))
+            S1 = A @ S0[0, h] + beta[0, h] * kk @ v[0, h][None, :]
+            np.testing.assert_allclose(fin[0, h], S1, rtol=1e-12, atol=1e-13)
+            np.testing.assert_allclose(o[0, h], 1.3 * S1.T @ q[0, h], rtol=1e-12, atol=1e-13)
+
+
+def _exact_matrix_form(q, k, v, a, beta, S0):
+    """Exact rational evaluation of the matrix form, token by token (lists of Fractions)."""
+    T, dk, dv = len(q), len(q[0]), len(v[0])
+    S = [row[:] for row in S0]
+    outs = []
+    for t in range(T):
+        # A = (I - b k k^T) Diag(a)
+        A = [[((1 if r == c else 0) - beta[t] * k[t][r] * k[t][c]) * a[t][c]
+              for c in range(dk)] for r in range(dk)]
+        S = [[sum(A[r][x] * S[x][j] for x in range(dk)) + beta[t] * k[t][r] * v[t][j]
+              for j in range(dv)] for r in range(dk)]
+        outs.append([sum(S[r][j] * q[t][r] for r in range(dk)) for j in range(dv)])
+    return outs, S
+
+
+# p3b: several tokens against exact rational arithmetic (decays a = 1/2, 3/4, ... exactly).
+def test_p3b_exact_rational_multi_token(oracle_mod):
+    rng = np.random.default_rng(33)
+    T, dk, dv = 4, 3, 2
+    fr = lambda x: Fraction(int(x), 8)
+    q = [[fr(rng.integers(-8, 9)) for _ in range(dk)] for _ in range(T)]
+    k = [[fr(rng.integers(-8, 9)) for _ in range(dk)] for _ in range(T)]
+    v = [[fr(rng.integers(-8, 9)) for _ in range(dv)] for _ in range(T)]
+    a = [[Fraction(int(rng.integers(1, 9)), 8) for _ in range(dk)] for _ in range(T)]
+    beta = [Fraction(int(rng.integers(0, 9)), 8) for _ in range(T)]
+    S0 = [[fr(rng.integers(-8, 9)) for _ in range(dv)] for _ in range(dk)]
+    outs, S = _exact_matrix_form(q, k, v, a, beta, S0)
+    f = lambda m: np.array([[float(x) for x in r] for r in m])
+    qa, ka, va = f(q)[:, None], f(k)[:, None], f(v)[:, None]
+    ga = np.log(f(a))[:, None]
+    o, fin = oracle_mod.forward(qa, ka, va, ga, np.array([[float(b)] for b in beta]),
+                                init_state=f(S0)[None, None])
+    np.testing.assert_allclose(o[:, 0], f(outs), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(fin[0, 0], f(S), rtol=1e-12, atol=1e-12)
+
+
+# p4: write invariant: beta = 1 and |k| = 1 give S_t^T k_t = v_t after every step, any a.
+def test_p4_write_invariant(oracle_mod):
+    rng = np.random.default_rng(4)
+    T, H, dk, dv = 12, 2, 5, 3
+    _, k, v, g, _ = _rand_inputs(rng, T, H, dk, dv)
+    beta = np.ones((T, H))
+    S0 = rng.standard_normal((1, H, dk, dv))
+    o, _ = oracle_mod.forward(k.copy(), k, v, g, beta, init_state=S0)
+    np.testing.assert_allclose(o, v, rtol=0, atol=1e-12)
+
+
+# p5: packages of any segmentation compose to the sequential pass (brute force over all
+# 2^(T-1) cut sets), and the exclusive scan replays every segment exactly.
+def test_p5_package_composition_all_cuts(oracle_mod):
+    rng = np.random.default_rng(5)
+    T, H, dk, dv = 9, 2, 3, 4
+    q, k, v, g, beta = _rand_inputs(rng, T, H, dk, dv, g_scale=0.3)
+    S0 = rng.standard_normal((1, H, dk, dv))
+    o_ref, fin_ref = oracle_mod.forward(q, k, v, g, beta, init_state=S0)
+    for mask in range(1 << (T - 1)):
+        cuts = [0] + [i + 1 for i in range(T - 1) if mask >> i & 1] + [T]
+        M, D = oracle_mod.package(k, v, g, beta, cuts)
+        # left fold with the composition rule, per head
+        for h in range(H):
+            Mc, Dc = np.eye(dk), np.zeros((dk, dv))
+            for p in range(len(cuts) - 1):
+                Mc, Dc = oracle_mod.compose(M[p, h], D[p, h], Mc, Dc)
+            np.testing.assert_allclose(Mc @ S0[0, h] + Dc, fin_ref[0, h], rtol=1e-11,
+                                       atol=1e-12)
+        seg_init, fin = oracle_mod.scan(M, D, [0, len(cuts) - 1], init_state=S0)
+        np.testing.assert_allclose(fin, fin_ref, rtol=1e-11, atol=1e-12)
+        o_rep, _ = oracle_mod.forward(q, k, v, g, beta, cu_seqlens=cuts, init_state=seg_init)
+        np.testing.assert_allclose(o_rep, o_ref, rtol=1e-11, atol=1e-12)
+
+
+# p5b: the package is the affine map of the segment: M S_in + D equals a run from S_in.
+def test_p5b_package_is_affine_map(oracle_mod):
+    rng = np.random.default_rng(55)
+    T, H, dk, dv = 20, 2, 4, 6
+    _, k, v, g, beta = _rand_inputs(rng, T, H, dk, dv, g_scale=0.2)
+    q = np.zeros((T, H, dk))
+    M, D = oracle_mod.package(k, v, g, beta, [0, T])
+    for _ in range(3):
+        S_in = rng.standard_normal((1, H, dk, dv))
+        _, fin = oracle_mod.forward(q, k, v, g, beta, init_state=S_in)
+        for h in range(H):
+            np.testing.assert_allclose(M[0, h] @ S_in[0, h] + D[0, h], fin[0, h],
+                                       rtol=1e-11, atol=1e-12)
+    # the composition rule is associative (checked, not assumed)
+    A = [(rng.standard_normal((dk, dk)), rng.standard_normal((dk, dv))) for _ in range(3)]
+    l = oracle_mod.compose(*A[2], *oracle_mod.compose(*A[1], *A[0]))
+    r = oracle_mod.compose(*oracle_mod.compose(*A[2], *A[1]), *A[0])
+    np.testing.assert_allclose(l[0], r[0], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(l[1], r[1], rtol=1e-12, atol=1e-12)
+
+
+# p6: checkpoint replay: run [0, t), keep S, run [t, T) from it == uninterrupted run.
+def test_p6_checkpoint_replay(oracle_mod):
+    rng = np.random.default_rng(6)
+    T, H, dk, dv = 14, 2, 3, 5
+    q, k, v, g, beta = _rand_inputs(rng, T, H, dk, dv)
+    S0 = rng.standard_normal((1, H, dk, dv))
+    o_ref, fin_ref = oracle_mod.forward(q, k, v, g, beta, init_state=S0)
+    for t in range(T + 1):
+        o1, s1 = oracle_mod.forward(q[:t], k[:t], v[:t], g[:t], beta[:t], init_state=S0)
+        o2, s2 = oracle_mod.forward(q[t:], k[t:], v[t:], g[t:], beta[t:], init_state=s1)
+        np.testing.assert_allclose(np.concatenate([o1, o2]), o_ref, rtol=1e-12, atol=1e-13)
+        np.testing.assert_allclose(s2, fin_ref, rtol=1e-12, atol=1e-13)
+
+
+# p7: structure: heads independent; value columns independent; joint linearity in (S0, V).
+def test_p7_structure(oracle_mod):
+    rng = np.random.default_rng(7)
+    T, H, dk, dv = 11, 3, 4, 5
+    q, k, v, g, beta = _rand_inputs(rng, T, H, dk, dv)
+    S0 = rng.standard_normal((1, H, dk, dv))
+    o, fin = oracle_mod.forward(q, k, v, g, beta, init_state=S0)
+    perm = [2, 0, 1]
+    op, fp = oracle_mod.forward(q[:, perm], k[:, perm], v[:, perm], g[:, perm], beta[:, perm],
+                                init_state=S0[:, perm])
+    np.testing.assert_allclose(op, o[:, perm], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(fp, fin[:, perm], rtol=1e-13, atol=1e-14)
+    j = 2
+    v2, S02 = v.copy(), S0.copy()
+    v2[:, :, j] = 0.0
+    S02[:, :, :, j] = 0.0
+    o2, f2 = oracle_mod.forward(q, k, v2, g, beta, init_state=S02)
+    keep = [c for c in range(dv) if c != j]
+    np.testing.assert_allclose(o2[:, :, keep], o[:, :, keep], rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(f2[..., keep], fin[..., keep], rtol=1e-13, atol=1e-14)
+    assert np.abs(o2[:, :, j]).max() == 0.0
+    vb, Sb = rng.standard_normal(v.shape), rng.standard_normal(S0.shape)
+    oa, fa = oracle_mod.forward(q, k, v, g, beta, init_state=S0)
+    ob, fb = oracle_mod.forward(q, k, vb, g, beta, init_state=Sb)
+    oc, fc = oracle_mod.forward(q, k, 2.0 * v - 3.0 * vb, g, beta, init_state=2.0 * S0 - 3.0 * Sb)
+    np.testing.assert_allclose(oc, 2.0 * oa - 3.0 * ob, rtol=1e-11, atol=1e-11)
+    np.testing.assert_allclose(fc, 2.0 * fa - 3.0 * fb, rtol=1e-11, atol=1e-11)
+
+
+# p8: contraction: |k| = 1, beta in [0,1], a <= 1 => |S_t|_F <= |S_{t-1}|_F + beta |v_t|.
+def test_p8_contraction(oracle_mod):
+    rng = np.random.default_rng(8)
+    T, H, dk, dv = 30, 2, 6, 4
+    q, k, v, g, beta = _rand_inputs(rng, T, H, dk, dv, g_scale=0.05)
+    S = rng.standard_normal((1, H, dk, dv)) * 3.0
+    for t in range(T):
+        _, S1 = oracle_mod.forward(q[t:t + 1], k[t:t + 1], v[t:t + 1], g[t:t + 1],
+                                   beta[t:t + 1], init_state=S)
+        for h in range(H):
+            lhs = np.linalg.norm(S1[0, h])
+            rhs = np.linalg.norm(S[0, h]) + beta[t, h] * np.linalg.norm(v[t, h])
+            assert lhs <= rhs * (1 + 1e-12)
+        S = S1
+
+
+# p10: at g = -softplus(N(0,1)) a 2048-token segment decays every channel by > 700 nats, so
+# its M is exactly zero even in double: such a split alone cannot test the scan. The erase
+# (I - b k k^T) contracts too, so slow decay alone is not enough; with the decay scaled by
+# 1e-4 and beta by 0.02 (the strong-coupling variant) M has spectral norm of order one.
+def test_p10_weak_segment_warning(oracle_mod):
+    rng = np.random.default_rng(10)
+    T, H, dk, dv = 2048, 1, 128, 2
+    _, k, v, g, beta = _rand_inputs(rng, T, H, dk, dv)
+    M, _ = oracle_mod.package(k, v, g, beta, [0, T])
+    assert np.abs(M).max() == 0.0
+    M2, _ = oracle_mod.package(k, v, g * 1e-4, beta * 0.02, [0, T])
+    assert np.linalg.norm(M2[0, 0], 2) > 0.3
+
+
+# decode is one step of the sequential pass on the slots the table names; padding rows
+# (negative ids) and out-of-range ids leave the pool untouched and output zeros.
+def test_decode_is_one_step(oracle_mod):
+    rng = np.random.default_rng(11)
+    B, H, dk, dv, n_slots = 6, 2, 3, 4, 9
+    q, k, v, g, beta = _rand_inputs(rng, B, H, dk, dv)
+    pool = rng.standard_normal((n_slots, H, dk, dv))
+    slots = np.array([4, 0, -1, 8, 12, 2])
+    before = pool.copy()
+    o, bad = oracle_mod.decode(q, k, v, g, beta, slots, pool, scale=0.5)
+    assert bad == 1
+    for b, s in enumerate(slots):
+        if s < 0 or s >= n_slots:
+            assert np.abs(o[b]).max() == 0.0
+            continue
+        ob, fb = oracle_mod.forward(q[b:b + 1], k[b:b + 1], v[b:b + 1], g[b:b + 1],
+                                    beta[b:b + 1], init_state=before[s][None], scale=0.5)
+        np.testing.assert_allclose(o[b], ob[0], rtol=0, atol=0)
+        np.testing.assert_allclose(pool[s], fb[0], rtol=0, atol=0)
+    untouched = [s for s in range(n_slots) if s not in set(slots.tolist())]
+    assert np.array_equal(pool[untouched], before[untouched])
+
+
+# varlen: packing sequences back to back equals running them one at a time.
+def test_varlen_packing(oracle_mod):
+    rng = np.random.default_rng(12)
+    lens = [5, 0, 9, 1]
+    T, H, dk, dv = sum(lens), 2, 3, 4
+    q, k, v, g, beta = _rand_inputs(rng, T, H, dk, dv)
+    S0 = rng.standard_normal((len(lens), H, dk, dv))
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    o, fin = oracle_mod.forward(q, k, v, g, beta, cu_seqlens=cu, init_state=S0)
+    for s in range(len(lens)):
+        a, b = cu[s], cu[s + 1]
+        oi, fi = oracle_mod.forward(q[a:b], k[a:b], v[a:b], g[a:b], beta[a:b],
+                                    init_state=S0[s:s + 1])
+        np.testing.assert_array_equal(o[a:b], oi)
+        np.testing.assert_array_equal(fin[s], fi[0])
+    assert np.array_equal(fin[1], S0[1])  # empty sequence keeps its state
