@@ -1,0 +1,341 @@
+"""Benchmark of the KDA hot path on GB300.
+
+One step = one pass of every hot-path call over synthetic inputs already resident in HBM:
+  * kda_chunk_prefill  on the 16k-token prefill (H=32, T=16384, d=128, bf16 q/k/v);
+  * kda_segment_package -> kda_package_scan -> kda_segment_replay on the same inputs split
+    into 8 segments of 2048 tokens;
+  * kda_decode_step    on 256 rows x 32 heads over a 4096-slot fp32 pool (8.6 GB).
+`value` is the headline metric: prefill tokens per second of kda_chunk_prefill on the 16k
+workload, from CUDA events around that call in each timed step; the other calls are reported
+under "components" (tokens/s, achieved GB/s against the measured HBM peak). Every input is
+larger than L2 (129 MB), so no flush is needed between timed iterations.
+
+`--impl reference` times the CPU oracle (double precision, all host cores) on a bounded
+sample of the same workload: the reference arm of this repository.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s (H=32, d=128, T=16k) and decode state GB/s vs roofline"
+UNIT = "tokens/s"
+
+# Algorithmic bytes per unit (the minimum HBM traffic of each call: every input read once,
+# every output written once). Token-head units for the prefill, (row, head) for decode.
+D = 128
+PREFILL_BYTES_PER_TOKEN_HEAD = 3 * D * 2 + D * 4 + 4 + D * 2   # q,k,v bf16 + g + beta + o
+STATE_BYTES = D * D * 4                                       # one fp32 state
+DECODE_BYTES_PER_ROW_HEAD = 2 * STATE_BYTES + 3 * D * 2 + D * 4 + 4 + D * 2
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, source="fallback")
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [x.strip() for x in l.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def run_gb300(args):
+    import torch
+    import torch.distributed as dist
+    from linear_attention_state_kda_gb300 import inputs, kda
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    kda.lib()
+    peaks = _peaks()
+
+    x = inputs.make_workload("prefill_16k", device=dev)
+    T, H = x.T, x.H
+    segs = inputs.workload_segments("segments_8x2048")
+    offs, seq_seg = inputs.segment_offsets(x.lens, segs)
+    offs, seq_seg = offs.to(dev), seq_seg.to(dev)
+    dec = inputs.make_workload("decode_256", device=dev)
+    B = dec.q.shape[0]
+
+    o = torch.empty_like(x.v)
+    fin = torch.empty(1, H, D, D, device=dev)
+    P = offs.numel() - 1
+    M = torch.empty(P, H, D, D, device=dev)
+    Dp = torch.empty(P, H, D, D, device=dev)
+    seg_init = torch.empty(P, H, D, D, device=dev)
+    fin2 = torch.empty(1, H, D, D, device=dev)
+    o2 = torch.empty_like(x.v)
+    ws = torch.empty(kda.package_scan_workspace(1, P, H, D, D), dtype=torch.uint8, device=dev)
+    od = torch.empty_like(dec.v)
+    stream = torch.cuda.current_stream()
+
+    def prefill():
+        kda.chunk_prefill(x.q, x.k, x.v, x.g, x.beta, o=o, final_state=fin)
+
+    def segment_path():
+        kda.segment_package(x.k, x.v, x.g, x.beta, offs, M=M, D=Dp)
+        kda.package_scan(M, Dp, seq_seg, P, seg_init=seg_init, final_state=fin2, workspace=ws)
+        kda.segment_replay(x.q, x.k, x.v, x.g, x.beta, offs, seg_init, o=o2)
+
+    def decode():
+        kda.decode_step(dec.q, dec.k, dec.v, dec.g, dec.beta, dec.slot_ids, dec.pool, o=od)
+
+    parts = [("prefill_16k", prefill), ("segments_8x2048", segment_path),
+             ("decode_256", decode)]
+    for _ in range(args.warmup):
+        for _, fn in parts:
+            fn()
+    torch.cuda.synchronize()
+
+    ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)] for n, _ in parts}
+    step_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+    launches0 = kda.launch_count()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        step_ev[0].record(stream)
+        for i in range(args.steps):
+            for n, fn in parts:
+                ev[n][i][0].record(stream)
+                fn()
+                ev[n][i][1].record(stream)
+        step_ev[1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    launches = kda.launch_count() - launches0
+    total_ms = step_ev[0].elapsed_time(step_ev[1])
+    comp_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / args.steps for n, _ in parts}
+    if world > 1:
+        t = torch.tensor([total_ms] + [comp_ms[n] for n, _ in parts], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t[0])
+        for i, (n, _) in enumerate(parts):
+            comp_ms[n] = float(t[1 + i])
+
+    hbm = peaks["hbm_gbs"]
+    pf_bytes = T * H * PREFILL_BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
+    seg_bytes = (T * H * (2 * D * 2 + D * 4 + 4)            # package pass: k, v, g, beta
+                 + P * H * 2 * STATE_BYTES                   # packages written
+                 + P * H * 2 * STATE_BYTES + P * H * STATE_BYTES + H * STATE_BYTES  # scan
+                 + T * H * PREFILL_BYTES_PER_TOKEN_HEAD + P * H * STATE_BYTES)     # replay
+    dec_bytes = B * H * DECODE_BYTES_PER_ROW_HEAD + B * 4
+    comps = {
+        "prefill_16k": dict(ms=comp_ms["prefill_16k"],
+                            tokens_per_s=T / (comp_ms["prefill_16k"] * 1e-3),
+                            algorithmic_bytes=pf_bytes,
+                            gbs=pf_bytes / (comp_ms["prefill_16k"] * 1e-3) / 1e9),
+        "segments_8x2048": dict(ms=comp_ms["segments_8x2048"],
+                                tokens_per_s=T / (comp_ms["segments_8x2048"] * 1e-3),
+                                algorithmic_bytes=seg_bytes,
+                                gbs=seg_bytes / (comp_ms["segments_8x2048"] * 1e-3) / 1e9),
+        "decode_256": dict(ms=comp_ms["decode_256"], algorithmic_bytes=dec_bytes,
+                           gbs=dec_bytes / (comp_ms["decode_256"] * 1e-3) / 1e9),
+    }
+    for c in comps.values():
+        c["hbm_frac"] = c["gbs"] / hbm
+    # dominant kernel: the largest share of the step
+    dom = max(comps, key=lambda n: comps[n]["ms"])
+    roofline = {"bound": "hbm", "achieved": round(comps[dom]["gbs"], 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(comps[dom]["gbs"] / hbm, 4), "traffic": None,
+                "kernel": dom, "peak_source": peaks["source"]}
+
+    # end to end through the public API with host buffers: pinned inputs -> device ->
+    # kda_chunk_prefill -> outputs back to pinned host memory, every step.
+    h_in = [t.cpu().pin_memory() for t in (x.q, x.k, x.v, x.g, x.beta)]
+    d_in = [torch.empty_like(t) for t in (x.q, x.k, x.v, x.g, x.beta)]
+    h_o = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    h_f = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = h_o.numel() * h_o.element_size() + h_f.numel() * h_f.element_size()
+
+    def e2e_step():
+        for h, d_ in zip(h_in, d_in):
+            d_.copy_(h, non_blocking=True)
+        kda.chunk_prefill(*d_in, o=o, final_state=fin)
+        h_o.copy_(o, non_blocking=True)
+        h_f.copy_(fin, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t[0])
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_heads)
+
+    value = world * T / (comps["prefill_16k"]["ms"] * 1e-3)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; q,v~N(0,1), k L2-normalised, g=-softplus(N(0,1)), "
+                "beta=sigmoid(N(0,1)))",
+        "config": {"workload": "prefill_16k: H=32, T=16384, dk=dv=128, chunk 64, bf16 q/k/v, "
+                               "fp32 g/beta/state; step also runs segments_8x2048 and "
+                               "decode_256 (256 rows x H32 over a 4096-slot pool)",
+                   "value_is": "tokens/s of kda_chunk_prefill per GPU x n_gpus",
+                   "l2": "inputs larger than L2; no flush", "parallelism": f"replicas{world}"},
+        "components": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
+                           for kk, vv in v.items()} for k, v in comps.items()},
+        "roofline": roofline,
+        "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "what": "kda_chunk_prefill with pinned host inputs copied in and o/final state "
+                        "copied out every step"},
+        "gpu_launches": int(launches),
+        "gpu_launches_per_step": launches / args.steps,
+        "clocks": clk.summary(),
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def cpu_baseline(heads):
+    """The oracle on a bounded sample of the prefill workload: `heads` of the 32 heads of the
+    16k-token prompt (heads are independent), scaled to whole-workload tokens/s."""
+    import torch
+    import oracle
+    from linear_attention_state_kda_gb300 import inputs
+    x = inputs.make_workload("prefill_16k", device="cpu")
+    hs = list(range(heads))
+    f = lambda t: t[:, hs].float().numpy().astype(np.float64)
+    q, k, v, g, b = f(x.q), f(x.k), f(x.v), f(x.g), f(x.beta)
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, g, b, threads=cores)
+    dt = time.perf_counter() - t0
+    tokens_per_s = x.T * (heads / x.H) / dt
+    return {"value": round(tokens_per_s, 2), "unit": UNIT, "cores": min(cores, heads * 4),
+            "kind": "oracle",
+            "sample": f"{heads} of {x.H} heads of the 16k-token prefill (double precision, "
+                      f"token by token), {dt:.2f} s, scaled by {x.H}/{heads} heads"}
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    per = []
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(args.cpu_heads)
+        if i >= args.warmup:
+            per.append(r)
+    value = statistics.median([r["value"] for r in per])
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": "prefill_16k (sampled heads)", "parallelism": "cpu"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
+                         "cores": per[-1]["cores"], "sample": per[-1]["sample"]},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--cpu-heads", type=int, default=4)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gb300(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,179 @@
+/*
+ * kda.h: C ABI of libkda.so, the GB300 (sm_103a) implementation of the Kimi Delta Attention
+ * (KDA) gated delta-rule state recurrence.
+ *
+ * The operation. Per sequence and head, with state S in R^{dk x dv} (row = key channel):
+ *     S_t = (I - beta_t k_t k_t^T) Diag(a_t) S_{t-1} + beta_t k_t v_t^T,   a_t = exp(g_t)
+ *     o_t = scale * S_t^T q_t
+ * g_t in R^{dk} is a per-key-channel log-decay (g <= 0), beta_t a scalar write strength.
+ * This is the "KDA" linear-attention state that pegainfer PR #970 ("feat(k3): cross-process
+ * CP whale gang - fleet-wide long-prompt prefill") prefills with FlashKDA per context-parallel
+ * segment, and whose per-segment "(M,D) packages" it exchanges and combines with a
+ * "Blelloch prefix-scan fallback" (whale-rendezvous and fabric data-plane commit messages).
+ * kern PR #44 keeps one KDA state block per packed sequence (varlen, cu_seqlens) and
+ * ATOM PR #2709 ("feat(kimi-k3): PP8 prefill for P/D serving - KDA state under PP")
+ * updates slot-addressed KDA state one decode token at a time.
+ *
+ * Layouts (all row-major, contiguous, device memory unless stated):
+ *     q, k, g : [tokens, H, dk]     v, o : [tokens, H, dv]     beta : [tokens, H]
+ *     states  : [n, H, dk, dv]      M : [n_segs, H, dk, dk]    D : [n_segs, H, dk, dv]
+ * q, k, v and o have the dtype given by kda_dtype; g, beta and all states are fp32.
+ * Sequences (or segments) are packed back to back along the token axis and delimited by
+ * int32 offset arrays (cu_seqlens[0] = 0, non-decreasing, last = total tokens).
+ *
+ * Supported shapes: dk = dv in {64, 128}; chunk = 64.
+ *
+ * Ownership and ordering. The caller owns every buffer. Each call borrows the pointers for
+ * the stream-ordered duration of the work it enqueues on `stream`; no call allocates device
+ * memory, synchronises the device or keeps state between calls (the one exception being the
+ * process-wide message returned by kda_last_error). Outputs must not alias inputs, except
+ * that the decode pool is read and written in place.
+ *
+ * Errors. Argument checks run on the host before any launch and return
+ * KDA_ERR_INVALID_ARG / KDA_ERR_UNSUPPORTED / KDA_ERR_WORKSPACE without enqueuing work;
+ * a failed launch returns KDA_ERR_CUDA. kda_last_error() then describes the failure.
+ * Conditions only the device can see are OR-ed into the optional device word `status`
+ * (see KDA_STATUS_*); the caller clears it and reads it back when convenient. Nothing
+ * traps, and no call falls back to another implementation.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* kda_stream_t; /* same type as cudaStream_t; NULL = legacy stream */
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1, /* null pointer, negative size, misaligned pointer, bad offsets */
+  KDA_ERR_UNSUPPORTED = 2, /* shape or dtype outside the supported set */
+  KDA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than the query returned */
+  KDA_ERR_CUDA = 4         /* a CUDA runtime/launch error; see kda_last_error() */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype; /* dtype of q, k, v and o */
+
+/* Bits OR-ed into the optional device status word. */
+#define KDA_STATUS_BAD_SLOT 1u    /* decode: a slot id >= n_slots was skipped */
+#define KDA_STATUS_DECAY_RANGE 2u /* prefill/package/replay: within one 64-token chunk some
+                                     key channel decayed by more than 160 nats (sum of -g over
+                                     the chunk > 160); results for that chunk are unreliable */
+#define KDA_STATUS_BAD_OFFSETS 4u /* an offset array was decreasing or out of range, or a
+                                     sequence had more segments than max_segs_per_seq; the
+                                     offending range was treated as empty */
+
+/* Message for the most recent non-OK status returned on this thread ("" if none). */
+KDA_API const char* kda_last_error(void);
+
+/* Library version string. */
+KDA_API const char* kda_version(void);
+
+/* Number of CUDA kernels this process has launched through the library so far (a
+ * diagnostic counter for benchmarks; every successful entry point adds its launches). */
+KDA_API uint64_t kda_launch_count(void);
+
+/*
+ * kda_chunk_prefill: chunked (WY/UT form) prefill over packed sequences.
+ *   n_seqs      number of sequences (>= 0); total_tokens = cu_seqlens[n_seqs].
+ *   cu_seqlens  device int32 [n_seqs + 1]; may be NULL when n_seqs == 1 (one sequence of
+ *               total_tokens tokens).
+ *   init_state  [n_seqs, H, dk, dv] fp32 entry states, or NULL for zeros.
+ *   o           [total_tokens, H, dv] output (dtype dt).
+ *   final_state [n_seqs, H, dk, dv] fp32 exit states, or NULL.
+ *   status      optional device word (KDA_STATUS_DECAY_RANGE).
+ * Source: the chunked FlashKDA prefill of kern PR #44 (varlen build with cu_seqlens and
+ * per-sequence state blocks) and pegainfer PR #970 ("same segment walk, same chunk step").
+ */
+KDA_API kda_status kda_chunk_prefill(kda_dtype dt, int n_seqs, int total_tokens,
+                             const int32_t* cu_seqlens, int H, int dk, int dv, int chunk,
+                             float scale, const void* q, const void* k, const void* v,
+                             const float* g, const float* beta, const float* init_state,
+                             void* o, float* final_state, uint32_t* status,
+                             kda_stream_t stream);
+
+/*
+ * kda_segment_package: per-segment affine (M, D) packages. For each segment
+ * [seg_offsets[p], seg_offsets[p+1]) and head, writes M [dk, dk] and D [dk, dv] such that
+ * running the recurrence over the segment from any entry state S_in ends in
+ * M S_in + D. No outputs o are produced and q is not read.
+ *   seg_offsets device int32 [n_segs + 1].
+ * Source: pegainfer PR #970, "KDA (M,D) packages" of the CP publish surface.
+ */
+KDA_API kda_status kda_segment_package(kda_dtype dt, int n_segs, int total_tokens,
+                               const int32_t* seg_offsets, int H, int dk, int dv, int chunk,
+                               const void* k, const void* v, const float* g,
+                               const float* beta, float* M, float* D, uint32_t* status,
+                               kda_stream_t stream);
+
+/*
+ * kda_package_scan: segmented exclusive prefix over packages with the composition
+ * (M2, D2) o (M1, D1) = (M2 M1, M2 D1 + D2), evaluated as a work-efficient (Blelloch)
+ * up-sweep/down-sweep tree per (sequence, head), then applied to the entry state:
+ *     seg_init[j]    = M_{<j} S_init + D_{<j}   (the state entering segment j)
+ *     final_state[s] = M_{all} S_init + D_{all} (the state after the sequence)
+ * Segments [seq_seg_offsets[s], seq_seg_offsets[s+1]) belong to sequence s, in token order.
+ *   seq_seg_offsets   device int32 [n_seqs + 1] (last = n_segs).
+ *   max_segs_per_seq  host upper bound on any sequence's segment count (1..65536); it sets
+ *                     the number of tree levels launched.
+ *   init_state        [n_seqs, H, dk, dv] or NULL (zeros).
+ *   seg_init          [n_segs, H, dk, dv] output.  final_state [n_seqs, H, dk, dv] or NULL.
+ *   workspace         device scratch of at least kda_package_scan_workspace(...) bytes,
+ *                     256-byte aligned; contents need not be initialised. It holds the
+ *                     padded tree: n_seqs * (3/2) * P2 * H packages of (dk*dk + dk*dv) fp32,
+ *                     P2 = max_segs_per_seq rounded up to a power of two.
+ *   status            optional device word (KDA_STATUS_BAD_OFFSETS).
+ * Source: pegainfer PR #970, "the Blelloch prefix-scan fallback" for combining packages.
+ */
+KDA_API size_t kda_package_scan_workspace(int n_seqs, int max_segs_per_seq, int H, int dk, int dv);
+KDA_API kda_status kda_package_scan(int n_seqs, int n_segs, const int32_t* seq_seg_offsets,
+                            int max_segs_per_seq, int H, int dk, int dv, const float* M,
+                            const float* D, const float* init_state, float* seg_init,
+                            float* final_state, void* workspace, size_t ws_bytes,
+                            uint32_t* status, kda_stream_t stream);
+
+/*
+ * kda_segment_replay: replays every segment from its prefix state: the chunked prefill with
+ * segments as the sequences and seg_init as their entry states. Writes o for every token and,
+ * if seg_final is not NULL, each segment's exit state.
+ * Source: pegainfer PR #970, each CP member prefills its own context segment.
+ */
+KDA_API kda_status kda_segment_replay(kda_dtype dt, int n_segs, int total_tokens,
+                              const int32_t* seg_offsets, int H, int dk, int dv, int chunk,
+                              float scale, const void* q, const void* k, const void* v,
+                              const float* g, const float* beta, const float* seg_init,
+                              void* o, float* seg_final, uint32_t* status,
+                              kda_stream_t stream);
+
+/*
+ * kda_decode_step: one token per batch row over a slot-addressed fp32 state pool,
+ * updated in place: for row b and head h, S = pool[slot_ids[b], h] becomes its successor
+ * and o[b, h] = scale * S_new^T q.
+ *   q, k, g [batch, H, dk]; v, o [batch, H, dv]; beta [batch, H].
+ *   slot_ids   device int32 [batch]. A negative id marks a padding row: it is skipped and
+ *              its o row is written as zeros. An id >= n_slots is skipped the same way and
+ *              sets KDA_STATUS_BAD_SLOT in *status. Two rows naming the same slot race.
+ *   state_pool [n_slots, H, dk, dv] fp32, read and written in place (16-byte aligned).
+ * Source: ATOM PR #2709 (slot-indexed KDA state for decode; read/write state indices) and
+ * kern PR #44 (recurrent-state slots per sequence).
+ */
+KDA_API kda_status kda_decode_step(kda_dtype dt, int batch, int H, int dk, int dv, float scale,
+                           const void* q, const void* k, const void* v, const float* g,
+                           const float* beta, const int32_t* slot_ids, float* state_pool,
+                           int64_t n_slots, void* o, uint32_t* status, kda_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

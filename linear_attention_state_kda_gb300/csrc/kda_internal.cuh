@@ -1,0 +1,80 @@
+// Internal declarations shared by the translation units of libkda.so.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+#include <string>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+// Sets the thread-local message returned by kda_last_error() and passes the status through.
+kda_status set_error(kda_status st, const std::string& msg);
+kda_status check_launch(const char* what);
+// Adds n to the process-wide launch counter returned by kda_launch_count().
+void count_launches(int n);
+
+// Per-token element access for the two input dtypes.
+__device__ __forceinline__ float ld_elem(const float* p, int64_t i) { return p[i]; }
+__device__ __forceinline__ float ld_elem(const __nv_bfloat16* p, int64_t i) {
+  return __bfloat162float(p[i]);
+}
+__device__ __forceinline__ void st_elem(float* p, int64_t i, float x) { p[i] = x; }
+__device__ __forceinline__ void st_elem(__nv_bfloat16* p, int64_t i, float x) {
+  p[i] = __float2bfloat16_rn(x);
+}
+
+// One chunked pass over packed token ranges ("sequences": prefill sequences, replayed
+// segments, or package segments). A CTA owns one (range, head, column tile).
+//
+// Column space: prefill/replay work on the dv value columns. Package mode works on the
+// augmented state [M | D] (dk + dv columns): columns < dk start from the identity and see
+// zero values, columns >= dk start from zero and see v.
+struct ChunkParams {
+  const void* q;          // [T, H, dk] (unused in package mode)
+  const void* k;          // [T, H, dk]
+  const void* v;          // [T, H, dv]
+  const float* g;         // [T, H, dk]
+  const float* beta;      // [T, H]
+  const int32_t* offsets; // [n_ranges + 1] device, or nullptr: one range [0, total_tokens)
+  int n_ranges, total_tokens, H, dk, dv;
+  float scale;
+  const float* init;      // [n_ranges, H, dk, dv] or nullptr (zeros)
+  void* o;                // [T, H, dv] or nullptr
+  float* final_state;     // [n_ranges, H, dk, dv] or nullptr
+  float* M;               // package mode: [n_ranges, H, dk, dk]
+  float* D;               // package mode: [n_ranges, H, dk, dv]
+  uint32_t* status;       // optional device status word
+  int package;            // 1 = package mode
+};
+
+// Chunk size of every chunked kernel.
+constexpr int kChunk = 64;
+// Decay spread (nats over one chunk, per key channel) the chunk kernels accept; beyond it
+// KDA_STATUS_DECAY_RANGE is raised.
+constexpr float kMaxChunkDecay = 160.0f;
+
+// FFMA (CUDA-core) chunk kernel: fp32 arithmetic throughout; any dtype.
+kda_status launch_chunk_simt(const ChunkParams& p, kda_dtype dt, cudaStream_t s);
+
+// Tensor-core (tcgen05/TMEM/TMA) chunk kernel for bf16 inputs; returns KDA_ERR_UNSUPPORTED
+// for shapes it does not handle.
+kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, cudaStream_t s);
+bool chunk_tc_supported(const ChunkParams& p, kda_dtype dt);
+
+// Decode step.
+kda_status launch_decode(kda_dtype dt, int batch, int H, int dk, int dv, float scale,
+                         const void* q, const void* k, const void* v, const float* g,
+                         const float* beta, const int32_t* slot_ids, float* pool,
+                         int64_t n_slots, void* o, uint32_t* status, cudaStream_t s);
+
+// Package scan.
+size_t scan_workspace_bytes(int n_seqs, int max_segs, int H, int dk, int dv);
+kda_status launch_scan(int n_seqs, int n_segs, const int32_t* seq_seg_offsets, int max_segs,
+                       int H, int dk, int dv, const float* M, const float* D,
+                       const float* init_state, float* seg_init, float* final_state,
+                       void* ws, size_t ws_bytes, uint32_t* status, cudaStream_t s);
+
+}  // namespace kda

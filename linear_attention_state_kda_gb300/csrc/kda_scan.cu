@@ -1,0 +1,243 @@
+// Segmented exclusive prefix over KDA segment packages.
+//
+// A package (M, D) maps a segment's entry state to its exit state, S_out = M S_in + D, and
+// two consecutive packages combine as (M2, D2) o (M1, D1) = (M2 M1, M2 D1 + D2) ("apply 1,
+// then 2"). pegainfer PR #970 exchanges these "KDA (M,D) packages" between context-parallel
+// ranks and names a "Blelloch prefix-scan fallback" for combining them; this file runs that
+// work-efficient scan on one GPU, per (sequence, head):
+//   * the sequence's packages are copied into a power-of-two tree, padded with (I, 0);
+//   * up-sweep: at stride d, node i (i+1 multiple of 2d) becomes a[i] o a[i-d];
+//   * the root (the whole sequence's package) gives the exit state, then becomes (I, 0);
+//   * down-sweep: at stride d, (a[i-d], a[i]) <- (a[i], a[i-d] o a[i]);
+//   * leaf j then holds the exclusive prefix (M_<j, D_<j), and the segment's entry state is
+//     M_<j S_init + D_<j.
+// Every combine is a dk x dk times dk x (dk + dv) product. A CTA computes a 32-row block of
+// one combine's result: it reads only its own rows of the left operand, so the left
+// operand's storage can receive the result in place.
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kRows = 32;       // rows of the result per CTA
+constexpr int kThreads = 256;
+
+__host__ __device__ inline int64_t pkg_floats(int dk, int dv) {
+  return (int64_t)dk * dk + (int64_t)dk * dv;
+}
+
+struct Tree {
+  float* base;    // [n_seqs][P2][H] packages (M then D)
+  float* tmp;     // [n_seqs][P2/2][H] packages
+  int P2, H, dk, dv, n_segs;
+  // Segment range of sequence s, or an empty range if the offsets are malformed.
+  __device__ bool seq_range(const int32_t* off, int s, int& first, int& cnt) const {
+    first = off[s];
+    cnt = off[s + 1] - first;
+    if (first < 0 || cnt < 0 || cnt > P2 || first + cnt > n_segs) {
+      first = 0;
+      cnt = 0;
+      return false;
+    }
+    return true;
+  }
+  __device__ float* node(int s, int i, int h) const {
+    return base + (((int64_t)s * P2 + i) * H + h) * pkg_floats(dk, dv);
+  }
+  __device__ float* tnode(int s, int i, int h) const {
+    return tmp + (((int64_t)s * (P2 / 2) + i) * H + h) * pkg_floats(dk, dv);
+  }
+};
+
+// Copy each sequence's packages into its padded tree; pad with (I, 0).
+__global__ void scan_fill(Tree t, const float* __restrict__ M, const float* __restrict__ D,
+                          const int32_t* __restrict__ seq_off, uint32_t* status) {
+  const int i = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  int first, cnt;
+  if (!t.seq_range(seq_off, s, first, cnt) && i == 0 && h == 0 && threadIdx.x == 0 && status)
+    atomicOr(status, KDA_STATUS_BAD_OFFSETS);
+  float* dst = t.node(s, i, h);
+  const int dk = t.dk, dv = t.dv;
+  if (i < cnt) {
+    const float* m = M + ((int64_t)(first + i) * t.H + h) * dk * dk;
+    const float* d = D + ((int64_t)(first + i) * t.H + h) * dk * dv;
+    for (int e = threadIdx.x; e < dk * dk; e += blockDim.x) dst[e] = m[e];
+    for (int e = threadIdx.x; e < dk * dv; e += blockDim.x) dst[dk * dk + e] = d[e];
+  } else {
+    for (int e = threadIdx.x; e < dk * dk; e += blockDim.x)
+      dst[e] = (e / dk == e % dk) ? 1.0f : 0.0f;
+    for (int e = threadIdx.x; e < dk * dv; e += blockDim.x) dst[dk * dk + e] = 0.0f;
+  }
+}
+
+// out = A o B for rows [r0, r0 + 32): out.M = A.M B.M, out.D = A.M B.D + A.D.
+// out may be A's storage (each CTA reads its rows of A before writing them).
+template <int DK, int DV>
+__device__ void combine_rows(const float* A, const float* B, float* out, int r0) {
+  __shared__ float Am[kRows][DK + 1];
+  __shared__ float Ad[kRows][DV];
+  for (int e = threadIdx.x; e < kRows * DK; e += blockDim.x)
+    Am[e / DK][e % DK] = A[(int64_t)(r0 + e / DK) * DK + e % DK];
+  for (int e = threadIdx.x; e < kRows * DV; e += blockDim.x)
+    Ad[e / DV][e % DV] = A[DK * DK + (int64_t)(r0 + e / DV) * DV + e % DV];
+  __syncthreads();
+  constexpr int W = DK + DV;  // result columns
+  for (int col = threadIdx.x; col < W; col += blockDim.x) {
+    const float* bcol = col < DK ? B + col : B + DK * DK + (col - DK);
+    const int ld = col < DK ? DK : DV;
+    float acc[kRows];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) acc[r] = col < DK ? 0.0f : Ad[r][col - DK];
+    for (int x = 0; x < DK; ++x) {
+      const float b = bcol[(int64_t)x * ld];
+#pragma unroll
+      for (int r = 0; r < kRows; ++r) acc[r] = fmaf(Am[r][x], b, acc[r]);
+    }
+    float* dst = col < DK ? out + col : out + DK * DK + (col - DK);
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) dst[(int64_t)(r0 + r) * ld] = acc[r];
+  }
+}
+
+// Up-sweep level d: node i = (2*pair + 2)*d - 1 becomes a[i] o a[i-d].
+template <int DK, int DV>
+__global__ void __launch_bounds__(kThreads) scan_up(Tree t, int d) {
+  const int pair = blockIdx.x, h = blockIdx.y / (DK / kRows);
+  const int r0 = (blockIdx.y % (DK / kRows)) * kRows, s = blockIdx.z;
+  const int i = (2 * pair + 2) * d - 1;
+  combine_rows<DK, DV>(t.node(s, i, h), t.node(s, i - d, h), t.node(s, i, h), r0);
+}
+
+// Down-sweep level d, first half: tmp[pair] = a[i-d] o a[i].
+template <int DK, int DV>
+__global__ void __launch_bounds__(kThreads) scan_down_combine(Tree t, int d) {
+  const int pair = blockIdx.x, h = blockIdx.y / (DK / kRows);
+  const int r0 = (blockIdx.y % (DK / kRows)) * kRows, s = blockIdx.z;
+  const int i = (2 * pair + 2) * d - 1;
+  combine_rows<DK, DV>(t.node(s, i - d, h), t.node(s, i, h), t.tnode(s, pair, h), r0);
+}
+
+// Down-sweep level d, second half: a[i-d] <- a[i]; a[i] <- tmp[pair].
+__global__ void scan_down_move(Tree t, int d) {
+  const int pair = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  const int i = (2 * pair + 2) * d - 1;
+  const int64_t n = pkg_floats(t.dk, t.dv);
+  float* L = t.node(s, i - d, h);
+  float* R = t.node(s, i, h);
+  const float* X = t.tnode(s, pair, h);
+  for (int64_t e = threadIdx.x; e < n; e += blockDim.x) {
+    L[e] = R[e];
+    R[e] = X[e];
+  }
+}
+
+// Applies package P (M then D) to S_init rows [r0, r0+32): out = M S_init + D (D if no init).
+template <int DK, int DV>
+__device__ void apply_rows(const float* P, const float* S_init, float* out, int r0) {
+  __shared__ float Am[kRows][DK + 1];
+  for (int e = threadIdx.x; e < kRows * DK; e += blockDim.x)
+    Am[e / DK][e % DK] = P[(int64_t)(r0 + e / DK) * DK + e % DK];
+  __syncthreads();
+  for (int col = threadIdx.x; col < DV; col += blockDim.x) {
+    for (int r = 0; r < kRows; ++r) {
+      float acc = P[DK * DK + (int64_t)(r0 + r) * DV + col];
+      if (S_init)
+        for (int x = 0; x < DK; ++x) acc = fmaf(Am[r][x], S_init[(int64_t)x * DV + col], acc);
+      out[(int64_t)(r0 + r) * DV + col] = acc;
+    }
+  }
+}
+
+// Root: exit state from the whole-sequence package, then reset the root to (I, 0).
+template <int DK, int DV>
+__global__ void __launch_bounds__(kThreads) scan_root(Tree t, const float* init,
+                                                      float* final_state) {
+  const int h = blockIdx.y / (DK / kRows);
+  const int r0 = (blockIdx.y % (DK / kRows)) * kRows, s = blockIdx.z;
+  float* root = t.node(s, t.P2 - 1, h);
+  const int64_t sd = (int64_t)DK * DV;
+  const float* si = init ? init + ((int64_t)s * t.H + h) * sd : nullptr;
+  if (final_state) apply_rows<DK, DV>(root, si, final_state + ((int64_t)s * t.H + h) * sd, r0);
+  __syncthreads();
+  for (int e = threadIdx.x; e < kRows * DK; e += blockDim.x) {
+    const int r = r0 + e / DK, c = e % DK;
+    root[(int64_t)r * DK + c] = (r == c) ? 1.0f : 0.0f;
+  }
+  for (int e = threadIdx.x; e < kRows * DV; e += blockDim.x)
+    root[DK * DK + (int64_t)(r0 + e / DV) * DV + e % DV] = 0.0f;
+}
+
+// Entry state of segment j of sequence s from its exclusive prefix.
+template <int DK, int DV>
+__global__ void __launch_bounds__(kThreads) scan_apply(Tree t, const int32_t* seq_off,
+                                                       const float* init, float* seg_init) {
+  const int j = blockIdx.x, h = blockIdx.y / (DK / kRows);
+  const int r0 = (blockIdx.y % (DK / kRows)) * kRows, s = blockIdx.z;
+  int first, cnt;
+  t.seq_range(seq_off, s, first, cnt);
+  if (j >= cnt) return;
+  const int64_t sd = (int64_t)DK * DV;
+  const float* si = init ? init + ((int64_t)s * t.H + h) * sd : nullptr;
+  apply_rows<DK, DV>(t.node(s, j, h), si, seg_init + ((int64_t)(first + j) * t.H + h) * sd, r0);
+}
+
+int next_pow2(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+template <int DK, int DV>
+kda_status run(int n_seqs, int n_segs, const int32_t* seq_off, int max_segs, int H,
+               const float* M,
+               const float* D, const float* init, float* seg_init, float* final_state,
+               void* ws, uint32_t* status, cudaStream_t s) {
+  Tree t;
+  t.P2 = next_pow2(max_segs);
+  t.H = H;
+  t.dk = DK;
+  t.dv = DV;
+  t.n_segs = n_segs;
+  t.base = (float*)ws;
+  t.tmp = t.base + (int64_t)n_seqs * t.P2 * H * pkg_floats(DK, DV);
+  const int rb = DK / kRows;
+  scan_fill<<<dim3(t.P2, H, n_seqs), kThreads, 0, s>>>(t, M, D, seq_off, status);
+  for (int d = 1; d < t.P2; d <<= 1)
+    scan_up<DK, DV><<<dim3(t.P2 / (2 * d), H * rb, n_seqs), kThreads, 0, s>>>(t, d);
+  scan_root<DK, DV><<<dim3(1, H * rb, n_seqs), kThreads, 0, s>>>(t, init, final_state);
+  for (int d = t.P2 / 2; d >= 1; d >>= 1) {
+    scan_down_combine<DK, DV><<<dim3(t.P2 / (2 * d), H * rb, n_seqs), kThreads, 0, s>>>(t, d);
+    scan_down_move<<<dim3(t.P2 / (2 * d), H, n_seqs), kThreads, 0, s>>>(t, d);
+  }
+  scan_apply<DK, DV><<<dim3(t.P2, H * rb, n_seqs), kThreads, 0, s>>>(t, seq_off, init,
+                                                                      seg_init);
+  int levels = 0;
+  for (int d = 1; d < t.P2; d <<= 1) ++levels;
+  count_launches(3 + 3 * levels);
+  return check_launch("kda_package_scan");
+}
+
+}  // namespace
+
+size_t scan_workspace_bytes(int n_seqs, int max_segs, int H, int dk, int dv) {
+  const int64_t P2 = next_pow2(max_segs < 1 ? 1 : max_segs);
+  const int64_t nodes = (int64_t)n_seqs * (P2 + P2 / 2) * H;
+  return (size_t)(nodes * pkg_floats(dk, dv) * sizeof(float)) + 256;
+}
+
+kda_status launch_scan(int n_seqs, int n_segs, const int32_t* seq_seg_offsets, int max_segs,
+                       int H, int dk, int dv, const float* M, const float* D,
+                       const float* init_state, float* seg_init, float* final_state,
+                       void* ws, size_t ws_bytes, uint32_t* status, cudaStream_t s) {
+  (void)ws_bytes;
+  if (n_seqs == 0) return KDA_OK;
+  if (dk == 128 && dv == 128)
+    return run<128, 128>(n_seqs, n_segs, seq_seg_offsets, max_segs, H, M, D, init_state, seg_init,
+                         final_state, ws, status, s);
+  if (dk == 64 && dv == 64)
+    return run<64, 64>(n_seqs, n_segs, seq_seg_offsets, max_segs, H, M, D, init_state, seg_init,
+                       final_state, ws, status, s);
+  return set_error(KDA_ERR_UNSUPPORTED, "kda_package_scan: dk = dv must be 64 or 128");
+}
+
+}  // namespace kda

@@ -1,0 +1,193 @@
+"""Thin Python binding of libkda.so (include/kda.h): one function per C entry point.
+
+Argument marshalling only: tensors are passed as raw device pointers with their sizes, on
+the current torch CUDA stream; every step of the computation runs in the library's CUDA
+kernels. Outputs that the caller does not supply are allocated with torch (plumbing).
+Loading fails loudly if the library was not built: there is no fallback.
+"""
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA = range(5)
+KDA_F32, KDA_BF16 = 0, 1
+STATUS_BAD_SLOT, STATUS_DECAY_RANGE, STATUS_BAD_OFFSETS = 1, 2, 4
+
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status, msg):
+        super().__init__(f"[kda status {status}] {msg}")
+        self.status = status
+
+
+def lib():
+    """The loaded libkda.so (ctypes). Raises if it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"libkda.so not found at {LIB_PATH}: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, F, Z, I64 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t,
+                       ctypes.c_int64)
+    L.kda_last_error.restype = ctypes.c_char_p
+    L.kda_last_error.argtypes = []
+    L.kda_version.restype = ctypes.c_char_p
+    L.kda_version.argtypes = []
+    L.kda_launch_count.restype = ctypes.c_uint64
+    L.kda_launch_count.argtypes = []
+    L.kda_chunk_prefill.restype = I
+    L.kda_chunk_prefill.argtypes = [I, I, I, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P]
+    L.kda_segment_package.restype = I
+    L.kda_segment_package.argtypes = [I, I, I, P, I, I, I, I, P, P, P, P, P, P, P, P]
+    L.kda_package_scan_workspace.restype = Z
+    L.kda_package_scan_workspace.argtypes = [I, I, I, I, I]
+    L.kda_package_scan.restype = I
+    L.kda_package_scan.argtypes = [I, I, P, I, I, I, I, P, P, P, P, P, P, Z, P, P]
+    L.kda_segment_replay.restype = I
+    L.kda_segment_replay.argtypes = [I, I, I, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P]
+    L.kda_decode_step.restype = I
+    L.kda_decode_step.argtypes = [I, I, I, I, I, F, P, P, P, P, P, P, P, I64, P, P, P]
+    _lib = L
+    return L
+
+
+def version():
+    return lib().kda_version().decode()
+
+
+def launch_count():
+    """Kernels launched through the library by this process so far."""
+    return int(lib().kda_launch_count())
+
+
+def last_error():
+    return lib().kda_last_error().decode()
+
+
+def _check(st):
+    if st != KDA_OK:
+        raise KdaError(st, last_error())
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _dt(t):
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def chunk_prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, scale=1.0, o=None,
+                  final_state=None, want_final=True, status=None, chunk=64, stream=None):
+    """kda_chunk_prefill. Returns (o, final_state)."""
+    _contig(q, k, v, g, beta, cu_seqlens, init_state, o, final_state)
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    n = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if o is None:
+        o = torch.empty(T, H, dv, dtype=q.dtype, device=q.device)
+    if final_state is None and want_final:
+        final_state = torch.empty(n, H, dk, dv, dtype=torch.float32, device=q.device)
+    _check(lib().kda_chunk_prefill(_dt(q), n, T, _ptr(cu_seqlens), H, dk, dv, chunk,
+                                   float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                   _ptr(beta), _ptr(init_state), _ptr(o), _ptr(final_state),
+                                   _ptr(status), _stream(stream)))
+    return o, final_state
+
+
+def segment_package(k, v, g, beta, seg_offsets, M=None, D=None, status=None, chunk=64,
+                    stream=None):
+    """kda_segment_package. Returns (M, D)."""
+    _contig(k, v, g, beta, seg_offsets, M, D)
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    P = seg_offsets.numel() - 1
+    if M is None:
+        M = torch.empty(P, H, dk, dk, dtype=torch.float32, device=k.device)
+    if D is None:
+        D = torch.empty(P, H, dk, dv, dtype=torch.float32, device=k.device)
+    _check(lib().kda_segment_package(_dt(k), P, T, _ptr(seg_offsets), H, dk, dv, chunk,
+                                     _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(M), _ptr(D),
+                                     _ptr(status), _stream(stream)))
+    return M, D
+
+
+def package_scan_workspace(n_seqs, max_segs_per_seq, H, dk, dv):
+    return int(lib().kda_package_scan_workspace(n_seqs, max_segs_per_seq, H, dk, dv))
+
+
+def package_scan(M, D, seq_seg_offsets, max_segs_per_seq, init_state=None, seg_init=None,
+                 final_state=None, want_final=True, workspace=None, status=None, stream=None):
+    """kda_package_scan. Returns (seg_init, final_state)."""
+    _contig(M, D, seq_seg_offsets, init_state, seg_init, final_state)
+    P, H, dk, dv = D.shape
+    n = seq_seg_offsets.numel() - 1
+    if seg_init is None:
+        seg_init = torch.empty(P, H, dk, dv, dtype=torch.float32, device=D.device)
+    if final_state is None and want_final:
+        final_state = torch.empty(n, H, dk, dv, dtype=torch.float32, device=D.device)
+    ws_bytes = package_scan_workspace(n, max_segs_per_seq, H, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=D.device)
+    _check(lib().kda_package_scan(n, P, _ptr(seq_seg_offsets), int(max_segs_per_seq), H, dk,
+                                  dv, _ptr(M), _ptr(D), _ptr(init_state), _ptr(seg_init),
+                                  _ptr(final_state), _ptr(workspace), workspace.numel(),
+                                  _ptr(status), _stream(stream)))
+    return seg_init, final_state
+
+
+def segment_replay(q, k, v, g, beta, seg_offsets, seg_init, scale=1.0, o=None,
+                   seg_final=None, want_final=False, status=None, chunk=64, stream=None):
+    """kda_segment_replay. Returns (o, seg_final)."""
+    _contig(q, k, v, g, beta, seg_offsets, seg_init, o, seg_final)
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    P = seg_offsets.numel() - 1
+    if o is None:
+        o = torch.empty(T, H, dv, dtype=q.dtype, device=q.device)
+    if seg_final is None and want_final:
+        seg_final = torch.empty(P, H, dk, dv, dtype=torch.float32, device=q.device)
+    _check(lib().kda_segment_replay(_dt(q), P, T, _ptr(seg_offsets), H, dk, dv, chunk,
+                                    float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                                    _ptr(beta), _ptr(seg_init), _ptr(o), _ptr(seg_final),
+                                    _ptr(status), _stream(stream)))
+    return o, seg_final
+
+
+def decode_step(q, k, v, g, beta, slot_ids, state_pool, scale=1.0, o=None, status=None,
+                stream=None):
+    """kda_decode_step (state_pool updated in place). Returns o."""
+    _contig(q, k, v, g, beta, slot_ids, state_pool, o)
+    B, H, dk = k.shape
+    dv = v.shape[2]
+    if o is None:
+        o = torch.empty(B, H, dv, dtype=q.dtype, device=q.device)
+    _check(lib().kda_decode_step(_dt(q), B, H, dk, dv, float(scale), _ptr(q), _ptr(k), _ptr(v),
+                                 _ptr(g), _ptr(beta), _ptr(slot_ids), _ptr(state_pool),
+                                 int(state_pool.shape[0]), _ptr(o), _ptr(status),
+                                 _stream(stream)))
+    return o

@@ -1,0 +1,102 @@
+"""The C-ABI library builds, loads and exports every declared symbol; host-side argument
+checks reject bad calls before any launch (no GPU needed: no call here reaches CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from linear_attention_state_kda_gb300 import build as libbuild
+    libbuild.build()
+    from linear_attention_state_kda_gb300 import kda
+    return kda.lib()
+
+
+def _declared():
+    with open(os.path.join(ROOT, "include", "kda.h")) as f:
+        src = f.read()
+    return sorted(set(re.findall(r"KDA_API\s+[\w\s\*]+?\b(kda_\w+)\s*\(", src)))
+
+
+def test_header_symbols_exported(L):
+    names = _declared()
+    assert len(names) >= 8, names
+    for n in names:
+        assert hasattr(L, n), f"{n} not exported"
+    for n in ["kda_chunk_prefill", "kda_segment_package", "kda_package_scan",
+              "kda_segment_replay", "kda_decode_step"]:
+        assert n in names
+
+
+def test_version(L):
+    from linear_attention_state_kda_gb300 import kda
+    assert "sm_103a" in kda.version()
+
+
+def test_workspace_query(L):
+    from linear_attention_state_kda_gb300 import kda
+    w = kda.package_scan_workspace(4, 16, 32, 128, 128)
+    # 4 sequences x (16 + 8) tree nodes x 32 heads x (128*128 + 128*128) fp32
+    assert w >= 4 * 24 * 32 * 2 * 128 * 128 * 4
+    assert kda.package_scan_workspace(1, 3, 2, 64, 64) == \
+        kda.package_scan_workspace(1, 4, 2, 64, 64)
+    assert kda.package_scan_workspace(0, 4, 2, 64, 64) == 0
+
+
+def _prefill(L, dt=1, n=1, T=64, cu=None, H=2, dk=128, dv=128, chunk=64, ptr=4096):
+    p = ptr
+    return L.kda_chunk_prefill(dt, n, T, cu, H, dk, dv, chunk, 1.0, p, p, p, p, p, None, p,
+                               None, None, None)
+
+
+def test_prefill_argument_checks(L):
+    from linear_attention_state_kda_gb300 import kda
+    assert _prefill(L, dk=96, dv=96) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(L, dk=128, dv=64) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(L, chunk=32) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(L, dt=7) == kda.KDA_ERR_UNSUPPORTED
+    assert _prefill(L, H=0) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill(L, T=-1) == kda.KDA_ERR_INVALID_ARG
+    assert _prefill(L, n=2, cu=None) == kda.KDA_ERR_INVALID_ARG
+    assert "cu_seqlens" in kda.last_error()
+    assert _prefill(L, ptr=4098) == kda.KDA_ERR_INVALID_ARG      # misaligned
+    assert "aligned" in kda.last_error()
+    # null inputs with tokens to process
+    assert L.kda_chunk_prefill(1, 1, 64, None, 2, 128, 128, 64, 1.0, None, None, None, None,
+                               None, None, None, None, None, None) == kda.KDA_ERR_INVALID_ARG
+    # nothing to do is OK and launches nothing
+    assert _prefill(L, n=0) == kda.KDA_OK
+
+
+def test_scan_and_package_checks(L):
+    from linear_attention_state_kda_gb300 import kda
+    p = 4096
+    assert L.kda_package_scan(1, 2, p, 2, 2, 128, 128, p, p, None, p, None, None, 0, None,
+                              None) == kda.KDA_ERR_WORKSPACE
+    assert L.kda_package_scan(1, 2, p, 0, 2, 128, 128, p, p, None, p, None, p, 1 << 40, None,
+                              None) == kda.KDA_ERR_INVALID_ARG
+    assert L.kda_package_scan(1, 2, p, 2, 2, 96, 96, p, p, None, p, None, p, 1 << 40, None,
+                              None) == kda.KDA_ERR_UNSUPPORTED
+    assert L.kda_segment_package(1, 2, 128, None, 2, 128, 128, 64, p, p, p, p, p, p, None,
+                                 None) == kda.KDA_ERR_INVALID_ARG
+    assert L.kda_segment_replay(1, 2, 128, None, 2, 128, 128, 64, 1.0, p, p, p, p, p, p, p,
+                                None, None, None) == kda.KDA_ERR_INVALID_ARG
+    assert "kda_segment_replay" in kda.last_error()
+
+
+def test_decode_checks(L):
+    from linear_attention_state_kda_gb300 import kda
+    p = 4096
+    assert L.kda_decode_step(1, 4, 2, 128, 128, 1.0, p, p, p, p, p, p, p, 0, p, None,
+                             None) == kda.KDA_ERR_INVALID_ARG
+    assert L.kda_decode_step(1, 4, 2, 128, 128, 1.0, p, p, p, p, p, p, p + 8, 10, p, None,
+                             None) == kda.KDA_ERR_INVALID_ARG
+    assert L.kda_decode_step(1, 4, 2, 32, 32, 1.0, p, p, p, p, p, p, p, 10, p, None,
+                             None) == kda.KDA_ERR_UNSUPPORTED
+    assert L.kda_decode_step(1, 0, 2, 128, 128, 1.0, p, p, p, p, p, p, p, 10, p, None,
+                             None) == kda.KDA_OK
