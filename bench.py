@@ -320,8 +320,42 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_profile_case(args):
+    """A small case of one call (inputs still larger than L2, a few GB on the device at most)
+    for ncu captures: `--profile-case prefill|package|replay|scan|decode`, `--launches N`."""
+    import torch
+    from linear_attention_state_kda_gb300 import inputs, kda
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    case = args.profile_case
+    if case == "decode":
+        d = inputs.make_decode(256, 32, D, D, 1024, seed=1004, device=dev)
+        fns = [lambda: kda.decode_step(d.q, d.k, d.v, d.g, d.beta, d.slot_ids, d.pool)]
+    else:
+        x = inputs.make_prefill([4096], 32, D, D, "bf16", seed=1001, device=dev)
+        offs = torch.tensor([0, 2048, 4096], dtype=torch.int32, device=dev)
+        sso = torch.tensor([0, 2], dtype=torch.int32, device=dev)
+        M, Dp = kda.segment_package(x.k, x.v, x.g, x.beta, offs)
+        si, _ = kda.package_scan(M, Dp, sso, 2)
+        fns = {
+            "prefill": [lambda: kda.chunk_prefill(x.q, x.k, x.v, x.g, x.beta)],
+            "package": [lambda: kda.segment_package(x.k, x.v, x.g, x.beta, offs, M=M, D=Dp)],
+            "scan": [lambda: kda.package_scan(M, Dp, sso, 2, seg_init=si)],
+            "replay": [lambda: kda.segment_replay(x.q, x.k, x.v, x.g, x.beta, offs, si)],
+        }[case]
+    torch.cuda.synchronize()
+    for _ in range(args.launches):
+        for f in fns:
+            f()
+    torch.cuda.synchronize()
+    print(f"profile case {case}: {args.launches} launch(es) done")
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--profile-case", default=None,
+                    choices=["prefill", "package", "scan", "replay", "decode"])
+    ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
@@ -331,7 +365,9 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    if args.impl == "reference":
+    if args.profile_case:
+        run_profile_case(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_gb300(args)

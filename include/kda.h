@@ -72,6 +72,8 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype; /* dtype of q, k, v and o 
 #define KDA_STATUS_BAD_OFFSETS 4u /* an offset array was decreasing or out of range, or a
                                      sequence had more segments than max_segs_per_seq; the
                                      offending range was treated as empty */
+#define KDA_STATUS_TIMEOUT 8u     /* a tensor-core CTA waited more than 2 s for its own copies
+                                     or MMAs and stopped early; its outputs are incomplete */
 
 /* Message for the most recent non-OK status returned on this thread ("" if none). */
 KDA_API const char* kda_last_error(void);
