@@ -145,6 +145,30 @@ KDA_API kda_status kda_package_scan(int n_seqs, int n_segs, const int32_t* seq_s
                             uint32_t* status, kda_stream_t stream);
 
 /*
+ * kda_package_scan_noalloc: kda_package_scan without a caller workspace, for callers that
+ * cannot allocate device memory (for instance a serving loop that has reserved all of HBM for
+ * its state pools, or a custom-op interface that provides no allocator). The pages have no
+ * counterpart of this call; it is a deployment convenience.
+ *   Arguments are those of kda_package_scan minus workspace/ws_bytes; the caller still passes
+ *   every input and output buffer.
+ *   Scratch: a 64 MiB, 256-byte aligned device array inside the library, reserved on every
+ *   GPU that loads the library and held until the process exits. A scan whose
+ *   kda_package_scan_workspace(...) exceeds 64 MiB returns KDA_ERR_WORKSPACE (use
+ *   kda_package_scan then). The call allocates nothing (no cudaMalloc or cudaFree).
+ *   The first call on a device looks up the array's device address with that device
+ *   current; make it before any stream capture. All calls share the one array and it keeps
+ *   the last call's contents (the scan writes all scratch it reads, so no clearing is needed);
+ *   calls that overlap on the GPU race on it.
+ */
+KDA_API kda_status kda_package_scan_noalloc(int n_seqs, int n_segs,
+                                            const int32_t* seq_seg_offsets,
+                                            int max_segs_per_seq, int H, int dk, int dv,
+                                            const float* M, const float* D,
+                                            const float* init_state, float* seg_init,
+                                            float* final_state, uint32_t* status,
+                                            kda_stream_t stream);
+
+/*
  * kda_segment_replay: replays every segment from its prefix state: the chunked prefill with
  * segments as the sequences and seg_init as their entry states. Writes o for every token and,
  * if seg_final is not NULL, each segment's exit state.

@@ -51,6 +51,8 @@ def lib():
     L.kda_package_scan_workspace.argtypes = [I, I, I, I, I]
     L.kda_package_scan.restype = I
     L.kda_package_scan.argtypes = [I, I, P, I, I, I, I, P, P, P, P, P, P, Z, P, P]
+    L.kda_package_scan_noalloc.restype = I
+    L.kda_package_scan_noalloc.argtypes = [I, I, P, I, I, I, I, P, P, P, P, P, P, P]
     L.kda_segment_replay.restype = I
     L.kda_segment_replay.argtypes = [I, I, I, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P]
     L.kda_decode_step.restype = I
@@ -157,6 +159,26 @@ def package_scan(M, D, seq_seg_offsets, max_segs_per_seq, init_state=None, seg_i
                                   dv, _ptr(M), _ptr(D), _ptr(init_state), _ptr(seg_init),
                                   _ptr(final_state), _ptr(workspace), workspace.numel(),
                                   _ptr(status), _stream(stream)))
+    return seg_init, final_state
+
+
+def package_scan_noalloc(M, D, seq_seg_offsets, max_segs_per_seq, init_state=None,
+                         seg_init=None, final_state=None, want_final=True, status=None,
+                         stream=None):
+    """kda_package_scan_noalloc: the scan with the library's built-in 64 MiB scratch, for
+    callers that cannot allocate device memory (pass seg_init / final_state to allocate
+    nothing here either). Returns (seg_init, final_state)."""
+    _contig(M, D, seq_seg_offsets, init_state, seg_init, final_state)
+    P, H, dk, dv = D.shape
+    n = seq_seg_offsets.numel() - 1
+    if seg_init is None:
+        seg_init = torch.empty(P, H, dk, dv, dtype=torch.float32, device=D.device)
+    if final_state is None and want_final:
+        final_state = torch.empty(n, H, dk, dv, dtype=torch.float32, device=D.device)
+    _check(lib().kda_package_scan_noalloc(n, P, _ptr(seq_seg_offsets), int(max_segs_per_seq),
+                                          H, dk, dv, _ptr(M), _ptr(D), _ptr(init_state),
+                                          _ptr(seg_init), _ptr(final_state), _ptr(status),
+                                          _stream(stream)))
     return seg_init, final_state
 
 
