@@ -138,16 +138,21 @@ def run_gb300(args):
     def prefill():
         kda.chunk_prefill(x.q, x.k, x.v, x.g, x.beta, o=o, final_state=fin)
 
-    def segment_path():
+    def package():
         kda.segment_package(x.k, x.v, x.g, x.beta, offs, M=M, D=Dp)
+
+    def scan():
         kda.package_scan(M, Dp, seq_seg, P, seg_init=seg_init, final_state=fin2, workspace=ws)
+
+    def replay():
         kda.segment_replay(x.q, x.k, x.v, x.g, x.beta, offs, seg_init, o=o2)
 
     def decode():
         kda.decode_step(dec.q, dec.k, dec.v, dec.g, dec.beta, dec.slot_ids, dec.pool, o=od)
 
-    parts = [("prefill_16k", prefill), ("segments_8x2048", segment_path),
-             ("decode_256", decode)]
+    # the segment path is package -> scan -> replay; each call is timed on its own too
+    parts = [("prefill_16k", prefill), ("seg_package", package), ("seg_scan", scan),
+             ("seg_replay", replay), ("decode_256", decode)]
     for _ in range(args.warmup):
         for _, fn in parts:
             fn()
@@ -180,6 +185,8 @@ def run_gb300(args):
         total_ms = float(t[0])
         for i, (n, _) in enumerate(parts):
             comp_ms[n] = float(t[1 + i])
+    comp_ms["segments_8x2048"] = (comp_ms["seg_package"] + comp_ms["seg_scan"] +
+                                  comp_ms["seg_replay"])
 
     hbm = peaks["hbm_gbs"]
     pf_bytes = T * H * PREFILL_BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
@@ -196,7 +203,9 @@ def run_gb300(args):
         "segments_8x2048": dict(ms=comp_ms["segments_8x2048"],
                                 tokens_per_s=T / (comp_ms["segments_8x2048"] * 1e-3),
                                 algorithmic_bytes=seg_bytes,
-                                gbs=seg_bytes / (comp_ms["segments_8x2048"] * 1e-3) / 1e9),
+                                gbs=seg_bytes / (comp_ms["segments_8x2048"] * 1e-3) / 1e9,
+                                package_ms=comp_ms["seg_package"], scan_ms=comp_ms["seg_scan"],
+                                replay_ms=comp_ms["seg_replay"]),
         "decode_256": dict(ms=comp_ms["decode_256"], algorithmic_bytes=dec_bytes,
                            gbs=dec_bytes / (comp_ms["decode_256"] * 1e-3) / 1e9),
     }

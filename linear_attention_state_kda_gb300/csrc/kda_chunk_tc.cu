@@ -6,29 +6,27 @@
 //   gamma = cumsum(g), rho = gamma_C / 2, Kh = k e^(gamma-rho), Qh = q e^(gamma-rho),
 //   Kb = k e^(rho-gamma), Sh = e^rho S_0
 //   A    = [Kh; Qh] Kb^T                       (MMA_A: M 128, N 64, K = dk)
-//   T    = (I + strict_lower(beta_r A_kk))^-1  (CUDA cores, blocked 16 x 16)
-//   W^T  = Kh^T (T diag(beta))^T               (MMA_W: A = Kh^T from TMEM, M = dk, N 64)
-//   Ut   = T diag(beta) V                      (MMA_U: N 32, K = 64 tokens)
+//   T    = (I + strict_lower(beta_r A_kk))^-1  (CUDA cores, blocked 16 x 16), TB = T diag(beta)
+//   W^T  = Kh^T TB^T                           (MMA_W: A = Kh^T from TMEM, M = dk, N 64)
+//   Ut   = TB V                                (MMA_U: A = TB from TMEM, N 32, K = 64 tokens)
 //   X    = [W; Qh] Sh                          (MMA_X: N 32, K = dk)
 //   U    = Ut - X[0:64]
-//   O    = X[64:128] + tril(A_qk) U            (MMA_Z accumulates into X)
+//   O    = X[64:128] + tril(A_qk) U            (MMA_Z: A = masked A from TMEM, into X)
 //   Y    = Kb^T U                              (MMA_Y: A = Kb^T from TMEM, M = dk, N 32)
-//   S_C  = e^rho (Sh + Y)                      (since gamma_C - rho = rho)
+//   S_C  = e^rho (Sh + Y) = e^(2 rho) S_0 + e^rho Y
 // Every MMA is kind::tf32 with fp32 accumulation in TMEM, and every shared-memory operand is
 // K-major in the 128-byte swizzle (tf32 operands read MN-major came back as zeros on this
-// part); the two products that contract over the chunk's tokens with a key-side operand
-// on the M side take that operand (Kh^T, Kb^T) from TMEM, where the operand-building threads
-// (one per key channel) store it directly. tf32 throughout holds the fp32 state within a few
-// 1e-3 of the double-precision recurrence; bf16 operands for the state-touching products
-// would not (measured by emulation against the oracle).
+// part); operands that would need the other orientation are staged in TMEM instead, by the
+// threads that produce them. tf32 throughout holds the fp32 state within a few 1e-3 of the
+// double-precision recurrence; bf16 operands for the state-touching products would not
+// (measured by emulation against the oracle).
 //
 // A CTA owns one (sequence or segment, head, 32-column tile of the state) and walks the
-// range's chunks in order; the tile's 128 x 32 state lives in registers of the first
-// warpgroup (thread c holds row c, which is TMEM lane c of the accumulators). q, k and the
-// value tile arrive by TMA (two 64-column 128-byte-swizzled boxes each for q and k); g and
-// beta are read directly by the per-channel scan. In package mode the CTA runs the same
-// chunks on one 32-column tile of the augmented state [M | D] (identity / zero start, zero /
-// v values) and produces no outputs.
+// range's chunks in order. The tile's 128 x 32 state lives in TMEM (lane = key channel).
+// q, k, v, g and beta of a chunk arrive by TMA (q and k as two 64-column 128-byte-swizzled
+// boxes each); the next chunk's loads are issued as soon as the staging buffer is free. In
+// package mode the CTA runs the same chunks on one 32-column tile of the augmented state
+// [M | D] (identity / zero start, zero / v values) and produces no outputs.
 //
 // Waits on mbarriers are bounded (2 s of globaltimer); on expiry the CTA raises
 // KDA_STATUS_TIMEOUT, drains its own MMAs and copies (bounded), frees its TMEM and returns.
@@ -52,9 +50,9 @@ constexpr uint32_t XA_OFF = 0;                    // [128 rows][128] fp32: [Kh |
 constexpr uint32_t XA_KB = 128 * 128;             //   K-blocks (32 columns) of 16 KiB
 constexpr uint32_t KB_OFF = XA_OFF + 4 * XA_KB;   // [64 rows][128] fp32: Kb
 constexpr uint32_t KB_KB = 64 * 128;
-constexpr uint32_t TQ_OFF = KB_OFF + 4 * KB_KB;   // per K-block: [TB 8K][zeros 8K][Aqk 8K]
-constexpr uint32_t TQ_KB = 3 * 8192;
-constexpr uint32_t VT_OFF = TQ_OFF + 2 * TQ_KB;   // [32 cols][64 tokens] fp32: V^T
+constexpr uint32_t TB_OFF = KB_OFF + 4 * KB_KB;   // [64 rows][64] fp32: T diag(beta)
+constexpr uint32_t TB_KB = 64 * 128;
+constexpr uint32_t VT_OFF = TB_OFF + 2 * TB_KB;   // [32 cols][64 tokens] fp32: V^T
 constexpr uint32_t VT_KB = 32 * 128;
 constexpr uint32_t UT_OFF = VT_OFF + 2 * VT_KB;   // [32 cols][64 tokens] fp32: U^T
 constexpr uint32_t UT_KB = 32 * 128;
@@ -63,26 +61,32 @@ constexpr uint32_t SH_KB = 32 * 128;
 constexpr uint32_t STG_OFF = SH_OFF + 4 * SH_KB;  // TMA staging (also T-solve scratch)
 constexpr uint32_t STG_Q = STG_OFF;               // 2 x [64][64] bf16 swizzled boxes
 constexpr uint32_t STG_K = STG_OFF + 16384;
-constexpr uint32_t STG_V = STG_OFF + 32768;       // [64][32] bf16, unswizzled
-constexpr uint32_t STG_BYTES = 36864;
+constexpr uint32_t STG_V = STG_OFF + 32768;       // [64][32] bf16
+constexpr uint32_t STG_G = STG_OFF + 36864;       // [64][128] fp32
+constexpr uint32_t STG_B = STG_OFF + 69632;       // [64][4] fp32 (beta of 4 heads)
+constexpr uint32_t STG_BYTES = 70656;
 constexpr uint32_t MISC_OFF = STG_OFF + STG_BYTES;
-constexpr uint32_t SMEM_BYTES = MISC_OFF + 4096 + 1024;  // + alignment slack
+constexpr uint32_t SMEM_BYTES = MISC_OFF + 2048 + 1024;  // + alignment slack
 
-// T-solve scratch inside the staging area (free between the operand build and the next TMA)
-constexpr int LA = 65;
-constexpr uint32_t SCR_A = STG_OFF;                    // A_kk [64][65] fp32
-constexpr uint32_t SCR_X = STG_OFF + 64 * LA * 4;      // X = T [64][65]
-constexpr uint32_t SCR_P = STG_OFF + 2 * 64 * LA * 4;  // 3 x [16][16]
-static_assert(SCR_P + 3 * 256 * 4 <= STG_OFF + STG_BYTES, "scratch overflow");
+// T-solve scratch inside the staging area (q, k, v and g are consumed by then; the next
+// chunk's loads are issued after the solve). Rows padded to 68 floats: 16-byte aligned rows
+// whose banks shift by 4 per row.
+constexpr int LA = 68;
+constexpr uint32_t SCR_A = STG_OFF;                    // beta_r A_kk [64][68] fp32
+constexpr uint32_t SCR_X = STG_OFF + 64 * LA * 4;      // X = (I + A_kk)^-1 [64][68]
+constexpr uint32_t SCR_P = STG_OFF + 2 * 64 * LA * 4;  // 3 x [16][16] partial products
+static_assert(SCR_P + 3 * 256 * 4 <= STG_B, "scratch overflow");
 
 // TMEM columns (512 allocated)
-constexpr uint32_t TM_A = 0;      // 64: A = [Kh; Qh] Kb^T
+constexpr uint32_t TM_A = 0;      // 64: [Kh; Qh] Kb^T; lanes 64..127 masked to tril(A_qk)
 constexpr uint32_t TM_WT = 64;    // 64: W^T (lanes = key channels)
 constexpr uint32_t TM_U = 128;    // 32: Ut (lanes 0..63 = tokens)
 constexpr uint32_t TM_X = 160;    // 32: X, then O in lanes 64..127
 constexpr uint32_t TM_Y = 192;    // 32: Y (lanes = key channels)
 constexpr uint32_t TM_KHT = 224;  // 64: Kh^T operand (lanes = key channels, columns = tokens)
 constexpr uint32_t TM_KBT = 288;  // 64: Kb^T operand
+constexpr uint32_t TM_TB = 352;   // 64: TB operand (lanes 0..63 = tokens; 64..127 zero)
+constexpr uint32_t TM_S = 416;    // 32: state tile (lanes = key channels)
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -90,7 +94,6 @@ struct Misc {
   uint64_t bar_tma, bar_a, bar_w, bar_x, bar_y, bar_drain;
   uint32_t tmem_base;
   int abort;
-  float beta[C];
   float part[2][DK];
 };
 
@@ -111,13 +114,16 @@ __device__ __forceinline__ float bf16at(const uint8_t* base, uint32_t off) {
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ CUtensorMap tmq,
                 const __grid_constant__ CUtensorMap tmk,
-                const __grid_constant__ CUtensorMap tmv) {
+                const __grid_constant__ CUtensorMap tmv,
+                const __grid_constant__ CUtensorMap tmg,
+                const __grid_constant__ CUtensorMap tmb) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   Misc* misc = reinterpret_cast<Misc*>(sm + MISC_OFF);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int qd = warp & 3;                 // TMEM lane quarter of this warp
+  const int ch = warp >> 2;                // column half of this warp in TMEM reads
   const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
   const int tile = blockIdx.x, h = blockIdx.y, sidx = blockIdx.z;
   const int H = p.H;
@@ -137,7 +143,7 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
       t_end = t_begin;
     }
   }
-  const uint32_t tx_bytes = (pkg ? 0u : 16384u) + 16384u + 4096u;
+  const uint32_t tx_bytes = (pkg ? 0u : 16384u) + 16384u + 4096u + 32768u + 1024u;
 
   // ---- one-time setup
   if (warp == 0) {
@@ -155,39 +161,42 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
     fence_mbar_init();
     tma_prefetch_desc(&tmk);
     tma_prefetch_desc(&tmv);
+    tma_prefetch_desc(&tmg);
+    tma_prefetch_desc(&tmb);
     if (!pkg) tma_prefetch_desc(&tmq);
   }
-  // zero block of the TB / Aqk region (rows 64..127 of TB == rows 0..63 of the Aqk view)
-  for (uint32_t e = tid; e < 2 * 2048; e += kThreads) {
-    const uint32_t kb = e >> 11, w = e & 2047;
-    f32at(sm, TQ_OFF + kb * TQ_KB + 8192)[w] = 0.0f;
-  }
-  if (pkg) {  // no queries: the Qh rows and the A_qk block stay zero
+  // TB: blocks above the diagonal stay zero; the solve rewrites the rest every chunk
+  for (uint32_t e = tid; e < 2 * 2048; e += kThreads) f32at(sm, TB_OFF)[e] = 0.0f;
+  if (pkg) {  // no queries: the Qh rows stay zero
     for (uint32_t e = tid; e < 4 * 2048; e += kThreads) {
       const uint32_t kb = e >> 11, w = e & 2047;
       f32at(sm, XA_OFF + kb * XA_KB + 8192)[w] = 0.0f;
     }
-    for (uint32_t e = tid; e < 2 * 2048; e += kThreads) {
-      const uint32_t kb = e >> 11, w = e & 2047;
-      f32at(sm, TQ_OFF + kb * TQ_KB + 16384)[w] = 0.0f;
-    }
-  }
-  // state tile: thread c < 128 holds row c
-  float S[TW], Sh[TW], Ut[TW];
-#pragma unroll
-  for (int j = 0; j < TW; ++j) {
-    float x = 0.0f;
-    if (tid < DK) {
-      if (pkg) x = (mcols && tid == j0 + j) ? 1.0f : 0.0f;
-      else if (p.init) x = p.init[(((int64_t)sidx * H + h) * DK + tid) * DK + j0 + j];
-    }
-    S[j] = x;
-    Sh[j] = 0.0f;
-    Ut[j] = 0.0f;
   }
   cta_sync();
   const uint32_t tbase = misc->tmem_base;
   const uint32_t sbase = smem_u32(sm);
+  {
+    // state tile into TMEM (lane = row c; warps 0-3 columns 0..15, warps 4-7 16..31), and
+    // zeros into the padding lanes 64..127 of the TB operand
+    float v[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int col = ch * 16 + j;
+      float x = 0.0f;
+      if (pkg) x = (mcols && c == j0 + col) ? 1.0f : 0.0f;
+      else if (p.init) x = p.init[(((int64_t)sidx * H + h) * DK + c) * DK + j0 + col];
+      v[j] = x;
+    }
+    tmem_st16(tbase + lane_base + TM_S + ch * 16, v);
+    if (qd >= 2) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[j] = 0.0f;
+      tmem_st16(tbase + lane_base + TM_TB + ch * 32, v);
+      tmem_st16(tbase + lane_base + TM_TB + ch * 32 + 16, v);
+    }
+    tmem_st_wait();
+  }
 
   auto issue_tma = [&](int t0) {
     mbar_arrive_expect_tx(&misc->bar_tma, tx_bytes);
@@ -198,6 +207,8 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
     tma_load_3d(sm + STG_K, &tmk, &misc->bar_tma, 0, h, t0);
     tma_load_3d(sm + STG_K + 8192, &tmk, &misc->bar_tma, 64, h, t0);
     tma_load_3d(sm + STG_V, &tmv, &misc->bar_tma, vcol0 < 0 ? 0 : vcol0, h, t0);
+    tma_load_3d(sm + STG_G, &tmg, &misc->bar_tma, 0, h, t0);
+    tma_load_2d(sm + STG_B, &tmb, &misc->bar_tma, h & ~3, t0);
   };
   bool tma_out = false;  // thread 0: a load is in flight, completing phase parity tma_par
   uint32_t tma_par = 0;
@@ -205,59 +216,70 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
     issue_tma(t_begin);
     tma_out = true;
   }
+  cta_sync();
 
+  const float* gs = f32at(sm, STG_G);
+  const float* bs4 = f32at(sm, STG_B);
+  const int hb = h & 3;
   uint32_t it = 0;
   bool ok = true;
   for (int t0 = t_begin; t0 < t_end; t0 += C, ++it) {
     const int n = min(C, t_end - t0);
     const uint32_t par = it & 1u;
     // ================= Ph1: decay, operands, state in the midpoint frame
+    if (!mbar_wait(&misc->bar_tma, par)) misc->abort = 1;
+    else tma_out = false;
+    const int nv = n - half * 32;  // valid rows in this thread's half
     float gl[32];
     float acc = 0.0f;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const int r = half * 32 + i;
-      gl[i] = (r < n) ? p.g[((int64_t)(t0 + r) * H + h) * DK + c] * kLog2e : 0.0f;
+      gl[i] = (i < nv) ? gs[(half * 32 + i) * DK + c] * kLog2e : 0.0f;
       acc += gl[i];
     }
     misc->part[half][c] = acc;
-    if (tid < C) misc->beta[tid] = (tid < n) ? p.beta[(int64_t)(t0 + tid) * H + h] : 0.0f;
     __syncthreads();
+    if (misc->abort) { ok = false; break; }
     const float p0 = misc->part[0][c], p1 = misc->part[1][c];
     const float rho2 = 0.5f * (p0 + p1);  // log2 units
     if (half == 0 && !((p0 + p1) >= -kMaxChunkDecay * kLog2e) && p.status)
       atomicOr(p.status, KDA_STATUS_DECAY_RANGE);
-    if (!mbar_wait(&misc->bar_tma, par)) misc->abort = 1;
-    else tma_out = false;
-    __syncthreads();
-    if (misc->abort) { ok = false; break; }
     {
+      // Row r = 32 half + t of every tile below: (r >> 3) and (r & 7) are compile-time per t,
+      // so each swizzled address is a per-thread base plus a constant and one XOR.
+      const uint32_t b16 = STG_K + (c >> 6) * 8192 + (c & 7) * 2 + half * 4096;
+      const uint32_t x16 = (c & 63) >> 3;
+      const uint32_t bxa = XA_OFF + (c >> 5) * XA_KB + (c & 3) * 4 + half * 4096;
+      const uint32_t bkb = KB_OFF + (c >> 5) * KB_KB + (c & 3) * 4 + half * 4096;
+      const uint32_t x32 = (c & 31) >> 2;
       float gam = half ? p0 : 0.0f;
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
         float kh[16], kb[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int r = half * 32 + blk * 16 + i;
-          gam += gl[blk * 16 + i];
+          const int t = blk * 16 + i;
+          const uint32_t row = (uint32_t)(t >> 3) * 1024u + (uint32_t)(t & 7) * 128u;
+          gam += gl[t];
           const float x = gam - rho2;
-          const float e1 = exp2f(x), e2 = exp2f(-x);
+          const float e1 = ex2_approx(x), e2 = ex2_approx(-x);
           float kv = 0.0f, qv = 0.0f;
-          if (r < n) {
-            kv = bf16at(sm, STG_K + sw128_off16(r, c, 8192));
-            if (!pkg) qv = bf16at(sm, STG_Q + sw128_off16(r, c, 8192));
+          if (t < nv) {
+            const uint32_t o16 = b16 + row + ((x16 ^ (uint32_t)(t & 7)) << 4);
+            kv = bf16at(sm, o16);
+            if (!pkg) qv = bf16at(sm, o16 - (STG_K - STG_Q));
           }
           kh[i] = kv * e1;
           kb[i] = kv * e2;
-          *f32at(sm, XA_OFF + sw128_off32(r, c, XA_KB)) = kh[i];
-          if (!pkg) *f32at(sm, XA_OFF + sw128_off32(64 + r, c, XA_KB)) = qv * e1;
-          *f32at(sm, KB_OFF + sw128_off32(r, c, KB_KB)) = kb[i];
+          const uint32_t sw = row + ((x32 ^ (uint32_t)(t & 7)) << 4);
+          *f32at(sm, bxa + sw) = kh[i];
+          if (!pkg) *f32at(sm, bxa + 8192 + sw) = qv * e1;
+          *f32at(sm, bkb + sw) = kb[i];
         }
         // Kh^T and Kb^T as TMEM operands: lane = channel c, column = token
         tmem_st16(tbase + lane_base + TM_KHT + half * 32 + blk * 16, kh);
         tmem_st16(tbase + lane_base + TM_KBT + half * 32 + blk * 16, kb);
       }
-      tmem_st_wait();
     }
     for (int e = tid; e < C * TW; e += kThreads) {  // V^T: row = value column, K = token
       const int j = e >> 6, r = e & 63;
@@ -265,15 +287,18 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
       if (r < n && has_v) x = bf16at(sm, STG_V + r * 64 + j * 2);
       *f32at(sm, VT_OFF + sw128_off32(j, r, VT_KB)) = x;
     }
-    float erho = 1.0f;
-    if (tid < DK) {
-      erho = exp2f(rho2);
+    const float erho = ex2_approx(rho2);
+    {  // Sh = e^rho S into the MMA_X operand (lane c; warps 0-3 cols 0..15, 4-7 16..31)
+      float s[16];
+      tmem_ld16(tbase + lane_base + TM_S + ch * 16, s);
+      const uint32_t bsh = SH_OFF + (c >> 5) * SH_KB + (c & 3) * 4 + (uint32_t)ch * 2048;
+      const uint32_t xs = (c & 31) >> 2;
 #pragma unroll
-      for (int j = 0; j < TW; ++j) {
-        Sh[j] = erho * S[j];
-        *f32at(sm, SH_OFF + sw128_off32(j, c, SH_KB)) = Sh[j];
-      }
+      for (int j = 0; j < 16; ++j)
+        *f32at(sm, bsh + (uint32_t)(j >> 3) * 1024u + (uint32_t)(j & 7) * 128u +
+                       ((xs ^ (uint32_t)(j & 7)) << 4)) = erho * s[j];
     }
+    tmem_st_wait();
     fence_proxy_async_smem();
     cta_sync();
     // ================= Ph2: A = [Kh; Qh] Kb^T
@@ -289,101 +314,142 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
     }
     if (!mbar_wait(&misc->bar_a, par)) misc->abort = 1;
     tc_fence_after();
-    // ================= Ph3: A_kk -> scratch, A_qk -> operand, then T
+    // ================= Ph3: A_kk -> scratch, A_qk masked in place, then T
     {
       float v[32];
-      const int ch = warp >> 2;
       tmem_ld32(tbase + lane_base + TM_A + ch * 32, v);
       const int R = qd * 32 + lane;
-      if (R < C) {
-        const float br = misc->beta[R];
-        float* Akk = f32at(sm, SCR_A);
+      if (R < C) {  // beta_r A_kk, strictly lower, as 16-byte row segments
+        const float br = bs4[R * 4 + hb];
+        float* arow = f32at(sm, SCR_A) + R * LA + ch * 32;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 32; j += 4) {
           const int i = ch * 32 + j;
-          Akk[R * LA + i] = (i < R) ? br * v[j] : 0.0f;
+          *reinterpret_cast<float4*>(arow + j) =
+              make_float4(i < R ? br * v[j] : 0.0f, i + 1 < R ? br * v[j + 1] : 0.0f,
+                          i + 2 < R ? br * v[j + 2] : 0.0f, i + 3 < R ? br * v[j + 3] : 0.0f);
         }
-      } else if (!pkg) {
+      } else {  // causal A_qk (diagonal included), the MMA_Z operand, rewritten in TMEM
         const int r = R - C;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const int i = ch * 32 + j;
-          *f32at(sm, TQ_OFF + 8192 + sw128_off32(C + r, i, TQ_KB)) = (i <= r) ? v[j] : 0.0f;
-        }
+        for (int j = 0; j < 32; ++j) v[j] = (ch * 32 + j <= r) ? v[j] : 0.0f;
+        tmem_st16(tbase + lane_base + TM_A + ch * 32, v);
+        tmem_st16(tbase + lane_base + TM_A + ch * 32 + 16, v + 16);
+        tmem_st_wait();
       }
     }
+    // beta (needed by every thread of the solve) out of the staging area before it is reused
+    float beta_r = 0.0f;
+    if (tid < C) beta_r = (tid < n) ? bs4[tid * 4 + hb] : 0.0f;
     cta_sync();
     if (misc->abort) { ok = false; break; }
+    float* betas = misc->part[0];  // the scan's partial sums are no longer needed
+    if (tid < C) betas[tid] = beta_r;
+    __syncthreads();
     {
-      float* Akk = f32at(sm, SCR_A);
+      // T = (I + A_kk)^-1 in 16 x 16 blocks; T diag(beta) goes straight into the TB operand.
+      const float* Akk = f32at(sm, SCR_A);
       float* X = f32at(sm, SCR_X);
       float* P = f32at(sm, SCR_P);
-      // diagonal 16 x 16 blocks: lane i of a 16-lane group owns column i of its block
+      // diagonal blocks: lane i of a 16-lane group owns column i of its block; right-looking
+      // substitution (x_l = 0 for l < i, so every update can run unconditionally)
       if (tid < 64) {
         const int blk = tid >> 4, i = tid & 15, I0 = blk * 16;
         float x[16];
 #pragma unroll
+        for (int r = 0; r < 16; ++r) x[r] = (r == i) ? 1.0f : 0.0f;
+#pragma unroll
+        for (int l = 0; l < 15; ++l)
+#pragma unroll
+          for (int r = l + 1; r < 16; ++r) x[r] = fmaf(-Akk[(I0 + r) * LA + I0 + l], x[l], x[r]);
+        const float bi = betas[I0 + i];
+#pragma unroll
         for (int r = 0; r < 16; ++r) {
-          float a = 0.0f;
-#pragma unroll
-          for (int l = 0; l < r; ++l) a = fmaf(Akk[(I0 + r) * LA + I0 + l], x[l], a);
-          x[r] = (r < i) ? 0.0f : (r == i ? 1.0f : -a);
+          X[(I0 + r) * LA + I0 + i] = x[r];
+          *f32at(sm, TB_OFF + sw128_off32(I0 + r, I0 + i, TB_KB)) = x[r] * bi;
         }
-#pragma unroll
-        for (int r = 0; r < 16; ++r) X[(I0 + r) * LA + I0 + i] = x[r];
-      }
-      // blocks above the diagonal are zero
-      for (int e = tid; e < 64 * 64; e += kThreads) {
-        const int r = e >> 6, i = e & 63;
-        if ((i >> 4) > (r >> 4)) X[r * LA + i] = 0.0f;
       }
       __syncthreads();
-      // off-diagonal blocks by distance: X_IJ = -X_II * sum_{L=J}^{I-1} A_IL X_LJ
+      // off-diagonal blocks by distance d: X_IJ = -X_II sum_{L=J}^{I-1} A_IL X_LJ (J = I - d);
+      // a thread computes 4 adjacent columns of one row of one block
       for (int dist = 1; dist < 4; ++dist) {
-        const int nb = 4 - dist;
-        for (int e = tid; e < nb * 256; e += kThreads) {
-          const int b = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-          const int J = b, I = b + dist;
-          float a = 0.0f;
-          for (int L = J; L < I; ++L)
+        const int tasks = (4 - dist) * 64;
+        const int b = tid >> 6, rr = (tid >> 2) & 15, cc = (tid & 3) * 4;
+        const int J = b, I = b + dist;
+        if (tid < tasks) {
+          float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int L = J; L < I; ++L) {
+            const float* arow = Akk + (I * 16 + rr) * LA + L * 16;
 #pragma unroll
-            for (int l = 0; l < 16; ++l)
-              a = fmaf(Akk[(I * 16 + rr) * LA + L * 16 + l], X[(L * 16 + l) * LA + J * 16 + cc],
-                       a);
-          P[b * 256 + rr * 16 + cc] = a;
+            for (int l = 0; l < 16; l += 4) {
+              const float4 av = *reinterpret_cast<const float4*>(arow + l);
+              const float avs[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const float4 xv =
+                    *reinterpret_cast<const float4*>(X + (L * 16 + l + u) * LA + J * 16 + cc);
+                a4.x = fmaf(avs[u], xv.x, a4.x);
+                a4.y = fmaf(avs[u], xv.y, a4.y);
+                a4.z = fmaf(avs[u], xv.z, a4.z);
+                a4.w = fmaf(avs[u], xv.w, a4.w);
+              }
+            }
+          }
+          *reinterpret_cast<float4*>(P + b * 256 + rr * 16 + cc) = a4;
         }
         __syncthreads();
-        for (int e = tid; e < nb * 256; e += kThreads) {
-          const int b = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-          const int J = b, I = b + dist;
-          float a = 0.0f;
+        if (tid < tasks) {
+          float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          const float* xrow = X + (I * 16 + rr) * LA + I * 16;
 #pragma unroll
-          for (int l = 0; l < 16; ++l)
-            a = fmaf(X[(I * 16 + rr) * LA + I * 16 + l], P[b * 256 + l * 16 + cc], a);
-          X[(I * 16 + rr) * LA + J * 16 + cc] = -a;
+          for (int l = 0; l < 16; l += 4) {
+            const float4 xv = *reinterpret_cast<const float4*>(xrow + l);
+            const float xs[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float4 pv = *reinterpret_cast<const float4*>(P + b * 256 + (l + u) * 16 + cc);
+              a4.x = fmaf(xs[u], pv.x, a4.x);
+              a4.y = fmaf(xs[u], pv.y, a4.y);
+              a4.z = fmaf(xs[u], pv.z, a4.z);
+              a4.w = fmaf(xs[u], pv.w, a4.w);
+            }
+          }
+          const float4 xo = make_float4(-a4.x, -a4.y, -a4.z, -a4.w);
+          *reinterpret_cast<float4*>(X + (I * 16 + rr) * LA + J * 16 + cc) = xo;
+          const float* bj = betas + J * 16 + cc;
+          *reinterpret_cast<float4*>(sm + TB_OFF + sw128_off32(I * 16 + rr, J * 16 + cc, TB_KB)) =
+              make_float4(xo.x * bj[0], xo.y * bj[1], xo.z * bj[2], xo.w * bj[3]);
         }
         __syncthreads();
       }
-      // T diag(beta) into the TB operand (K-major: row = token r, K = token i)
-      for (int e = tid; e < C * C; e += kThreads) {
-        const int r = e >> 6, i = e & 63;
-        const float x = (i <= r) ? X[r * LA + i] * misc->beta[i] : 0.0f;
-        *f32at(sm, TQ_OFF + sw128_off32(r, i, TQ_KB)) = x;
+      // TB rows into TMEM (lanes 0..63) as the A operand of MMA_U
+      if (qd < 2 && has_v) {
+        const int r = qd * 32 + lane;
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const float4 t4 =
+              *reinterpret_cast<const float4*>(sm + TB_OFF + sw128_off32(r, ch * 32 + j, TB_KB));
+          v[j] = t4.x; v[j + 1] = t4.y; v[j + 2] = t4.z; v[j + 3] = t4.w;
+        }
+        tmem_st16(tbase + lane_base + TM_TB + ch * 32, v);
+        tmem_st16(tbase + lane_base + TM_TB + ch * 32 + 16, v + 16);
+        tmem_st_wait();
       }
     }
     fence_proxy_async_smem();
     cta_sync();
-    // ================= Ph4: W^T = Kh^T TB^T, Ut = TB V; then prefetch the next chunk
+    // ================= Ph4: W^T = Kh^T TB^T, Ut = TB V; then load the next chunk
     if (tid == 0) {
       const uint32_t idw = idesc_make(kFmtTF32, 128, 64, false, false);
       const uint32_t idu = idesc_make(kFmtTF32, 128, 32, false, false);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const uint64_t tb = sdesc_sw128(sbase + TQ_OFF + (s >> 2) * TQ_KB + (s & 3) * 32, 16, 1024);
+        const uint64_t tb = sdesc_sw128(sbase + TB_OFF + (s >> 2) * TB_KB + (s & 3) * 32, 16, 1024);
         mma_tf32_ts(tbase + TM_WT, tbase + TM_KHT + s * 8, tb, idw, s > 0);
         if (has_v) {
           const uint64_t bv = sdesc_sw128(sbase + VT_OFF + (s >> 2) * VT_KB + (s & 3) * 32, 16, 1024);
-          mma_tf32(tbase + TM_U, tb, bv, idu, s > 0);
+          mma_tf32_ts(tbase + TM_U, tbase + TM_TB + s * 8, bv, idu, s > 0);
         }
       }
       mma_commit(&misc->bar_w);
@@ -395,15 +461,16 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
     }
     if (!mbar_wait(&misc->bar_w, par)) misc->abort = 1;
     tc_fence_after();
-    // ================= Ph5: W into the Kh rows of XA; Ut into registers
+    // ================= Ph5: W into the Kh rows of XA
     {
       float v[32];
-      const int ch = warp >> 2;  // token half
-      tmem_ld32(tbase + lane_base + TM_WT + ch * 32, v);
+      tmem_ld32(tbase + lane_base + TM_WT + ch * 32, v);  // tokens ch*32.., channel c
+      const uint32_t bw = XA_OFF + (c >> 5) * XA_KB + (c & 3) * 4 + (uint32_t)ch * 4096;
+      const uint32_t x32 = (c & 31) >> 2;
 #pragma unroll
       for (int j = 0; j < 32; ++j)
-        *f32at(sm, XA_OFF + sw128_off32(ch * 32 + j, c, XA_KB)) = v[j];
-      if (warp < 2 && has_v) tmem_ld32(tbase + lane_base + TM_U, Ut);
+        *f32at(sm, bw + (uint32_t)(j >> 3) * 1024u + (uint32_t)(j & 7) * 128u +
+                       ((x32 ^ (uint32_t)(j & 7)) << 4)) = v[j];
     }
     fence_proxy_async_smem();
     cta_sync();
@@ -421,12 +488,18 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
     }
     if (!mbar_wait(&misc->bar_x, par)) misc->abort = 1;
     tc_fence_after();
-    if (warp < 2) {  // token rows 0..63: U = Ut - W Sh, stored as U^T (K-major)
-      float x[32];
-      tmem_ld32(tbase + lane_base + TM_X, x);
+    if (qd < 2) {  // token rows 0..63: U = Ut - W Sh (columns 16 ch ..), stored as U^T
+      float x[16], u[16];
+      tmem_ld16(tbase + lane_base + TM_X + ch * 16, x);
+      if (has_v) tmem_ld16(tbase + lane_base + TM_U + ch * 16, u);
+      else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) u[j] = 0.0f;
+      }
       const int r = qd * 32 + lane;
 #pragma unroll
-      for (int j = 0; j < TW; ++j) *f32at(sm, UT_OFF + sw128_off32(j, r, UT_KB)) = Ut[j] - x[j];
+      for (int j = 0; j < 16; ++j)
+        *f32at(sm, UT_OFF + sw128_off32(ch * 16 + j, r, UT_KB)) = u[j] - x[j];
     }
     fence_proxy_async_smem();
     cta_sync();
@@ -438,24 +511,20 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
       for (int s = 0; s < 8; ++s) {
         const uint64_t b = sdesc_sw128(sbase + UT_OFF + (s >> 2) * UT_KB + (s & 3) * 32, 16, 1024);
         mma_tf32_ts(tbase + TM_Y, tbase + TM_KBT + s * 8, b, idy, s > 0);
-        if (!pkg) {
-          const uint64_t az =
-              sdesc_sw128(sbase + TQ_OFF + 8192 + (s >> 2) * TQ_KB + (s & 3) * 32, 16, 1024);
-          mma_tf32(tbase + TM_X, az, b, idy, 1);
-        }
+        if (!pkg) mma_tf32_ts(tbase + TM_X, tbase + TM_A + s * 8, b, idy, 1);
       }
       mma_commit(&misc->bar_y);
     }
     if (!mbar_wait(&misc->bar_y, par)) misc->abort = 1;
     tc_fence_after();
-    if (warp >= 2 && warp < 4 && !pkg && p.o) {  // output rows (Qh rows 64..127)
-      float x[32];
-      tmem_ld32(tbase + lane_base + TM_X, x);
+    if (qd >= 2 && !pkg && p.o) {  // output rows (Qh rows 64..127), 16 columns per warp
+      float x[16];
+      tmem_ld16(tbase + lane_base + TM_X + ch * 16, x);
       const int r = qd * 32 + lane - C;
       if (r < n) {
-        __nv_bfloat16* o = (__nv_bfloat16*)p.o + ((int64_t)(t0 + r) * H + h) * DK + j0;
+        __nv_bfloat16* o = (__nv_bfloat16*)p.o + ((int64_t)(t0 + r) * H + h) * DK + j0 + ch * 16;
 #pragma unroll
-        for (int j = 0; j < TW; j += 8) {
+        for (int j = 0; j < 16; j += 8) {
           uint4 pk;
           __nv_bfloat162 b0 = __floats2bfloat162_rn(p.scale * x[j], p.scale * x[j + 1]);
           __nv_bfloat162 b1 = __floats2bfloat162_rn(p.scale * x[j + 2], p.scale * x[j + 3]);
@@ -469,35 +538,40 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
         }
       }
     }
-    if (tid < DK) {  // state rows: S = e^rho (Sh + Y)
-      float y[32];
-      tmem_ld32(tbase + lane_base + TM_Y, y);
+    {  // state: S = e^(2 rho) S + e^rho Y (lane c; 16 columns per warp)
+      float s[16], y[16];
+      tmem_ld16(tbase + lane_base + TM_S + ch * 16, s);
+      tmem_ld16(tbase + lane_base + TM_Y + ch * 16, y);
 #pragma unroll
-      for (int j = 0; j < TW; ++j) S[j] = erho * (Sh[j] + y[j]);
+      for (int j = 0; j < 16; ++j) s[j] = erho * fmaf(erho, s[j], y[j]);
+      tmem_st16(tbase + lane_base + TM_S + ch * 16, s);
+      tmem_st_wait();
     }
     cta_sync();
     if (misc->abort) { ok = false; break; }
   }
   // ---- exit state of this tile
   if (!ok) {
-    // Let this CTA's in-flight MMAs and prefetch drain (bounded) before its shared memory
-    // and TMEM are released.
+    // Let this CTA's in-flight MMAs and loads drain (bounded) before its shared memory and
+    // TMEM are released.
     if (tid == 0) {
       if (p.status) atomicOr(p.status, KDA_STATUS_TIMEOUT);
       mma_commit(&misc->bar_drain);
       mbar_wait(&misc->bar_drain, 0, 100000000ull);
       if (tma_out) mbar_wait(&misc->bar_tma, tma_par, 100000000ull);
     }
-  } else if (tid < DK) {
+  } else {
+    float s[16];
+    tmem_ld16(tbase + lane_base + TM_S + ch * 16, s);
     const int64_t sh = (int64_t)sidx * H + h;
+    float* dst = nullptr;
+    if (pkg) dst = mcols ? p.M + (sh * DK + c) * DK + j0 : p.D + (sh * DK + c) * DK + vcol0;
+    else if (p.final_state) dst = p.final_state + (sh * DK + c) * DK + j0;
+    if (dst) {
 #pragma unroll
-    for (int j = 0; j < TW; ++j) {
-      if (pkg) {
-        if (mcols) p.M[(sh * DK + tid) * DK + j0 + j] = S[j];
-        else p.D[(sh * DK + tid) * DK + vcol0 + j] = S[j];
-      } else if (p.final_state) {
-        p.final_state[(sh * DK + tid) * DK + j0 + j] = S[j];
-      }
+      for (int j = 0; j < 16; j += 4)
+        *reinterpret_cast<float4*>(dst + ch * 16 + j) =
+            make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
     }
   }
   cta_sync();
@@ -525,36 +599,54 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [T, H, d] bf16 viewed as a 3-D tensor (d, H, T); box (box_d, 1, 64 tokens).
-bool make_map(CUtensorMap* m, const void* ptr, int T, int H, int d, int box_d, bool swizzle) {
+// [T, H, d] (bf16, or fp32 when f32) viewed as a 3-D tensor (d, H, T); box (box_d, 1, 64).
+bool make_map3(CUtensorMap* m, const void* ptr, int T, int H, int d, int box_d, bool swizzle,
+               bool f32) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
+  const cuuint64_t es_bytes = f32 ? 4 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+  cuuint64_t strides[2] = {(cuuint64_t)d * es_bytes, (cuuint64_t)H * d * es_bytes};
   cuuint32_t box[3] = {(cuuint32_t)box_d, 1, (cuuint32_t)C};
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
-                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                   const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// beta [T, H] fp32 as a 2-D tensor (H, T); box (4 heads, 64 tokens).
+bool make_map_beta(CUtensorMap* m, const float* ptr, int T, int H) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)H * 4};
+  cuuint32_t box[2] = {4, (cuuint32_t)C};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 }  // namespace
 
 bool chunk_tc_supported(const ChunkParams& p, kda_dtype dt) {
-  return dt == KDA_BF16 && p.dk == 128 && p.dv == 128 && p.total_tokens > 0 &&
-         encode_fn() != nullptr;
+  return dt == KDA_BF16 && p.dk == 128 && p.dv == 128 && p.total_tokens > 0 && p.H % 4 == 0 &&
+         ((uintptr_t)p.beta % 16) == 0 && encode_fn() != nullptr;
 }
 
 kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, cudaStream_t s) {
   (void)dt;
   if (p.n_ranges == 0) return KDA_OK;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mg, mb;
   const void* qp = p.q ? p.q : p.k;
-  if (!make_map(&mq, qp, p.total_tokens, p.H, 128, 64, true) ||
-      !make_map(&mk, p.k, p.total_tokens, p.H, 128, 64, true) ||
-      !make_map(&mv, p.v, p.total_tokens, p.H, 128, TW, false))
+  if (!make_map3(&mq, qp, p.total_tokens, p.H, 128, 64, true, false) ||
+      !make_map3(&mk, p.k, p.total_tokens, p.H, 128, 64, true, false) ||
+      !make_map3(&mv, p.v, p.total_tokens, p.H, 128, TW, false, false) ||
+      !make_map3(&mg, p.g, p.total_tokens, p.H, 128, 128, false, true) ||
+      !make_map_beta(&mb, p.beta, p.total_tokens, p.H))
     return set_error(KDA_ERR_CUDA, "tensor-core chunk kernel: cuTensorMapEncodeTiled failed");
   cudaError_t e = cudaFuncSetAttribute(chunk_tc_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
@@ -563,7 +655,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, cudaStream_t s) {
                                        cudaGetErrorString(e));
   const int cols = p.package ? (p.dk + p.dv) : p.dv;
   dim3 grid(cols / TW, p.H, p.n_ranges);
-  chunk_tc_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(p, mq, mk, mv);
+  chunk_tc_kernel<<<grid, kThreads, SMEM_BYTES, s>>>(p, mq, mk, mv, mg, mb);
   count_launches(1);
   return check_launch("tensor-core chunk kernel");
 }
