@@ -100,6 +100,26 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(vals):
+    """Element-wise maximum of a list of floats over all ranks (identity on one rank). The
+    job's time is its slowest rank's time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in vals]
+    t = torch.tensor([float(v) for v in vals], dtype=torch.float64)
+    if dist.get_backend() == "nccl":
+        t = t.cuda()
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu().tolist()]
+
+
+def weak_scaling_value(units_per_rank, world, ms):
+    """Whole-job throughput when every rank processes `units_per_rank` units (replicas):
+    all ranks' units over the slowest rank's time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
 def run_gb300(args):
     import torch
     import torch.distributed as dist
@@ -179,12 +199,10 @@ def run_gb300(args):
     launches = kda.launch_count() - launches0
     total_ms = step_ev[0].elapsed_time(step_ev[1])
     comp_ms = {n: sum(a.elapsed_time(b) for a, b in ev[n]) / args.steps for n, _ in parts}
-    if world > 1:
-        t = torch.tensor([total_ms] + [comp_ms[n] for n, _ in parts], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t[0])
-        for i, (n, _) in enumerate(parts):
-            comp_ms[n] = float(t[1 + i])
+    red = max_over_ranks([total_ms] + [comp_ms[n] for n, _ in parts])
+    total_ms = red[0]
+    for i, (n, _) in enumerate(parts):
+        comp_ms[n] = red[1 + i]
     comp_ms["segments_8x2048"] = (comp_ms["seg_package"] + comp_ms["seg_scan"] +
                                   comp_ms["seg_replay"])
 
@@ -243,16 +261,13 @@ def run_gb300(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t[0])
+    e2e_ms = max_over_ranks([e2e_ms])[0]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_heads)
 
-    value = world * T / (comps["prefill_16k"]["ms"] * 1e-3)
+    value = weak_scaling_value(T, world, comps["prefill_16k"]["ms"])
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 4),
@@ -267,7 +282,7 @@ def run_gb300(args):
         "components": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
                            for kk, vv in v.items()} for k, v in comps.items()},
         "roofline": roofline,
-        "e2e": {"value": round(world * T / (e2e_ms * 1e-3), 1), "unit": UNIT,
+        "e2e": {"value": round(weak_scaling_value(T, world, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "what": "kda_chunk_prefill with pinned host inputs copied in and o/final state "
                         "copied out every step"},

@@ -11,10 +11,13 @@
 //   * down-sweep: at stride d, (a[i-d], a[i]) <- (a[i], a[i-d] o a[i]);
 //   * leaf j then holds the exclusive prefix (M_<j, D_<j), and the segment's entry state is
 //     M_<j S_init + D_<j.
-// Every combine is a dk x dk times dk x (dk + dv) product. A CTA computes a 32-row block of
-// one combine's result: it reads only its own rows of the left operand, so the left
-// operand's storage can receive the result in place.
+// Every combine is a dk x dk times dk x (dk + dv) product. For dk = dv = 128 the combines and
+// the entry-state applications run on tcgen05 tensor cores with a 3xTF32 split (namespace tc
+// below). The CUDA-core version (dk = 64) has a CTA compute a 32-row block of one combine's
+// result: it reads only its own rows of the left operand, so that storage can take the
+// result in place.
 #include "kda_internal.cuh"
+#include "ptx.cuh"
 
 namespace kda {
 namespace {
@@ -181,10 +184,220 @@ __global__ void __launch_bounds__(kThreads) scan_apply(Tree t, const int32_t* se
   apply_rows<DK, DV>(t.node(s, j, h), si, seg_init + ((int64_t)(first + j) * t.H + h) * sd, r0);
 }
 
+// ------------------------------------------------------------------ tensor-core combines
+// For dk = dv = 128 the combines run on tcgen05: a CTA computes one 64-column tile of
+// out = A o B = (A.M B.M, A.M B.D + A.D) (or of a prefix applied to an entry state,
+// out.D = A.M S + A.D). A.M is the K-major A operand (128 x 128); the tile of [B.M | B.D] is
+// staged transposed as the K-major B operand (64 x 128); the product accumulates in TMEM.
+// Every product is split 3xTF32 to keep fp32-level accuracy through the tree's levels:
+//   X = X_hi + X_lo, X_hi = X with its low 13 mantissa bits cleared (what a tf32 MMA reads),
+//   X_lo = X - X_hi (exact); A B ~ A_hi B_hi + A_hi B_lo + A_lo B_hi  (error ~ 2^-21 rel.).
+// A combine's result goes to a separate node (tmp) because every tile CTA reads all of A.
+namespace tc {
+
+using namespace ptx;
+
+constexpr int DK = 128;
+constexpr int NT = 64;                          // output columns per CTA
+constexpr uint32_t A_KB = 128 * 128;            // A operand K-block: 128 rows x 128 B
+constexpr uint32_t B_KB = NT * 128;             // B operand K-block: 64 rows x 128 B
+constexpr uint32_t AH = 0, AL = 4 * A_KB, BH = 8 * A_KB, BL = 8 * A_KB + 4 * B_KB;
+constexpr uint32_t SMEM = BL + 4 * B_KB + 1024;  // + alignment slack
+
+__device__ __forceinline__ float hi(float x) {
+  return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
+// One 64-column tile (tile < 2: M columns, else D columns) of A o B. bm may be null (state
+// application: D tiles only). Whole-CTA function (256 threads).
+__device__ void combine_tile(const float* A, const float* bm, const float* bd, float* om,
+                             float* od, int tile, uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tslot;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool mtile = tile < DK / NT;
+  const int col0 = (mtile ? tile : tile - DK / NT) * NT;
+  const float* B = mtile ? bm : bd;  // [128 (k)][128 (n)] row-major
+  float* out = mtile ? om : od;
+  if (warp == 0) {
+    tmem_alloc(&tslot, NT);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  for (int e = tid; e < 128 * 32; e += blockDim.x) {  // A.M -> hi / lo, K-major [r][k]
+    const int r = e >> 5, k4 = (e & 31) * 4;
+    const float4 a = *reinterpret_cast<const float4*>(A + r * DK + k4);
+    const float4 h = make_float4(hi(a.x), hi(a.y), hi(a.z), hi(a.w));
+    const uint32_t off = sw128_off32(r, k4, A_KB);
+    *reinterpret_cast<float4*>(sm + AH + off) = h;
+    *reinterpret_cast<float4*>(sm + AL + off) =
+        make_float4(a.x - h.x, a.y - h.y, a.z - h.z, a.w - h.w);
+  }
+  for (int e = tid; e < 128 * (NT / 4); e += blockDim.x) {  // B tile, transposed
+    const int k = e / (NT / 4), n4 = (e % (NT / 4)) * 4;
+    const float4 b = *reinterpret_cast<const float4*>(B + k * DK + col0 + n4);
+    const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t off = sw128_off32(n4 + u, k, B_KB);
+      const float h = hi(bv[u]);
+      *reinterpret_cast<float*>(sm + BH + off) = h;
+      *reinterpret_cast<float*>(sm + BL + off) = bv[u] - h;
+    }
+  }
+  fence_proxy_async_smem();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tslot;
+  if (tid == 0) {
+    const uint32_t sb = smem_u32(sm);
+    const uint32_t idesc = idesc_make(kFmtTF32, 128, NT, false, false);
+#pragma unroll 1
+    for (int s = 0; s < 16; ++s) {
+      const uint32_t ka = (s >> 2) * A_KB + (s & 3) * 32, kb = (s >> 2) * B_KB + (s & 3) * 32;
+      const uint64_t ah = sdesc_sw128(sb + AH + ka, 16, 1024);
+      const uint64_t al = sdesc_sw128(sb + AL + ka, 16, 1024);
+      const uint64_t bh = sdesc_sw128(sb + BH + kb, 16, 1024);
+      const uint64_t bl = sdesc_sw128(sb + BL + kb, 16, 1024);
+      mma_tf32(tbase, ah, bh, idesc, s > 0 ? 1u : 0u);
+      mma_tf32(tbase, ah, bl, idesc, 1);
+      mma_tf32(tbase, al, bh, idesc, 1);
+    }
+    mma_commit(&bar);
+  }
+  const bool ok = mbar_wait(&bar, 0);
+  if (!ok && tid == 0 && status) atomicOr(status, KDA_STATUS_TIMEOUT);
+  tc_fence_after();
+  {  // warp w: lanes 32 (w % 4).. (rows), columns 32 (w / 4)..; D tiles add A.D
+    const int r = (warp & 3) * 32 + lane, cb = (warp >> 2) * 32;
+    float v[32];
+    tmem_ld32(tbase + ((uint32_t)((warp & 3) * 32) << 16) + cb, v);
+    if (ok) {
+      const float* ad = A + DK * DK + r * DK + col0 + cb;
+      float* dst = out + r * DK + col0 + cb;
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        float4 x = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        if (!mtile) {
+          const float4 a = *reinterpret_cast<const float4*>(ad + j);
+          x.x += a.x; x.y += a.y; x.z += a.z; x.w += a.w;
+        }
+        *reinterpret_cast<float4*>(dst + j) = x;
+      }
+    }
+  }
+  if (!ok && tid == 0) {  // let the MMAs drain (bounded) before the TMEM is released
+    mbar_wait(&bar, 0, 100000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tbase, NT);
+}
+
+// MODE 0: up-sweep at stride d: tmp[pair] = a[i] o a[i-d]
+// MODE 1: down-sweep at stride d: tmp[pair] = a[i-d] o a[i]
+// MODE 2: exit state: final[s] = root applied to init[s]
+// MODE 3: entry states: seg_init[first + j] = a[j] applied to init[s]
+template <int MODE>
+__global__ void __launch_bounds__(256, 1)
+scan_tc(Tree t, int d, const int32_t* seq_off, const float* init, float* outp,
+        uint32_t* status) {
+  const int tile = blockIdx.x, idx = blockIdx.y;
+  const int s = blockIdx.z / t.H, h = blockIdx.z % t.H;
+  const int64_t sd = (int64_t)DK * DK;
+  if (MODE <= 1) {
+    const int i = (2 * idx + 2) * d - 1;
+    const float* A = t.node(s, MODE == 0 ? i : i - d, h);
+    const float* B = t.node(s, MODE == 0 ? i - d : i, h);
+    float* o = t.tnode(s, idx, h);
+    combine_tile(A, B, B + sd, o, o + sd, tile, status);
+  } else if (MODE == 2) {
+    combine_tile(t.node(s, t.P2 - 1, h), nullptr, init + ((int64_t)s * t.H + h) * sd, nullptr,
+                 outp + ((int64_t)s * t.H + h) * sd, tile + DK / NT, status);
+  } else {
+    int first, cnt;
+    t.seq_range(seq_off, s, first, cnt);
+    if (idx >= cnt) return;  // whole CTA
+    combine_tile(t.node(s, idx, h), nullptr, init + ((int64_t)s * t.H + h) * sd, nullptr,
+                 outp + ((int64_t)(first + idx) * t.H + h) * sd, tile + DK / NT, status);
+  }
+}
+
+// a[i] <- tmp[pair] after an up-sweep level
+__global__ void scan_up_move(Tree t, int d) {
+  const int pair = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  const int i = (2 * pair + 2) * d - 1;
+  float4* R = reinterpret_cast<float4*>(t.node(s, i, h));
+  const float4* X = reinterpret_cast<const float4*>(t.tnode(s, pair, h));
+  const int64_t n = pkg_floats(t.dk, t.dv) / 4;
+  for (int64_t e = threadIdx.x; e < n; e += blockDim.x) R[e] = X[e];
+}
+
+}  // namespace tc
+
 int next_pow2(int x) {
   int p = 1;
   while (p < x) p <<= 1;
   return p;
+}
+
+// dk = dv = 128 on tensor cores. Same tree and same kernels for fill / reset / copies.
+kda_status run_tc(int n_seqs, int n_segs, const int32_t* seq_off, int max_segs, int H,
+                  const float* M, const float* D, const float* init, float* seg_init,
+                  float* final_state, void* ws, uint32_t* status, cudaStream_t s) {
+  constexpr int DK = 128, DV = 128;
+  Tree t;
+  t.P2 = next_pow2(max_segs);
+  t.H = H;
+  t.dk = DK;
+  t.dv = DV;
+  t.n_segs = n_segs;
+  t.base = (float*)ws;
+  t.tmp = t.base + (int64_t)n_seqs * t.P2 * H * pkg_floats(DK, DV);
+  const int rb = DK / kRows;
+  const unsigned zh = (unsigned)(n_seqs * H);
+  const int smem = (int)tc::SMEM;
+  cudaFuncSetAttribute(tc::scan_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaFuncSetAttribute(tc::scan_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaFuncSetAttribute(tc::scan_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaFuncSetAttribute(tc::scan_tc<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  int launches = 0;
+  scan_fill<<<dim3(t.P2, H, n_seqs), kThreads, 0, s>>>(t, M, D, seq_off, status);
+  ++launches;
+  for (int d = 1; d < t.P2; d <<= 1) {
+    tc::scan_tc<0><<<dim3(4, t.P2 / (2 * d), zh), 256, smem, s>>>(t, d, seq_off, init, nullptr,
+                                                                  status);
+    tc::scan_up_move<<<dim3(t.P2 / (2 * d), H, n_seqs), kThreads, 0, s>>>(t, d);
+    launches += 2;
+  }
+  if (final_state && init) {
+    tc::scan_tc<2><<<dim3(2, 1, zh), 256, smem, s>>>(t, 0, seq_off, init, final_state, status);
+    ++launches;
+  }
+  // reset the root to (I, 0); without an entry state the exit state is the root's D
+  scan_root<DK, DV><<<dim3(1, H * rb, n_seqs), kThreads, 0, s>>>(
+      t, nullptr, init ? nullptr : final_state);
+  ++launches;
+  for (int d = t.P2 / 2; d >= 1; d >>= 1) {
+    tc::scan_tc<1><<<dim3(4, t.P2 / (2 * d), zh), 256, smem, s>>>(t, d, seq_off, init, nullptr,
+                                                                  status);
+    scan_down_move<<<dim3(t.P2 / (2 * d), H, n_seqs), kThreads, 0, s>>>(t, d);
+    launches += 2;
+  }
+  if (init)
+    tc::scan_tc<3><<<dim3(2, t.P2, zh), 256, smem, s>>>(t, 0, seq_off, init, seg_init, status);
+  else
+    scan_apply<DK, DV><<<dim3(t.P2, H * rb, n_seqs), kThreads, 0, s>>>(t, seq_off, nullptr,
+                                                                        seg_init);
+  ++launches;
+  count_launches(launches);
+  return check_launch("kda_package_scan (tensor cores)");
 }
 
 template <int DK, int DV>
@@ -231,6 +444,9 @@ kda_status launch_scan(int n_seqs, int n_segs, const int32_t* seq_seg_offsets, i
                        void* ws, size_t ws_bytes, uint32_t* status, cudaStream_t s) {
   (void)ws_bytes;
   if (n_seqs == 0) return KDA_OK;
+  if (dk == 128 && dv == 128 && (int64_t)n_seqs * H <= 65535)
+    return run_tc(n_seqs, n_segs, seq_seg_offsets, max_segs, H, M, D, init_state, seg_init,
+                  final_state, ws, status, s);
   if (dk == 128 && dv == 128)
     return run<128, 128>(n_seqs, n_segs, seq_seg_offsets, max_segs, H, M, D, init_state, seg_init,
                          final_state, ws, status, s);
