@@ -4,20 +4,19 @@
 // Chunk algebra (64-token chunk, state S_0 entering it, log-midpoint frame; the same algebra
 // as the CUDA-core kernel in kda_chunk_simt.cu, which states it in full):
 //   gamma = cumsum(g), rho = gamma_C / 2, Kh = k e^(gamma-rho), Qh = q e^(gamma-rho),
-//   Kb = k e^(rho-gamma), Sh = e^rho S_0
-//   A    = [Kh; Qh] Kb^T                       (MMA_A: M 128, N 64, K = dk)
-//   T    = (I + strict_lower(beta_r A_kk))^-1  (CUDA cores, blocked 16 x 16), TB = T diag(beta)
-//   W^T  = Kh^T TB^T                           (MMA_W: A = Kh^T from TMEM, M = dk, N 64)
-//   Ut   = TB V                                (MMA_U: A = TB from TMEM, N 32, K = 64 tokens)
-//   X    = [W; Qh] Sh                          (MMA_X: N 32, K = dk)
-//   U    = Ut - X[0:64]
-//   O    = X[64:128] + tril(A_qk) U            (MMA_Z: A = masked A from TMEM, into X)
-//   Y    = Kb^T U                              (MMA_Y: A = Kb^T from TMEM, M = dk, N 32)
-//   S_C  = e^rho (Sh + Y) = e^(2 rho) S_0 + e^rho Y
-// Every MMA is kind::tf32 with fp32 accumulation in TMEM, and every shared-memory operand is
-// K-major in the 128-byte swizzle (tf32 operands read MN-major came back as zeros on this
-// part); operands that would need the other orientation are staged in TMEM instead, by the
-// threads that produce them. tf32 throughout holds the fp32 state within a few 1e-3 of the
+//   Kb = k e^(rho-gamma), Sh = e^rho S_0, T = (I + strict_lower(beta_r Kh Kb^T))^-1
+//   U   = T diag(beta) V - T diag(beta) Kh Sh = TB (V - Kh Sh)           (TB = T diag(beta))
+//   O   = Qh Sh + tril(Qh Kb^T) U,    S_C = e^rho (Sh + Kb^T U)
+// Forming V - Kh Sh in fp32 before the product with TB (instead of subtracting two separately
+// rounded products TB V and (TB Kh) Sh) both removes a product and avoids cancellation.
+// Per chunk, three tensor-core rounds (all kind::tf32, fp32 accumulation in TMEM):
+//   round 1: A = [Kh; Qh] Kb^T (M 128, N 64, K = dk) and X = [Kh; Qh] Sh (M 128, N 32)
+//   round 2: U = TB (V - X[0:64])                  (A = TB from TMEM, K = 64 tokens)
+//   round 3: Y = Kb^T U  (A = Kb^T from TMEM)  and  X[64:128] += tril(A_qk) U  (A from TMEM)
+// with the T solve (CUDA cores, blocked 16 x 16) between rounds 1 and 2. Every shared-memory
+// operand is K-major in the 128-byte swizzle (tf32 operands read MN-major came back as zeros
+// on this part); operands needed in the other orientation are staged in TMEM by the threads
+// that produce them. tf32 throughout holds the fp32 state within a few 1e-3 of the
 // double-precision recurrence; bf16 operands for the state-touching products would not
 // (measured by emulation against the oracle).
 //
@@ -46,13 +45,11 @@ constexpr int TW = 32;        // state columns per CTA
 constexpr int kThreads = 256;
 
 // shared-memory map (byte offsets from a 1024-byte aligned base)
-constexpr uint32_t XA_OFF = 0;                    // [128 rows][128] fp32: [Kh | W ; Qh]
+constexpr uint32_t XA_OFF = 0;                    // [128 rows][128] fp32: [Kh ; Qh]
 constexpr uint32_t XA_KB = 128 * 128;             //   K-blocks (32 columns) of 16 KiB
 constexpr uint32_t KB_OFF = XA_OFF + 4 * XA_KB;   // [64 rows][128] fp32: Kb
 constexpr uint32_t KB_KB = 64 * 128;
-constexpr uint32_t TB_OFF = KB_OFF + 4 * KB_KB;   // [64 rows][64] fp32: T diag(beta)
-constexpr uint32_t TB_KB = 64 * 128;
-constexpr uint32_t VT_OFF = TB_OFF + 2 * TB_KB;   // [32 cols][64 tokens] fp32: V^T
+constexpr uint32_t VT_OFF = KB_OFF + 4 * KB_KB;   // [32 cols][64 tokens] fp32: (V - Kh Sh)^T
 constexpr uint32_t VT_KB = 32 * 128;
 constexpr uint32_t UT_OFF = VT_OFF + 2 * VT_KB;   // [32 cols][64 tokens] fp32: U^T
 constexpr uint32_t UT_KB = 32 * 128;
@@ -70,31 +67,31 @@ constexpr uint32_t SMEM_BYTES = MISC_OFF + 2048 + 1024;  // + alignment slack
 
 // T-solve scratch inside the staging area (q, k, v and g are consumed by then; the next
 // chunk's loads are issued after the solve). Rows padded to 68 floats: 16-byte aligned rows
-// whose banks shift by 4 per row.
+// whose banks shift by 4 per row. SCR_A does not overlap the value staging, SCR_X does.
 constexpr int LA = 68;
 constexpr uint32_t SCR_A = STG_OFF;                    // beta_r A_kk [64][68] fp32
 constexpr uint32_t SCR_X = STG_OFF + 64 * LA * 4;      // X = (I + A_kk)^-1 [64][68]
 constexpr uint32_t SCR_P = STG_OFF + 2 * 64 * LA * 4;  // 3 x [16][16] partial products
 static_assert(SCR_P + 3 * 256 * 4 <= STG_B, "scratch overflow");
+static_assert(SCR_A + 64 * LA * 4 <= STG_V, "A_kk scratch must not overlap the value tile");
 
 // TMEM columns (512 allocated)
 constexpr uint32_t TM_A = 0;      // 64: [Kh; Qh] Kb^T; lanes 64..127 masked to tril(A_qk)
-constexpr uint32_t TM_WT = 64;    // 64: W^T (lanes = key channels)
-constexpr uint32_t TM_U = 128;    // 32: Ut (lanes 0..63 = tokens)
-constexpr uint32_t TM_X = 160;    // 32: X, then O in lanes 64..127
-constexpr uint32_t TM_Y = 192;    // 32: Y (lanes = key channels)
-constexpr uint32_t TM_KHT = 224;  // 64: Kh^T operand (lanes = key channels, columns = tokens)
-constexpr uint32_t TM_KBT = 288;  // 64: Kb^T operand
-constexpr uint32_t TM_TB = 352;   // 64: TB operand (lanes 0..63 = tokens; 64..127 zero)
-constexpr uint32_t TM_S = 416;    // 32: state tile (lanes = key channels)
+constexpr uint32_t TM_X = 64;     // 32: [Kh; Qh] Sh, then O in lanes 64..127
+constexpr uint32_t TM_U = 96;     // 32: U (lanes 0..63 = tokens)
+constexpr uint32_t TM_Y = 128;    // 32: Kb^T U (lanes = key channels)
+constexpr uint32_t TM_KBT = 160;  // 64: Kb^T operand (lanes = key channels, columns = tokens)
+constexpr uint32_t TM_TB = 224;   // 64: TB operand (lanes 0..63 = tokens; 64..127 zero)
+constexpr uint32_t TM_S = 288;    // 32: state tile (lanes = key channels)
 
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Misc {
-  uint64_t bar_tma, bar_a, bar_w, bar_x, bar_y, bar_drain;
+  uint64_t bar_tma, bar_1, bar_2, bar_3, bar_drain;
   uint32_t tmem_base;
   int abort;
   float part[2][DK];
+  float beta[C];
 };
 
 __device__ __forceinline__ void cta_sync() {
@@ -152,10 +149,9 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
   }
   if (tid == 0) {
     mbar_init(&misc->bar_tma, 1);
-    mbar_init(&misc->bar_a, 1);
-    mbar_init(&misc->bar_w, 1);
-    mbar_init(&misc->bar_x, 1);
-    mbar_init(&misc->bar_y, 1);
+    mbar_init(&misc->bar_1, 1);
+    mbar_init(&misc->bar_2, 1);
+    mbar_init(&misc->bar_3, 1);
     mbar_init(&misc->bar_drain, 1);
     misc->abort = 0;
     fence_mbar_init();
@@ -165,8 +161,6 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
     tma_prefetch_desc(&tmb);
     if (!pkg) tma_prefetch_desc(&tmq);
   }
-  // TB: blocks above the diagonal stay zero; the solve rewrites the rest every chunk
-  for (uint32_t e = tid; e < 2 * 2048; e += kThreads) f32at(sm, TB_OFF)[e] = 0.0f;
   if (pkg) {  // no queries: the Qh rows stay zero
     for (uint32_t e = tid; e < 4 * 2048; e += kThreads) {
       const uint32_t kb = e >> 11, w = e & 2047;
@@ -238,6 +232,7 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
       acc += gl[i];
     }
     misc->part[half][c] = acc;
+    if (tid < C) misc->beta[tid] = (tid < n) ? bs4[tid * 4 + hb] : 0.0f;
     __syncthreads();
     if (misc->abort) { ok = false; break; }
     const float p0 = misc->part[0][c], p1 = misc->part[1][c];
@@ -255,7 +250,7 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
       float gam = half ? p0 : 0.0f;
 #pragma unroll
       for (int blk = 0; blk < 2; ++blk) {
-        float kh[16], kb[16];
+        float kb[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int t = blk * 16 + i;
@@ -269,26 +264,18 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
             kv = bf16at(sm, o16);
             if (!pkg) qv = bf16at(sm, o16 - (STG_K - STG_Q));
           }
-          kh[i] = kv * e1;
           kb[i] = kv * e2;
           const uint32_t sw = row + ((x32 ^ (uint32_t)(t & 7)) << 4);
-          *f32at(sm, bxa + sw) = kh[i];
+          *f32at(sm, bxa + sw) = kv * e1;
           if (!pkg) *f32at(sm, bxa + 8192 + sw) = qv * e1;
           *f32at(sm, bkb + sw) = kb[i];
         }
-        // Kh^T and Kb^T as TMEM operands: lane = channel c, column = token
-        tmem_st16(tbase + lane_base + TM_KHT + half * 32 + blk * 16, kh);
+        // Kb^T as the TMEM operand of round 3: lane = channel c, column = token
         tmem_st16(tbase + lane_base + TM_KBT + half * 32 + blk * 16, kb);
       }
     }
-    for (int e = tid; e < C * TW; e += kThreads) {  // V^T: row = value column, K = token
-      const int j = e >> 6, r = e & 63;
-      float x = 0.0f;
-      if (r < n && has_v) x = bf16at(sm, STG_V + r * 64 + j * 2);
-      *f32at(sm, VT_OFF + sw128_off32(j, r, VT_KB)) = x;
-    }
     const float erho = ex2_approx(rho2);
-    {  // Sh = e^rho S into the MMA_X operand (lane c; warps 0-3 cols 0..15, 4-7 16..31)
+    {  // Sh = e^rho S into the round-1 operand (lane c; warps 0-3 cols 0..15, 4-7 16..31)
       float s[16];
       tmem_ld16(tbase + lane_base + TM_S + ch * 16, s);
       const uint32_t bsh = SH_OFF + (c >> 5) * SH_KB + (c & 3) * 4 + (uint32_t)ch * 2048;
@@ -301,26 +288,29 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
     tmem_st_wait();
     fence_proxy_async_smem();
     cta_sync();
-    // ================= Ph2: A = [Kh; Qh] Kb^T
+    // ================= round 1: A = [Kh; Qh] Kb^T, X = [Kh; Qh] Sh
     if (tid == 0) {
-      const uint32_t idesc = idesc_make(kFmtTF32, 128, 64, false, false);
+      const uint32_t ida = idesc_make(kFmtTF32, 128, 64, false, false);
+      const uint32_t idx = idesc_make(kFmtTF32, 128, 32, false, false);
 #pragma unroll
       for (int s = 0; s < 16; ++s) {
         const uint64_t a = sdesc_sw128(sbase + XA_OFF + (s >> 2) * XA_KB + (s & 3) * 32, 16, 1024);
         const uint64_t b = sdesc_sw128(sbase + KB_OFF + (s >> 2) * KB_KB + (s & 3) * 32, 16, 1024);
-        mma_tf32(tbase + TM_A, a, b, idesc, s > 0);
+        const uint64_t bs = sdesc_sw128(sbase + SH_OFF + (s >> 2) * SH_KB + (s & 3) * 32, 16, 1024);
+        mma_tf32(tbase + TM_A, a, b, ida, s > 0);
+        mma_tf32(tbase + TM_X, a, bs, idx, s > 0);
       }
-      mma_commit(&misc->bar_a);
+      mma_commit(&misc->bar_1);
     }
-    if (!mbar_wait(&misc->bar_a, par)) misc->abort = 1;
+    if (!mbar_wait(&misc->bar_1, par)) misc->abort = 1;
     tc_fence_after();
-    // ================= Ph3: A_kk -> scratch, A_qk masked in place, then T
+    // ================= Ph3: A_kk -> scratch, A_qk masked in place, V - Kh Sh -> operand
     {
       float v[32];
       tmem_ld32(tbase + lane_base + TM_A + ch * 32, v);
       const int R = qd * 32 + lane;
       if (R < C) {  // beta_r A_kk, strictly lower, as 16-byte row segments
-        const float br = bs4[R * 4 + hb];
+        const float br = misc->beta[R];
         float* arow = f32at(sm, SCR_A) + R * LA + ch * 32;
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
@@ -329,7 +319,16 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
               make_float4(i < R ? br * v[j] : 0.0f, i + 1 < R ? br * v[j + 1] : 0.0f,
                           i + 2 < R ? br * v[j + 2] : 0.0f, i + 3 < R ? br * v[j + 3] : 0.0f);
         }
-      } else {  // causal A_qk (diagonal included), the MMA_Z operand, rewritten in TMEM
+        // (V - Kh Sh) for token R, 16 value columns per warp, stored transposed (K = token)
+        float x[16];
+        tmem_ld16(tbase + lane_base + TM_X + ch * 16, x);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int col = ch * 16 + j;
+          const float vv = (R < n && has_v) ? bf16at(sm, STG_V + R * 64 + col * 2) : 0.0f;
+          *f32at(sm, VT_OFF + sw128_off32(col, R, VT_KB)) = vv - x[j];
+        }
+      } else {  // causal A_qk (diagonal included), the round-3 operand, rewritten in TMEM
         const int r = R - C;
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = (ch * 32 + j <= r) ? v[j] : 0.0f;
@@ -338,16 +337,10 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
         tmem_st_wait();
       }
     }
-    // beta (needed by every thread of the solve) out of the staging area before it is reused
-    float beta_r = 0.0f;
-    if (tid < C) beta_r = (tid < n) ? bs4[tid * 4 + hb] : 0.0f;
     cta_sync();
     if (misc->abort) { ok = false; break; }
-    float* betas = misc->part[0];  // the scan's partial sums are no longer needed
-    if (tid < C) betas[tid] = beta_r;
-    __syncthreads();
     {
-      // T = (I + A_kk)^-1 in 16 x 16 blocks; T diag(beta) goes straight into the TB operand.
+      // T = (I + A_kk)^-1 in 16 x 16 blocks
       const float* Akk = f32at(sm, SCR_A);
       float* X = f32at(sm, SCR_X);
       float* P = f32at(sm, SCR_P);
@@ -362,11 +355,15 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
         for (int l = 0; l < 15; ++l)
 #pragma unroll
           for (int r = l + 1; r < 16; ++r) x[r] = fmaf(-Akk[(I0 + r) * LA + I0 + l], x[l], x[r]);
-        const float bi = betas[I0 + i];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-          X[(I0 + r) * LA + I0 + i] = x[r];
-          *f32at(sm, TB_OFF + sw128_off32(I0 + r, I0 + i, TB_KB)) = x[r] * bi;
+        for (int r = 0; r < 16; ++r) X[(I0 + r) * LA + I0 + i] = x[r];
+      } else {
+        // blocks above the diagonal are zero (read by the TB copy below)
+        for (int e = tid - 64; e < 6 * 256; e += kThreads - 64) {
+          const int b = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+          const int I = b < 3 ? 0 : (b < 5 ? 1 : 2);
+          const int J = b < 3 ? b + 1 : (b < 5 ? b - 1 : 3);
+          X[(I * 16 + rr) * LA + J * 16 + cc] = 0.0f;
         }
       }
       __syncthreads();
@@ -414,23 +411,24 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
               a4.w = fmaf(xs[u], pv.w, a4.w);
             }
           }
-          const float4 xo = make_float4(-a4.x, -a4.y, -a4.z, -a4.w);
-          *reinterpret_cast<float4*>(X + (I * 16 + rr) * LA + J * 16 + cc) = xo;
-          const float* bj = betas + J * 16 + cc;
-          *reinterpret_cast<float4*>(sm + TB_OFF + sw128_off32(I * 16 + rr, J * 16 + cc, TB_KB)) =
-              make_float4(xo.x * bj[0], xo.y * bj[1], xo.z * bj[2], xo.w * bj[3]);
+          *reinterpret_cast<float4*>(X + (I * 16 + rr) * LA + J * 16 + cc) =
+              make_float4(-a4.x, -a4.y, -a4.z, -a4.w);
         }
         __syncthreads();
       }
-      // TB rows into TMEM (lanes 0..63) as the A operand of MMA_U
-      if (qd < 2 && has_v) {
+      // TB = T diag(beta) into TMEM lanes 0..63 (the round-2 A operand)
+      if (qd < 2) {
         const int r = qd * 32 + lane;
+        const float* xrow = X + r * LA + ch * 32;
+        const float* bt = misc->beta + ch * 32;
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; j += 4) {
-          const float4 t4 =
-              *reinterpret_cast<const float4*>(sm + TB_OFF + sw128_off32(r, ch * 32 + j, TB_KB));
-          v[j] = t4.x; v[j + 1] = t4.y; v[j + 2] = t4.z; v[j + 3] = t4.w;
+          const float4 t4 = *reinterpret_cast<const float4*>(xrow + j);
+          v[j] = t4.x * bt[j];
+          v[j + 1] = t4.y * bt[j + 1];
+          v[j + 2] = t4.z * bt[j + 2];
+          v[j + 3] = t4.w * bt[j + 3];
         }
         tmem_st16(tbase + lane_base + TM_TB + ch * 32, v);
         tmem_st16(tbase + lane_base + TM_TB + ch * 32 + 16, v + 16);
@@ -439,72 +437,34 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
     }
     fence_proxy_async_smem();
     cta_sync();
-    // ================= Ph4: W^T = Kh^T TB^T, Ut = TB V; then load the next chunk
+    // ================= round 2: U = TB (V - Kh Sh); then load the next chunk
     if (tid == 0) {
-      const uint32_t idw = idesc_make(kFmtTF32, 128, 64, false, false);
       const uint32_t idu = idesc_make(kFmtTF32, 128, 32, false, false);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const uint64_t tb = sdesc_sw128(sbase + TB_OFF + (s >> 2) * TB_KB + (s & 3) * 32, 16, 1024);
-        mma_tf32_ts(tbase + TM_WT, tbase + TM_KHT + s * 8, tb, idw, s > 0);
-        if (has_v) {
-          const uint64_t bv = sdesc_sw128(sbase + VT_OFF + (s >> 2) * VT_KB + (s & 3) * 32, 16, 1024);
-          mma_tf32_ts(tbase + TM_U, tbase + TM_TB + s * 8, bv, idu, s > 0);
-        }
+        const uint64_t bv = sdesc_sw128(sbase + VT_OFF + (s >> 2) * VT_KB + (s & 3) * 32, 16, 1024);
+        mma_tf32_ts(tbase + TM_U, tbase + TM_TB + s * 8, bv, idu, s > 0);
       }
-      mma_commit(&misc->bar_w);
+      mma_commit(&misc->bar_2);
       if (t0 + C < t_end) {
         issue_tma(t0 + C);
         tma_out = true;
         tma_par = (it + 1) & 1u;
       }
     }
-    if (!mbar_wait(&misc->bar_w, par)) misc->abort = 1;
+    if (!mbar_wait(&misc->bar_2, par)) misc->abort = 1;
     tc_fence_after();
-    // ================= Ph5: W into the Kh rows of XA
-    {
-      float v[32];
-      tmem_ld32(tbase + lane_base + TM_WT + ch * 32, v);  // tokens ch*32.., channel c
-      const uint32_t bw = XA_OFF + (c >> 5) * XA_KB + (c & 3) * 4 + (uint32_t)ch * 4096;
-      const uint32_t x32 = (c & 31) >> 2;
-#pragma unroll
-      for (int j = 0; j < 32; ++j)
-        *f32at(sm, bw + (uint32_t)(j >> 3) * 1024u + (uint32_t)(j & 7) * 128u +
-                       ((x32 ^ (uint32_t)(j & 7)) << 4)) = v[j];
-    }
-    fence_proxy_async_smem();
-    cta_sync();
-    if (misc->abort) { ok = false; break; }
-    // ================= Ph6: X = [W; Qh] Sh
-    if (tid == 0) {
-      const uint32_t idx = idesc_make(kFmtTF32, 128, 32, false, false);
-#pragma unroll
-      for (int s = 0; s < 16; ++s) {
-        const uint64_t a = sdesc_sw128(sbase + XA_OFF + (s >> 2) * XA_KB + (s & 3) * 32, 16, 1024);
-        const uint64_t b = sdesc_sw128(sbase + SH_OFF + (s >> 2) * SH_KB + (s & 3) * 32, 16, 1024);
-        mma_tf32(tbase + TM_X, a, b, idx, s > 0);
-      }
-      mma_commit(&misc->bar_x);
-    }
-    if (!mbar_wait(&misc->bar_x, par)) misc->abort = 1;
-    tc_fence_after();
-    if (qd < 2) {  // token rows 0..63: U = Ut - W Sh (columns 16 ch ..), stored as U^T
-      float x[16], u[16];
-      tmem_ld16(tbase + lane_base + TM_X + ch * 16, x);
-      if (has_v) tmem_ld16(tbase + lane_base + TM_U + ch * 16, u);
-      else {
-#pragma unroll
-        for (int j = 0; j < 16; ++j) u[j] = 0.0f;
-      }
+    if (qd < 2) {  // token rows 0..63: U (16 columns per warp) stored as U^T (K-major)
+      float u[16];
+      tmem_ld16(tbase + lane_base + TM_U + ch * 16, u);
       const int r = qd * 32 + lane;
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        *f32at(sm, UT_OFF + sw128_off32(ch * 16 + j, r, UT_KB)) = u[j] - x[j];
+      for (int j = 0; j < 16; ++j) *f32at(sm, UT_OFF + sw128_off32(ch * 16 + j, r, UT_KB)) = u[j];
     }
     fence_proxy_async_smem();
     cta_sync();
     if (misc->abort) { ok = false; break; }
-    // ================= Ph7: Y = Kb^T U, O = X_q + tril(A_qk) U
+    // ================= round 3: Y = Kb^T U, O = X_q + tril(A_qk) U
     if (tid == 0) {
       const uint32_t idy = idesc_make(kFmtTF32, 128, 32, false, false);
 #pragma unroll
@@ -513,9 +473,9 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
         mma_tf32_ts(tbase + TM_Y, tbase + TM_KBT + s * 8, b, idy, s > 0);
         if (!pkg) mma_tf32_ts(tbase + TM_X, tbase + TM_A + s * 8, b, idy, 1);
       }
-      mma_commit(&misc->bar_y);
+      mma_commit(&misc->bar_3);
     }
-    if (!mbar_wait(&misc->bar_y, par)) misc->abort = 1;
+    if (!mbar_wait(&misc->bar_3, par)) misc->abort = 1;
     tc_fence_after();
     if (qd >= 2 && !pkg && p.o) {  // output rows (Qh rows 64..127), 16 columns per warp
       float x[16];
