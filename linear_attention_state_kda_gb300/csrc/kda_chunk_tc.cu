@@ -76,18 +76,19 @@ static_assert(SCR_P + 3 * 256 * 4 <= STG_B, "scratch overflow");
 static_assert(SCR_A + 64 * LA * 4 <= STG_V, "A_kk scratch must not overlap the value tile");
 
 // TMEM columns (512 allocated)
-constexpr uint32_t TM_A = 0;      // 64: [Kh; Qh] Kb^T; lanes 64..127 masked to tril(A_qk)
-constexpr uint32_t TM_X = 64;     // 32: [Kh; Qh] Sh, then O in lanes 64..127
-constexpr uint32_t TM_U = 96;     // 32: U (lanes 0..63 = tokens)
-constexpr uint32_t TM_Y = 128;    // 32: Kb^T U (lanes = key channels)
-constexpr uint32_t TM_KBT = 160;  // 64: Kb^T operand (lanes = key channels, columns = tokens)
-constexpr uint32_t TM_TB = 224;   // 64: TB operand (lanes 0..63 = tokens; 64..127 zero)
-constexpr uint32_t TM_S = 288;    // 32: state tile (lanes = key channels)
+// (A and Kb^T are double-buffered: the next chunk's are built while round 3 reads these.)
+constexpr uint32_t TM_A0 = 0;     // 2 x 64: [Kh; Qh] Kb^T; lanes 64..127 masked to tril(A_qk)
+constexpr uint32_t TM_X = 128;    // 32: [Kh; Qh] Sh, then O in lanes 64..127
+constexpr uint32_t TM_U = 160;    // 32: U (lanes 0..63 = tokens)
+constexpr uint32_t TM_Y = 192;    // 32: Kb^T U (lanes = key channels)
+constexpr uint32_t TM_KBT0 = 224; // 2 x 64: Kb^T operand (lanes = key channels, cols = tokens)
+constexpr uint32_t TM_TB = 352;   // 64: TB operand (lanes 0..63 = tokens; 64..127 zero)
+constexpr uint32_t TM_S = 416;    // 32: state tile (lanes = key channels)
 
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct Misc {
-  uint64_t bar_tma, bar_1, bar_2, bar_3, bar_drain;
+  uint64_t bar_tma, bar_a, bar_x, bar_2, bar_3, bar_drain;
   uint32_t tmem_base;
   int abort;
   float part[2][DK];
@@ -149,7 +150,8 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
   }
   if (tid == 0) {
     mbar_init(&misc->bar_tma, 1);
-    mbar_init(&misc->bar_1, 1);
+    mbar_init(&misc->bar_a, 1);
+    mbar_init(&misc->bar_x, 1);
     mbar_init(&misc->bar_2, 1);
     mbar_init(&misc->bar_3, 1);
     mbar_init(&misc->bar_drain, 1);
@@ -215,13 +217,14 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
   const float* gs = f32at(sm, STG_G);
   const float* bs4 = f32at(sm, STG_B);
   const int hb = h & 3;
-  uint32_t it = 0;
-  bool ok = true;
-  for (int t0 = t_begin; t0 < t_end; t0 += C, ++it) {
-    const int n = min(C, t_end - t0);
-    const uint32_t par = it & 1u;
-    // ================= Ph1: decay, operands, state in the midpoint frame
-    if (!mbar_wait(&misc->bar_tma, par)) misc->abort = 1;
+
+  // Operand build of one chunk (state-independent): waits for its loads, forms the decay
+  // prefix, writes Kh, Qh (XA), Kb (KB) and Kb^T (TMEM buffer kbuf); returns this thread's
+  // channel's rho in log2 units. Whole-CTA; sets misc->abort on a timed-out load.
+  auto build = [&](int tc0, uint32_t itc) -> float {
+    const int n = min(C, t_end - tc0);
+    const uint32_t kbt = TM_KBT0 + (itc & 1u) * 64u;
+    if (!mbar_wait(&misc->bar_tma, itc & 1u)) misc->abort = 1;
     else tma_out = false;
     const int nv = n - half * 32;  // valid rows in this thread's half
     float gl[32];
@@ -234,7 +237,6 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
     misc->part[half][c] = acc;
     if (tid < C) misc->beta[tid] = (tid < n) ? bs4[tid * 4 + hb] : 0.0f;
     __syncthreads();
-    if (misc->abort) { ok = false; break; }
     const float p0 = misc->part[0][c], p1 = misc->part[1][c];
     const float rho2 = 0.5f * (p0 + p1);  // log2 units
     if (half == 0 && !((p0 + p1) >= -kMaxChunkDecay * kLog2e) && p.status)
@@ -271,9 +273,39 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
           *f32at(sm, bkb + sw) = kb[i];
         }
         // Kb^T as the TMEM operand of round 3: lane = channel c, column = token
-        tmem_st16(tbase + lane_base + TM_KBT + half * 32 + blk * 16, kb);
+        tmem_st16(tbase + lane_base + kbt + half * 32 + blk * 16, kb);
       }
     }
+    tmem_st_wait();
+    return rho2;
+  };
+  // A = [Kh; Qh] Kb^T of a built chunk into TMEM buffer (itc & 1); thread 0.
+  auto issue_a = [&](uint32_t itc) {
+    const uint32_t ida = idesc_make(kFmtTF32, 128, 64, false, false);
+#pragma unroll
+    for (int s = 0; s < 16; ++s) {
+      const uint64_t a = sdesc_sw128(sbase + XA_OFF + (s >> 2) * XA_KB + (s & 3) * 32, 16, 1024);
+      const uint64_t b = sdesc_sw128(sbase + KB_OFF + (s >> 2) * KB_KB + (s & 3) * 32, 16, 1024);
+      mma_tf32(tbase + TM_A0 + (itc & 1u) * 64u, a, b, ida, s > 0);
+    }
+    mma_commit(&misc->bar_a);
+  };
+
+  uint32_t it = 0;
+  bool ok = true;
+  float rho2 = 0.0f;
+  if (t_end > t_begin) {
+    rho2 = build(t_begin, 0);
+    fence_proxy_async_smem();
+    cta_sync();
+    if (misc->abort) ok = false;
+    else if (tid == 0) issue_a(0);
+  }
+  for (int t0 = t_begin; ok && t0 < t_end; t0 += C, ++it) {
+    const int n = min(C, t_end - t0);
+    const uint32_t par = it & 1u;
+    const uint32_t tma_a = TM_A0 + par * 64u, tm_kbt = TM_KBT0 + par * 64u;
+    // ================= Ph1: state in the midpoint frame (operands were built earlier)
     const float erho = ex2_approx(rho2);
     {  // Sh = e^rho S into the round-1 operand (lane c; warps 0-3 cols 0..15, 4-7 16..31)
       float s[16];
@@ -285,29 +317,25 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
         *f32at(sm, bsh + (uint32_t)(j >> 3) * 1024u + (uint32_t)(j & 7) * 128u +
                        ((xs ^ (uint32_t)(j & 7)) << 4)) = erho * s[j];
     }
-    tmem_st_wait();
     fence_proxy_async_smem();
     cta_sync();
-    // ================= round 1: A = [Kh; Qh] Kb^T, X = [Kh; Qh] Sh
+    // ================= round 1: X = [Kh; Qh] Sh (A of this chunk is already in flight)
     if (tid == 0) {
-      const uint32_t ida = idesc_make(kFmtTF32, 128, 64, false, false);
       const uint32_t idx = idesc_make(kFmtTF32, 128, 32, false, false);
 #pragma unroll
       for (int s = 0; s < 16; ++s) {
         const uint64_t a = sdesc_sw128(sbase + XA_OFF + (s >> 2) * XA_KB + (s & 3) * 32, 16, 1024);
-        const uint64_t b = sdesc_sw128(sbase + KB_OFF + (s >> 2) * KB_KB + (s & 3) * 32, 16, 1024);
         const uint64_t bs = sdesc_sw128(sbase + SH_OFF + (s >> 2) * SH_KB + (s & 3) * 32, 16, 1024);
-        mma_tf32(tbase + TM_A, a, b, ida, s > 0);
         mma_tf32(tbase + TM_X, a, bs, idx, s > 0);
       }
-      mma_commit(&misc->bar_1);
+      mma_commit(&misc->bar_x);
     }
-    if (!mbar_wait(&misc->bar_1, par)) misc->abort = 1;
+    if (!mbar_wait(&misc->bar_a, par)) misc->abort = 1;
     tc_fence_after();
     // ================= Ph3: A_kk -> scratch, A_qk masked in place, V - Kh Sh -> operand
     {
       float v[32];
-      tmem_ld32(tbase + lane_base + TM_A + ch * 32, v);
+      tmem_ld32(tbase + lane_base + tma_a + ch * 32, v);
       const int R = qd * 32 + lane;
       if (R < C) {  // beta_r A_kk, strictly lower, as 16-byte row segments
         const float br = misc->beta[R];
@@ -319,22 +347,27 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
               make_float4(i < R ? br * v[j] : 0.0f, i + 1 < R ? br * v[j + 1] : 0.0f,
                           i + 2 < R ? br * v[j + 2] : 0.0f, i + 3 < R ? br * v[j + 3] : 0.0f);
         }
-        // (V - Kh Sh) for token R, 16 value columns per warp, stored transposed (K = token)
-        float x[16];
-        tmem_ld16(tbase + lane_base + TM_X + ch * 16, x);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const int col = ch * 16 + j;
-          const float vv = (R < n && has_v) ? bf16at(sm, STG_V + R * 64 + col * 2) : 0.0f;
-          *f32at(sm, VT_OFF + sw128_off32(col, R, VT_KB)) = vv - x[j];
-        }
       } else {  // causal A_qk (diagonal included), the round-3 operand, rewritten in TMEM
         const int r = R - C;
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = (ch * 32 + j <= r) ? v[j] : 0.0f;
-        tmem_st16(tbase + lane_base + TM_A + ch * 32, v);
-        tmem_st16(tbase + lane_base + TM_A + ch * 32 + 16, v + 16);
+        tmem_st16(tbase + lane_base + tma_a + ch * 32, v);
+        tmem_st16(tbase + lane_base + tma_a + ch * 32 + 16, v + 16);
         tmem_st_wait();
+      }
+    }
+    if (!mbar_wait(&misc->bar_x, par)) misc->abort = 1;
+    tc_fence_after();
+    if (qd < 2) {
+      // (V - Kh Sh) for token R, 16 value columns per warp, stored transposed (K = token)
+      const int R = qd * 32 + lane;
+      float x[16];
+      tmem_ld16(tbase + lane_base + TM_X + ch * 16, x);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int col = ch * 16 + j;
+        const float vv = (R < n && has_v) ? bf16at(sm, STG_V + R * 64 + col * 2) : 0.0f;
+        *f32at(sm, VT_OFF + sw128_off32(col, R, VT_KB)) = vv - x[j];
       }
     }
     cta_sync();
@@ -367,54 +400,49 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
         }
       }
       __syncthreads();
-      // off-diagonal blocks by distance d: X_IJ = -X_II sum_{L=J}^{I-1} A_IL X_LJ (J = I - d);
-      // a thread computes 4 adjacent columns of one row of one block
-      for (int dist = 1; dist < 4; ++dist) {
-        const int tasks = (4 - dist) * 64;
-        const int b = tid >> 6, rr = (tid >> 2) & 15, cc = (tid & 3) * 4;
-        const int J = b, I = b + dist;
-        if (tid < tasks) {
-          float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int L = J; L < I; ++L) {
-            const float* arow = Akk + (I * 16 + rr) * LA + L * 16;
+      // off-diagonal blocks by distance d: X_IJ = -X_II sum_{L=J}^{I-1} A_IL X_LJ (J = I - d).
+      // Warp w < 2 (4 - d) owns block J = w / 2 and its 8-column half w % 2; both 16 x 16
+      // block products run as warp-level 3xTF32 MMAs (fp32-level accuracy), the partial
+      // product P passing through a per-warp 16 x 8 tile of shared memory.
+      {
+        const int gq = lane >> 2, tq = lane & 3;
+        float* Pw = P + warp * 128;  // [16][8]
+        for (int dist = 1; dist < 4; ++dist) {
+          if (warp < 2 * (4 - dist)) {
+            const int J = warp >> 1, I = J + dist, n0 = J * 16 + (warp & 1) * 8;
+            float d[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int L = J; L < I; ++L) {
 #pragma unroll
-            for (int l = 0; l < 16; l += 4) {
-              const float4 av = *reinterpret_cast<const float4*>(arow + l);
-              const float avs[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const float4 xv =
-                    *reinterpret_cast<const float4*>(X + (L * 16 + l + u) * LA + J * 16 + cc);
-                a4.x = fmaf(avs[u], xv.x, a4.x);
-                a4.y = fmaf(avs[u], xv.y, a4.y);
-                a4.z = fmaf(avs[u], xv.z, a4.z);
-                a4.w = fmaf(avs[u], xv.w, a4.w);
+              for (int kk = 0; kk < 16; kk += 8) {
+                const float* ar = Akk + (I * 16 + gq) * LA + L * 16 + kk + tq;
+                const float a[4] = {ar[0], ar[8 * LA], ar[4], ar[8 * LA + 4]};
+                const float* br = X + (L * 16 + kk + tq) * LA + n0 + gq;
+                const float bv[2] = {br[0], br[4 * LA]};
+                mma16x8x8_3xtf32(d, a, bv);
               }
             }
-          }
-          *reinterpret_cast<float4*>(P + b * 256 + rr * 16 + cc) = a4;
-        }
-        __syncthreads();
-        if (tid < tasks) {
-          float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f);
-          const float* xrow = X + (I * 16 + rr) * LA + I * 16;
+            Pw[gq * 8 + 2 * tq] = d[0];
+            Pw[gq * 8 + 2 * tq + 1] = d[1];
+            Pw[(gq + 8) * 8 + 2 * tq] = d[2];
+            Pw[(gq + 8) * 8 + 2 * tq + 1] = d[3];
+            __syncwarp();
+            float e[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int l = 0; l < 16; l += 4) {
-            const float4 xv = *reinterpret_cast<const float4*>(xrow + l);
-            const float xs[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float4 pv = *reinterpret_cast<const float4*>(P + b * 256 + (l + u) * 16 + cc);
-              a4.x = fmaf(xs[u], pv.x, a4.x);
-              a4.y = fmaf(xs[u], pv.y, a4.y);
-              a4.z = fmaf(xs[u], pv.z, a4.z);
-              a4.w = fmaf(xs[u], pv.w, a4.w);
+            for (int kk = 0; kk < 16; kk += 8) {
+              const float* ar = X + (I * 16 + gq) * LA + I * 16 + kk + tq;
+              const float a[4] = {ar[0], ar[8 * LA], ar[4], ar[8 * LA + 4]};
+              const float bv[2] = {Pw[(kk + tq) * 8 + gq], Pw[(kk + tq + 4) * 8 + gq]};
+              mma16x8x8_3xtf32(e, a, bv);
             }
+            float* xr = X + (I * 16 + gq) * LA + n0 + 2 * tq;
+            xr[0] = -e[0];
+            xr[1] = -e[1];
+            xr[8 * LA] = -e[2];
+            xr[8 * LA + 1] = -e[3];
+            __syncwarp();
           }
-          *reinterpret_cast<float4*>(X + (I * 16 + rr) * LA + J * 16 + cc) =
-              make_float4(-a4.x, -a4.y, -a4.z, -a4.w);
+          __syncthreads();
         }
-        __syncthreads();
       }
       // TB = T diag(beta) into TMEM lanes 0..63 (the round-2 A operand)
       if (qd < 2) {
@@ -470,10 +498,19 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const uint64_t b = sdesc_sw128(sbase + UT_OFF + (s >> 2) * UT_KB + (s & 3) * 32, 16, 1024);
-        mma_tf32_ts(tbase + TM_Y, tbase + TM_KBT + s * 8, b, idy, s > 0);
-        if (!pkg) mma_tf32_ts(tbase + TM_X, tbase + TM_A + s * 8, b, idy, 1);
+        mma_tf32_ts(tbase + TM_Y, tbase + tm_kbt + s * 8, b, idy, s > 0);
+        if (!pkg) mma_tf32_ts(tbase + TM_X, tbase + tma_a + s * 8, b, idy, 1);
       }
       mma_commit(&misc->bar_3);
+    }
+    // While round 3 runs: build the next chunk's operands (its loads were issued in round 2;
+    // XA and KB are free, and its A and Kb^T go to the other TMEM buffers) and start its A.
+    float rho2_next = rho2;
+    if (t0 + C < t_end) {
+      rho2_next = build(t0 + C, it + 1);
+      fence_proxy_async_smem();
+      cta_sync();
+      if (tid == 0 && !misc->abort) issue_a(it + 1);
     }
     if (!mbar_wait(&misc->bar_3, par)) misc->abort = 1;
     tc_fence_after();
@@ -507,9 +544,11 @@ chunk_tc_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ C
       tmem_st16(tbase + lane_base + TM_S + ch * 16, s);
       tmem_st_wait();
     }
+    rho2 = rho2_next;
     cta_sync();
     if (misc->abort) { ok = false; break; }
   }
+  if (misc->abort) ok = false;
   // ---- exit state of this tile
   if (!ok) {
     // Let this CTA's in-flight MMAs and loads drain (bounded) before its shared memory and

@@ -235,6 +235,37 @@ __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// ---------------------------------------------------------------- warp-level MMA
+// D(16x8) += A(16x8, row) * B(8x8, col) in tf32 with fp32 accumulation, one warp. Fragments
+// (g = lane / 4, t = lane % 4): a0 A[g][t], a1 A[g+8][t], a2 A[g][t+4], a3 A[g+8][t+4];
+// b0 B[t][g], b1 B[t+4][g]; d0 D[g][2t], d1 D[g][2t+1], d2 D[g+8][2t], d3 D[g+8][2t+1].
+// Used for the 16 x 16 block products of the chunk's triangular solve, too small for tcgen05.
+__device__ __forceinline__ void mma16x8x8_tf32(float* d, const uint32_t* a, const uint32_t* b) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// 3xTF32: D += A B with A = Ah + Al, B = Bh + Bl (Xh = X with the low 13 mantissa bits
+// cleared, Xl = X - Xh), dropping only Al Bl: fp32-level accuracy from tf32 MMAs.
+__device__ __forceinline__ void mma16x8x8_3xtf32(float* d, const float* a, const float* b) {
+  uint32_t ah[4], al[4], bh[2], bl[2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    ah[i] = __float_as_uint(a[i]) & 0xFFFFE000u;
+    al[i] = __float_as_uint(a[i] - __uint_as_float(ah[i]));
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    bh[i] = __float_as_uint(b[i]) & 0xFFFFE000u;
+    bl[i] = __float_as_uint(b[i] - __uint_as_float(bh[i]));
+  }
+  mma16x8x8_tf32(d, al, bh);
+  mma16x8x8_tf32(d, ah, bl);
+  mma16x8x8_tf32(d, ah, bh);
+}
+
 // ---------------------------------------------------------------- descriptors
 // Instruction descriptor, dense MMA with fp32 accumulation.
 //   bits 4-5 D format (1 = f32); 7-9 A format; 10-12 B format (kind::f16: 0 f16, 1 bf16;
