@@ -86,6 +86,17 @@ KDA_API const char* kda_version(void);
 KDA_API uint64_t kda_launch_count(void);
 
 /*
+ * kda_chunk_workspace: bytes of device scratch that kda_chunk_prefill, kda_segment_package
+ * and kda_segment_replay need for n_ranges sequences (or segments) over total_tokens tokens;
+ * 0 when such a call needs none (fp32 inputs, dk = dv = 64, or H not a multiple of 4, all
+ * served by the CUDA-core kernel). The tensor-core path precomputes every state-independent
+ * factor of each (64-token chunk, head) into one record of 147,968 bytes; it keeps
+ * (total_tokens / 64 + n_ranges) * H records.
+ */
+KDA_API size_t kda_chunk_workspace(kda_dtype dt, int n_ranges, int total_tokens, int H, int dk,
+                                   int dv);
+
+/*
  * kda_chunk_prefill: chunked (WY/UT form) prefill over packed sequences.
  *   n_seqs      number of sequences (>= 0); total_tokens = cu_seqlens[n_seqs].
  *   cu_seqlens  device int32 [n_seqs + 1]; may be NULL when n_seqs == 1 (one sequence of
@@ -93,6 +104,9 @@ KDA_API uint64_t kda_launch_count(void);
  *   init_state  [n_seqs, H, dk, dv] fp32 entry states, or NULL for zeros.
  *   o           [total_tokens, H, dv] output (dtype dt).
  *   final_state [n_seqs, H, dk, dv] fp32 exit states, or NULL.
+ *   workspace   device scratch of at least kda_chunk_workspace(dt, n_seqs, total_tokens, H,
+ *               dk, dv) bytes, 256-byte aligned, contents need not be initialised; may be
+ *               NULL when that query returns 0 (KDA_ERR_WORKSPACE otherwise).
  *   status      optional device word (KDA_STATUS_DECAY_RANGE).
  * Source: the chunked FlashKDA prefill of kern PR #44 (varlen build with cu_seqlens and
  * per-sequence state blocks) and pegainfer PR #970 ("same segment walk, same chunk step").
@@ -101,8 +115,8 @@ KDA_API kda_status kda_chunk_prefill(kda_dtype dt, int n_seqs, int total_tokens,
                              const int32_t* cu_seqlens, int H, int dk, int dv, int chunk,
                              float scale, const void* q, const void* k, const void* v,
                              const float* g, const float* beta, const float* init_state,
-                             void* o, float* final_state, uint32_t* status,
-                             kda_stream_t stream);
+                             void* o, float* final_state, void* workspace,
+                             size_t ws_bytes, uint32_t* status, kda_stream_t stream);
 
 /*
  * kda_segment_package: per-segment affine (M, D) packages. For each segment
@@ -110,13 +124,14 @@ KDA_API kda_status kda_chunk_prefill(kda_dtype dt, int n_seqs, int total_tokens,
  * running the recurrence over the segment from any entry state S_in ends in
  * M S_in + D. No outputs o are produced and q is not read.
  *   seg_offsets device int32 [n_segs + 1].
+ *   workspace   as for kda_chunk_prefill, sized by kda_chunk_workspace(dt, n_segs, ...).
  * Source: pegainfer PR #970, "KDA (M,D) packages" of the CP publish surface.
  */
 KDA_API kda_status kda_segment_package(kda_dtype dt, int n_segs, int total_tokens,
                                const int32_t* seg_offsets, int H, int dk, int dv, int chunk,
                                const void* k, const void* v, const float* g,
-                               const float* beta, float* M, float* D, uint32_t* status,
-                               kda_stream_t stream);
+                               const float* beta, float* M, float* D, void* workspace,
+                               size_t ws_bytes, uint32_t* status, kda_stream_t stream);
 
 /*
  * kda_package_scan: segmented exclusive prefix over packages with the composition
@@ -171,15 +186,16 @@ KDA_API kda_status kda_package_scan_noalloc(int n_seqs, int n_segs,
 /*
  * kda_segment_replay: replays every segment from its prefix state: the chunked prefill with
  * segments as the sequences and seg_init as their entry states. Writes o for every token and,
- * if seg_final is not NULL, each segment's exit state.
+ * if seg_final is not NULL, each segment's exit state. workspace as for kda_chunk_prefill,
+ * sized by kda_chunk_workspace(dt, n_segs, ...).
  * Source: pegainfer PR #970, each CP member prefills its own context segment.
  */
 KDA_API kda_status kda_segment_replay(kda_dtype dt, int n_segs, int total_tokens,
                               const int32_t* seg_offsets, int H, int dk, int dv, int chunk,
                               float scale, const void* q, const void* k, const void* v,
                               const float* g, const float* beta, const float* seg_init,
-                              void* o, float* seg_final, uint32_t* status,
-                              kda_stream_t stream);
+                              void* o, float* seg_final, void* workspace, size_t ws_bytes,
+                              uint32_t* status, kda_stream_t stream);
 
 /*
  * kda_decode_step: one token per batch row over a slot-addressed fp32 state pool,

@@ -45,8 +45,21 @@ kda_status check_shape(const char* fn, kda_dtype dt, int H, int dk, int dv, int 
     if (!(cond)) return set_error(st, msg);  \
   } while (0)
 
-kda_status chunked(const char* fn, const ChunkParams& p, kda_dtype dt, cudaStream_t s) {
-  if (chunk_tc_supported(p, dt)) return launch_chunk_tc(p, dt, s);
+size_t chunk_workspace(kda_dtype dt, int n_ranges, int total_tokens, int H, int dk, int dv) {
+  if (n_ranges <= 0 || total_tokens <= 0 || H <= 0) return 0;
+  if (!chunk_tc_shape_ok(dt, n_ranges, total_tokens, H, dk, dv)) return 0;
+  return chunk_tc_workspace_bytes(n_ranges, total_tokens, H);
+}
+
+kda_status chunked(const char* fn, const ChunkParams& p, kda_dtype dt, void* ws, size_t ws_bytes,
+                   cudaStream_t s) {
+  const size_t need = chunk_workspace(dt, p.n_ranges, p.total_tokens, p.H, p.dk, p.dv);
+  if (need > 0) {
+    KDA_REQUIRE(ws && ws_bytes >= need && aligned(ws, 256), KDA_ERR_WORKSPACE,
+                std::string(fn) + ": workspace missing, too small or not 256-byte aligned (need " +
+                    std::to_string(need) + " bytes)");
+  }
+  if (chunk_tc_supported(p, dt)) return launch_chunk_tc(p, dt, ws, ws_bytes, s);
   return launch_chunk_simt(p, dt, s);
 }
 
@@ -63,12 +76,16 @@ const char* kda_version(void) { return "kda-gb300 0.1 (sm_103a)"; }
 
 uint64_t kda_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+size_t kda_chunk_workspace(kda_dtype dt, int n_ranges, int total_tokens, int H, int dk, int dv) {
+  return chunk_workspace(dt, n_ranges, total_tokens, H, dk, dv);
+}
+
 kda_status kda_chunk_prefill(kda_dtype dt, int n_seqs, int total_tokens,
                              const int32_t* cu_seqlens, int H, int dk, int dv, int chunk,
                              float scale, const void* q, const void* k, const void* v,
                              const float* g, const float* beta, const float* init_state,
-                             void* o, float* final_state, uint32_t* status,
-                             kda_stream_t stream) {
+                             void* o, float* final_state, void* workspace, size_t ws_bytes,
+                             uint32_t* status, kda_stream_t stream) {
   const char* fn = "kda_chunk_prefill";
   kda_status st = check_shape(fn, dt, H, dk, dv, chunk);
   if (st != KDA_OK) return st;
@@ -91,14 +108,14 @@ kda_status kda_chunk_prefill(kda_dtype dt, int n_seqs, int total_tokens,
   p.H = H; p.dk = dk; p.dv = dv; p.scale = scale;
   p.init = init_state; p.o = o; p.final_state = final_state; p.status = status;
   p.package = 0;
-  return chunked(fn, p, dt, (cudaStream_t)stream);
+  return chunked(fn, p, dt, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
 kda_status kda_segment_package(kda_dtype dt, int n_segs, int total_tokens,
                                const int32_t* seg_offsets, int H, int dk, int dv, int chunk,
                                const void* k, const void* v, const float* g,
-                               const float* beta, float* M, float* D, uint32_t* status,
-                               kda_stream_t stream) {
+                               const float* beta, float* M, float* D, void* workspace,
+                               size_t ws_bytes, uint32_t* status, kda_stream_t stream) {
   const char* fn = "kda_segment_package";
   kda_status st = check_shape(fn, dt, H, dk, dv, chunk);
   if (st != KDA_OK) return st;
@@ -118,7 +135,7 @@ kda_status kda_segment_package(kda_dtype dt, int n_segs, int total_tokens,
   p.offsets = seg_offsets; p.n_ranges = n_segs; p.total_tokens = total_tokens;
   p.H = H; p.dk = dk; p.dv = dv; p.scale = 1.0f;
   p.M = M; p.D = D; p.status = status; p.package = 1;
-  return chunked(fn, p, dt, (cudaStream_t)stream);
+  return chunked(fn, p, dt, workspace, ws_bytes, (cudaStream_t)stream);
 }
 
 size_t kda_package_scan_workspace(int n_seqs, int max_segs_per_seq, int H, int dk, int dv) {
@@ -158,13 +175,13 @@ kda_status kda_segment_replay(kda_dtype dt, int n_segs, int total_tokens,
                               const int32_t* seg_offsets, int H, int dk, int dv, int chunk,
                               float scale, const void* q, const void* k, const void* v,
                               const float* g, const float* beta, const float* seg_init,
-                              void* o, float* seg_final, uint32_t* status,
-                              kda_stream_t stream) {
+                              void* o, float* seg_final, void* workspace, size_t ws_bytes,
+                              uint32_t* status, kda_stream_t stream) {
   KDA_REQUIRE(n_segs == 0 || seg_offsets, KDA_ERR_INVALID_ARG,
               "kda_segment_replay: seg_offsets must be non-null");
   kda_status st = kda_chunk_prefill(dt, n_segs, total_tokens, seg_offsets, H, dk, dv, chunk,
-                                    scale, q, k, v, g, beta, seg_init, o, seg_final, status,
-                                    stream);
+                                    scale, q, k, v, g, beta, seg_init, o, seg_final, workspace,
+                                    ws_bytes, status, stream);
   if (st != KDA_OK) {
     std::string m = g_last_error;
     if (m.rfind("kda_chunk_prefill", 0) == 0) m = "kda_segment_replay" + m.substr(17);

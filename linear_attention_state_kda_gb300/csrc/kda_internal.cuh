@@ -59,10 +59,15 @@ constexpr float kMaxChunkDecay = 160.0f;
 // FFMA (CUDA-core) chunk kernel: fp32 arithmetic throughout; any dtype.
 kda_status launch_chunk_simt(const ChunkParams& p, kda_dtype dt, cudaStream_t s);
 
-// Tensor-core (tcgen05/TMEM/TMA) chunk kernel for bf16 inputs; returns KDA_ERR_UNSUPPORTED
-// for shapes it does not handle.
-kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, cudaStream_t s);
+// Tensor-core (tcgen05/TMEM/TMA) chunk path for bf16 inputs with dk = dv = 128: a parallel
+// per-(chunk, head) prep kernel writing workspace records, then the in-order state kernel.
+// chunk_tc_shape_ok decides from shapes alone whether the path (and so the workspace)
+// applies; chunk_tc_supported also checks the pointers.
+bool chunk_tc_shape_ok(kda_dtype dt, int n_ranges, int total_tokens, int H, int dk, int dv);
+size_t chunk_tc_workspace_bytes(int n_ranges, int total_tokens, int H);
 bool chunk_tc_supported(const ChunkParams& p, kda_dtype dt);
+kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, size_t ws_bytes,
+                           cudaStream_t s);
 
 // Decode step.
 kda_status launch_decode(kda_dtype dt, int batch, int H, int dk, int dv, float scale,

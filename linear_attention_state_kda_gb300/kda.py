@@ -43,10 +43,13 @@ def lib():
     L.kda_version.argtypes = []
     L.kda_launch_count.restype = ctypes.c_uint64
     L.kda_launch_count.argtypes = []
+    L.kda_chunk_workspace.restype = Z
+    L.kda_chunk_workspace.argtypes = [I, I, I, I, I, I]
     L.kda_chunk_prefill.restype = I
-    L.kda_chunk_prefill.argtypes = [I, I, I, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P]
+    L.kda_chunk_prefill.argtypes = [I, I, I, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, Z, P,
+                                    P]
     L.kda_segment_package.restype = I
-    L.kda_segment_package.argtypes = [I, I, I, P, I, I, I, I, P, P, P, P, P, P, P, P]
+    L.kda_segment_package.argtypes = [I, I, I, P, I, I, I, I, P, P, P, P, P, P, P, Z, P, P]
     L.kda_package_scan_workspace.restype = Z
     L.kda_package_scan_workspace.argtypes = [I, I, I, I, I]
     L.kda_package_scan.restype = I
@@ -54,7 +57,8 @@ def lib():
     L.kda_package_scan_noalloc.restype = I
     L.kda_package_scan_noalloc.argtypes = [I, I, P, I, I, I, I, P, P, P, P, P, P, P]
     L.kda_segment_replay.restype = I
-    L.kda_segment_replay.argtypes = [I, I, I, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P]
+    L.kda_segment_replay.argtypes = [I, I, I, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, Z, P,
+                                     P]
     L.kda_decode_step.restype = I
     L.kda_decode_step.argtypes = [I, I, I, I, I, F, P, P, P, P, P, P, P, I64, P, P, P]
     _lib = L
@@ -103,9 +107,26 @@ def _contig(*ts):
             raise ValueError("tensors must be contiguous")
 
 
+def chunk_workspace(dtype, n_ranges, total_tokens, H, dk, dv):
+    """kda_chunk_workspace: scratch bytes of the chunked calls (0 if none is needed)."""
+    dt = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    return int(lib().kda_chunk_workspace(dt, n_ranges, total_tokens, H, dk, dv))
+
+
+def _chunk_ws(workspace, dtype, n_ranges, T, H, dk, dv, device):
+    need = chunk_workspace(dtype, n_ranges, T, H, dk, dv)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=device)
+    if workspace is None:
+        return None, 0
+    return workspace, workspace.numel() * workspace.element_size()
+
+
 def chunk_prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, scale=1.0, o=None,
-                  final_state=None, want_final=True, status=None, chunk=64, stream=None):
-    """kda_chunk_prefill. Returns (o, final_state)."""
+                  final_state=None, want_final=True, status=None, chunk=64, workspace=None,
+                  stream=None):
+    """kda_chunk_prefill. Returns (o, final_state). `workspace` (uint8 device tensor of at
+    least chunk_workspace(...) bytes) is allocated here when not given."""
     _contig(q, k, v, g, beta, cu_seqlens, init_state, o, final_state)
     T, H, dk = k.shape
     dv = v.shape[2]
@@ -114,15 +135,16 @@ def chunk_prefill(q, k, v, g, beta, cu_seqlens=None, init_state=None, scale=1.0,
         o = torch.empty(T, H, dv, dtype=q.dtype, device=q.device)
     if final_state is None and want_final:
         final_state = torch.empty(n, H, dk, dv, dtype=torch.float32, device=q.device)
+    ws, ws_bytes = _chunk_ws(workspace, q.dtype, n, T, H, dk, dv, q.device)
     _check(lib().kda_chunk_prefill(_dt(q), n, T, _ptr(cu_seqlens), H, dk, dv, chunk,
                                    float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                    _ptr(beta), _ptr(init_state), _ptr(o), _ptr(final_state),
-                                   _ptr(status), _stream(stream)))
+                                   _ptr(ws), ws_bytes, _ptr(status), _stream(stream)))
     return o, final_state
 
 
 def segment_package(k, v, g, beta, seg_offsets, M=None, D=None, status=None, chunk=64,
-                    stream=None):
+                    workspace=None, stream=None):
     """kda_segment_package. Returns (M, D)."""
     _contig(k, v, g, beta, seg_offsets, M, D)
     T, H, dk = k.shape
@@ -132,9 +154,10 @@ def segment_package(k, v, g, beta, seg_offsets, M=None, D=None, status=None, chu
         M = torch.empty(P, H, dk, dk, dtype=torch.float32, device=k.device)
     if D is None:
         D = torch.empty(P, H, dk, dv, dtype=torch.float32, device=k.device)
+    ws, ws_bytes = _chunk_ws(workspace, k.dtype, P, T, H, dk, dv, k.device)
     _check(lib().kda_segment_package(_dt(k), P, T, _ptr(seg_offsets), H, dk, dv, chunk,
                                      _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(M), _ptr(D),
-                                     _ptr(status), _stream(stream)))
+                                     _ptr(ws), ws_bytes, _ptr(status), _stream(stream)))
     return M, D
 
 
@@ -183,7 +206,8 @@ def package_scan_noalloc(M, D, seq_seg_offsets, max_segs_per_seq, init_state=Non
 
 
 def segment_replay(q, k, v, g, beta, seg_offsets, seg_init, scale=1.0, o=None,
-                   seg_final=None, want_final=False, status=None, chunk=64, stream=None):
+                   seg_final=None, want_final=False, status=None, chunk=64, workspace=None,
+                   stream=None):
     """kda_segment_replay. Returns (o, seg_final)."""
     _contig(q, k, v, g, beta, seg_offsets, seg_init, o, seg_final)
     T, H, dk = k.shape
@@ -193,10 +217,11 @@ def segment_replay(q, k, v, g, beta, seg_offsets, seg_init, scale=1.0, o=None,
         o = torch.empty(T, H, dv, dtype=q.dtype, device=q.device)
     if seg_final is None and want_final:
         seg_final = torch.empty(P, H, dk, dv, dtype=torch.float32, device=q.device)
+    ws, ws_bytes = _chunk_ws(workspace, q.dtype, P, T, H, dk, dv, q.device)
     _check(lib().kda_segment_replay(_dt(q), P, T, _ptr(seg_offsets), H, dk, dv, chunk,
                                     float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                     _ptr(beta), _ptr(seg_init), _ptr(o), _ptr(seg_final),
-                                    _ptr(status), _stream(stream)))
+                                    _ptr(ws), ws_bytes, _ptr(status), _stream(stream)))
     return o, seg_final
 
 

@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -51,7 +52,7 @@ def test_workspace_query(L):
 def _prefill(L, dt=1, n=1, T=64, cu=None, H=2, dk=128, dv=128, chunk=64, ptr=4096):
     p = ptr
     return L.kda_chunk_prefill(dt, n, T, cu, H, dk, dv, chunk, 1.0, p, p, p, p, p, None, p,
-                               None, None, None)
+                               None, None, 0, None, None)
 
 
 def test_prefill_argument_checks(L):
@@ -68,9 +69,35 @@ def test_prefill_argument_checks(L):
     assert "aligned" in kda.last_error()
     # null inputs with tokens to process
     assert L.kda_chunk_prefill(1, 1, 64, None, 2, 128, 128, 64, 1.0, None, None, None, None,
-                               None, None, None, None, None, None) == kda.KDA_ERR_INVALID_ARG
+                               None, None, None, None, None, 0, None,
+                               None) == kda.KDA_ERR_INVALID_ARG
     # nothing to do is OK and launches nothing
     assert _prefill(L, n=0) == kda.KDA_OK
+    # the tensor-core shapes need the caller's workspace (checked before any launch)
+    assert _prefill(L, H=4) == kda.KDA_ERR_WORKSPACE
+    assert "workspace" in kda.last_error()
+    need = kda.chunk_workspace(torch.bfloat16, 1, 64, 4, 128, 128)
+    assert L.kda_chunk_prefill(1, 1, 64, None, 4, 128, 128, 64, 1.0, 4096, 4096, 4096, 4096,
+                               4096, None, 4096, None, 4096, need - 1, None,
+                               None) == kda.KDA_ERR_WORKSPACE
+    assert L.kda_chunk_prefill(1, 1, 64, None, 4, 128, 128, 64, 1.0, 4096, 4096, 4096, 4096,
+                               4096, None, 4096, None, 4096 + 16, need, None,
+                               None) == kda.KDA_ERR_WORKSPACE
+
+
+def test_chunk_workspace_query(L):
+    from linear_attention_state_kda_gb300 import kda
+    bf, f32 = torch.bfloat16, torch.float32
+    # one record of 147,968 bytes per (chunk slot, head); slots = T // 64 + ranges
+    assert kda.chunk_workspace(bf, 1, 16384, 32, 128, 128) == (256 + 1) * 32 * 147968
+    assert kda.chunk_workspace(bf, 8, 16384, 32, 128, 128) == (256 + 8) * 32 * 147968
+    assert kda.chunk_workspace(bf, 3, 100, 4, 128, 128) == (1 + 3) * 4 * 147968
+    # paths that need none: fp32, d = 64, H not a multiple of 4, nothing to do
+    assert kda.chunk_workspace(f32, 1, 16384, 32, 128, 128) == 0
+    assert kda.chunk_workspace(bf, 1, 16384, 32, 64, 64) == 0
+    assert kda.chunk_workspace(bf, 1, 16384, 6, 128, 128) == 0
+    assert kda.chunk_workspace(bf, 1, 0, 32, 128, 128) == 0
+    assert kda.chunk_workspace(bf, 0, 64, 32, 128, 128) == 0
 
 
 def test_scan_and_package_checks(L):
@@ -82,10 +109,10 @@ def test_scan_and_package_checks(L):
                               None) == kda.KDA_ERR_INVALID_ARG
     assert L.kda_package_scan(1, 2, p, 2, 2, 96, 96, p, p, None, p, None, p, 1 << 40, None,
                               None) == kda.KDA_ERR_UNSUPPORTED
-    assert L.kda_segment_package(1, 2, 128, None, 2, 128, 128, 64, p, p, p, p, p, p, None,
-                                 None) == kda.KDA_ERR_INVALID_ARG
+    assert L.kda_segment_package(1, 2, 128, None, 2, 128, 128, 64, p, p, p, p, p, p, None, 0,
+                                 None, None) == kda.KDA_ERR_INVALID_ARG
     assert L.kda_segment_replay(1, 2, 128, None, 2, 128, 128, 64, 1.0, p, p, p, p, p, p, p,
-                                None, None, None) == kda.KDA_ERR_INVALID_ARG
+                                None, None, 0, None, None) == kda.KDA_ERR_INVALID_ARG
     assert "kda_segment_replay" in kda.last_error()
 
 
