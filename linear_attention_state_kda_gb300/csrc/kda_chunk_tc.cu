@@ -134,6 +134,14 @@ constexpr uint32_t SCR_A = P_KB;          // beta_r A_kk [64][68] (Kb is dead by
 constexpr uint32_t SCR_X = P_XTRA;        // (I + A_kk)^-1 [64][68]
 constexpr uint32_t SCR_P = P_XTRA + 64 * LA * 4;  // 8 warps x [16][8]
 constexpr uint32_t P_MISC = SCR_P + 8 * 128 * 4;
+// Workspace-record staging for the bulk-tensor stores, over Kb, [K'^T ; V^T] and TB^T (all
+// dead once R is complete): W, Q'' and U0 as 4 boxes of [64 rows][32] fp32, O0 as 2 boxes of
+// [64 rows][64] bf16, each in the 128-byte swizzle.
+constexpr uint32_t ST_W = P_KB;
+constexpr uint32_t ST_Q = P_KB + 32768;
+constexpr uint32_t ST_U = P_KB + 65536;
+constexpr uint32_t ST_O = P_KB + 98304;
+static_assert(ST_O + 16384 <= P_XTRA, "record staging overflow");
 constexpr uint32_t P_SMEM = P_MISC + 2048 + 1024;
 static_assert(64 * LA * 4 <= 32768, "A_kk scratch must fit in the Kb buffer");
 static_assert(P_KB % 1024 == 0 && P_BE % 1024 == 0 && P_TBT % 1024 == 0, "alignment");
@@ -160,7 +168,10 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
                   const __grid_constant__ CUtensorMap tmk,
                   const __grid_constant__ CUtensorMap tmv,
                   const __grid_constant__ CUtensorMap tmg,
-                  const __grid_constant__ CUtensorMap tmb, const Ws ws, const int n_items) {
+                  const __grid_constant__ CUtensorMap tmb,
+                  const __grid_constant__ CUtensorMap twq_st,
+                  const __grid_constant__ CUtensorMap tu0_st,
+                  const __grid_constant__ CUtensorMap to0_st, const Ws ws, const int n_items) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   PrepMisc* misc = reinterpret_cast<PrepMisc*>(sm + P_MISC);
@@ -219,9 +230,12 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
     if (it < n_items) issue_tma(t0, hh);
     return it < n_items;
   };
-  bool tma_out = false;  // thread 0: a load is in flight, completing phase parity tma_par
+  // Loads are issued by the loader thread (warp 1), MMAs by thread 0, so that the next item's
+  // loads go out while thread 0 is issuing the A1 product.
+  constexpr int kLoader = 32;
+  bool tma_out = false;  // loader: a load is in flight, completing phase parity tma_par
   uint32_t tma_par = 0;
-  if (tid == 0) tma_out = advance(blockIdx.x);
+  if (tid == kLoader) tma_out = advance(blockIdx.x);
   cta_sync();
 
   uint32_t k_it = 0;
@@ -232,7 +246,7 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
     const uint32_t par = k_it & 1u;
     // ================= decay prefix (channel role: channel c, token half)
     if (!mbar_wait(&misc->bar_tma, par)) misc->abort = 1;
-    else if (tid == 0) tma_out = false;
+    else if (tid == kLoader) tma_out = false;
     {
       const int c = tid & (DK - 1), half = tid >> 7;
       const uint32_t gbase =
@@ -265,6 +279,7 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
         *f32at(sm, gbase + (uint32_t)i * 128u + ((xg ^ (uint32_t)(i & 7)) << 4)) = gam - rho2;
       }
     }
+    if (tid == 0) bulk_wait_read0();  // the previous record has left the staging buffers
     __syncthreads();
     // ================= operands (row role: token t; key rows in warps 0,1,4,5, query rows
     // and values in warps 2,3,6,7; channel half chh)
@@ -274,8 +289,37 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
       const uint32_t tsw = (uint32_t)(t & 7);
       const uint32_t grow = P_STG_G + (uint32_t)t * 128u;
       const uint32_t brow = (uint32_t)t * 128u;
+      // Kb (the B operand of A1) and Kb'^T (workspace) of token t: key-row threads cover the
+      // first 32 channels of their half, query-row threads the last 32, so both roles issue
+      // 96 exponentials per thread
+      float* kbt_out = ws.kbt + (size_t)item * DK * C + t;
+      auto load_x = [&](int c0, float* x) {  // gamma - rho of channels c0 .. c0 + 7
+        const uint32_t g0 = grow + (uint32_t)(c0 >> 5) * 8192u;
+        const float4 xa = *reinterpret_cast<const float4*>(
+            sm + g0 + (((((uint32_t)c0 & 31u) >> 2) ^ tsw) << 4));
+        const float4 xb = *reinterpret_cast<const float4*>(
+            sm + g0 + ((((((uint32_t)c0 + 4u) & 31u) >> 2) ^ tsw) << 4));
+        x[0] = xa.x; x[1] = xa.y; x[2] = xa.z; x[3] = xa.w;
+        x[4] = xb.x; x[5] = xb.y; x[6] = xb.z; x[7] = xb.w;
+      };
+      auto load_bf8 = [&](uint32_t stg, int c0, float* y) {  // 8 staged bf16 of row t
+        unpack8(*reinterpret_cast<const uint4*>(sm + stg + (uint32_t)(c0 >> 6) * 8192u + brow +
+                                                 (((((uint32_t)c0 & 63u) >> 3) ^ tsw) << 4)),
+                y);
+      };
+      auto kb_out = [&](int c0, const float* x, const float* kv) {
+        float kb[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          kb[e] = (valid ? kv[e] : 0.0f) * ex2_approx(-x[e]);
+          kbt_out[(size_t)(c0 + e) * C] = kb[e] * misc->erho[c0 + e];
+        }
+        *reinterpret_cast<float4*>(sm + P_KB + sw128_off32(t, c0, P_KB_KB)) =
+            make_float4(kb[0], kb[1], kb[2], kb[3]);
+        *reinterpret_cast<float4*>(sm + P_KB + sw128_off32(t, c0 + 4, P_KB_KB)) =
+            make_float4(kb[4], kb[5], kb[6], kb[7]);
+      };
       if (qd < 2) {
-        float* kbt_out = ws.kbt + (size_t)item * DK * C + t;
 #pragma unroll 1
         for (int cb = 0; cb < 64; cb += 16) {
           float kh[16];
@@ -283,31 +327,15 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
           for (int u = 0; u < 16; u += 8) {
             const int c0 = chh * 64 + cb + u;
             float x[8], kv[8];
-            const uint32_t g0 = grow + (uint32_t)(c0 >> 5) * 8192u;
-            const float4 xa = *reinterpret_cast<const float4*>(
-                sm + g0 + (((((uint32_t)c0 & 31u) >> 2) ^ tsw) << 4));
-            const float4 xb = *reinterpret_cast<const float4*>(
-                sm + g0 + ((((((uint32_t)c0 + 4u) & 31u) >> 2) ^ tsw) << 4));
-            x[0] = xa.x; x[1] = xa.y; x[2] = xa.z; x[3] = xa.w;
-            x[4] = xb.x; x[5] = xb.y; x[6] = xb.z; x[7] = xb.w;
-            unpack8(*reinterpret_cast<const uint4*>(
-                        sm + P_STG_K + (uint32_t)(c0 >> 6) * 8192u + brow +
-                        (((((uint32_t)c0 & 63u) >> 3) ^ tsw) << 4)),
-                    kv);
-            float kb[8];
+            load_x(c0, x);
+            load_bf8(P_STG_K, c0, kv);
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-              const float kk = valid ? kv[e] : 0.0f;
-              const float er = misc->erho[c0 + e];
-              kh[u + e] = kk * ex2_approx(x[e]);
-              kb[e] = kk * ex2_approx(-x[e]);
-              *f32at(sm, P_BE + sw128_off32(c0 + e, t, P_BE_KB)) = kh[u + e] * er;  // K'^T
-              kbt_out[(size_t)(c0 + e) * C] = kb[e] * er;                             // Kb'^T
+              kh[u + e] = (valid ? kv[e] : 0.0f) * ex2_approx(x[e]);
+              *f32at(sm, P_BE + sw128_off32(c0 + e, t, P_BE_KB)) =
+                  kh[u + e] * misc->erho[c0 + e];  // K'^T
             }
-            *reinterpret_cast<float4*>(sm + P_KB + sw128_off32(t, c0, P_KB_KB)) =
-                make_float4(kb[0], kb[1], kb[2], kb[3]);
-            *reinterpret_cast<float4*>(sm + P_KB + sw128_off32(t, c0 + 4, P_KB_KB)) =
-                make_float4(kb[4], kb[5], kb[6], kb[7]);
+            if (cb < 32) kb_out(c0, x, kv);
           }
           tmem_st16(tbase + lane_base + TM_XA + chh * 64 + cb, kh);
         }
@@ -318,32 +346,25 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
 #pragma unroll
           for (int u = 0; u < 16; u += 8) {
             const int c0 = chh * 64 + cb + u;
-            float vv[8];
-            unpack8(*reinterpret_cast<const uint4*>(
-                        sm + P_STG_V + (uint32_t)(c0 >> 6) * 8192u + brow +
-                        (((((uint32_t)c0 & 63u) >> 3) ^ tsw) << 4)),
-                    vv);
+            float vv[8], x[8];
+            load_bf8(P_STG_V, c0, vv);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
               *f32at(sm, P_BE + sw128_off32(128 + c0 + e, t, P_BE_KB)) = valid ? vv[e] : 0.0f;
+            if (need_out || cb >= 32) load_x(c0, x);
             if (need_out) {
-              float x[8], qv[8];
-              const uint32_t g0 = grow + (uint32_t)(c0 >> 5) * 8192u;
-              const float4 xa = *reinterpret_cast<const float4*>(
-                  sm + g0 + (((((uint32_t)c0 & 31u) >> 2) ^ tsw) << 4));
-              const float4 xb = *reinterpret_cast<const float4*>(
-                  sm + g0 + ((((((uint32_t)c0 + 4u) & 31u) >> 2) ^ tsw) << 4));
-              x[0] = xa.x; x[1] = xa.y; x[2] = xa.z; x[3] = xa.w;
-              x[4] = xb.x; x[5] = xb.y; x[6] = xb.z; x[7] = xb.w;
-              unpack8(*reinterpret_cast<const uint4*>(
-                          sm + P_STG_Q + (uint32_t)(c0 >> 6) * 8192u + brow +
-                          (((((uint32_t)c0 & 63u) >> 3) ^ tsw) << 4)),
-                      qv);
+              float qv[8];
+              load_bf8(P_STG_Q, c0, qv);
 #pragma unroll
               for (int e = 0; e < 8; ++e) qh[u + e] = valid ? qv[e] * ex2_approx(x[e]) : 0.0f;
             } else {
 #pragma unroll
               for (int e = 0; e < 8; ++e) qh[u + e] = 0.0f;
+            }
+            if (cb >= 32) {
+              float kv[8];
+              load_bf8(P_STG_K, c0, kv);
+              kb_out(c0, x, kv);
             }
           }
           tmem_st16(tbase + lane_base + TM_XA + chh * 64 + cb, qh);
@@ -363,6 +384,8 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
         mma_tf32_ts(tbase + TM_A1, tbase + TM_XA + s * 8, b, ida, s > 0);
       }
       mma_commit(&misc->bar_a);
+    }
+    if (tid == kLoader && !misc->abort) {
       tma_out = advance(item + gridDim.x);
       tma_par = par ^ 1u;
     }
@@ -523,57 +546,69 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
     if (misc->abort) break;
     if (!mbar_wait(&misc->bar_e, par)) misc->abort = 1;
     tc_fence_after();
-    // ================= workspace record
-    if (qd < 2) {  // W (columns 0..127) or U0 (columns 128..255) of token row t
-      const int t = qd * 32 + lane;
-      float* dst = chh == 0 ? ws.wq + ((size_t)item * 128 + t) * 128
-                            : ws.u0 + ((size_t)item * 64 + t) * 128;
-#pragma unroll 1
-      for (int cc = 0; cc < 128; cc += 32) {
-        float v[32];
-        tmem_ld32(tbase + lane_base + TM_R + chh * 128 + cc, v);
-#pragma unroll
-        for (int j = 0; j < 32; j += 4)
-          *reinterpret_cast<float4*>(dst + cc + j) =
-              make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-      }
-    } else if (need_out) {
-      const int t = (qd - 2) * 32 + lane;
-      if (chh == 0) {  // Q'' = scale (Qh e^rho - P K')
-        float* dst = ws.wq + ((size_t)item * 128 + 64 + t) * 128;
+    // ================= workspace record: rows staged in shared memory in the boxes'
+    // 128-byte swizzle (16-byte chunk j of row t at ((j ^ (t & 7)) << 4)), then bulk stores
+    {
+      const int t = (qd & 1) * 32 + lane;
+      const uint32_t rsw = (uint32_t)t * 128u;
+      const uint32_t tx = (uint32_t)(t & 7);
+      if (qd < 2 || (need_out && chh == 0)) {  // fp32 rows: W, U0 or Q'' = scale (Q' - P K')
+        const uint32_t dst = qd < 2 ? (chh == 0 ? ST_W : ST_U) : ST_Q;
+        const uint32_t src = qd < 2 ? TM_R + chh * 128 : TM_R;
 #pragma unroll 1
         for (int cc = 0; cc < 128; cc += 32) {
-          float v[32], qh[32];
-          tmem_ld32(tbase + lane_base + TM_R + cc, v);
-          tmem_ld32(tbase + lane_base + TM_XA + cc, qh);
+          float v[32];
+          tmem_ld32(tbase + lane_base + src + cc, v);
+          if (qd >= 2) {
+            float qh[32];
+            tmem_ld32(tbase + lane_base + TM_XA + cc, qh);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = p.scale * (qh[j] * misc->erho[cc + j] - v[j]);
+            for (int j = 0; j < 32; ++j) v[j] = p.scale * (qh[j] * misc->erho[cc + j] - v[j]);
+          }
+          const uint32_t box = dst + (uint32_t)(cc >> 5) * 8192u + rsw;
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(dst + cc + j) =
-                make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<float4*>(sm + box + (((uint32_t)j ^ tx) << 4)) =
+                make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         }
-      } else {  // O0 = scale P V
-        __nv_bfloat16* dst = ws.o0 + ((size_t)item * 64 + t) * 128;
+      } else if (need_out) {  // O0 = scale P V (bf16)
 #pragma unroll 1
         for (int cc = 0; cc < 128; cc += 32) {
           float v[32];
           tmem_ld32(tbase + lane_base + TM_R + 128 + cc, v);
+          const uint32_t box = ST_O + (uint32_t)(cc >> 6) * 8192u + rsw;
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
+          for (int k = 0; k < 4; ++k) {
+            const float* w = v + 8 * k;
             uint4 pk;
-            __nv_bfloat162 b0 = __floats2bfloat162_rn(p.scale * v[j], p.scale * v[j + 1]);
-            __nv_bfloat162 b1 = __floats2bfloat162_rn(p.scale * v[j + 2], p.scale * v[j + 3]);
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(p.scale * v[j + 4], p.scale * v[j + 5]);
-            __nv_bfloat162 b3 = __floats2bfloat162_rn(p.scale * v[j + 6], p.scale * v[j + 7]);
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(p.scale * w[0], p.scale * w[1]);
+            __nv_bfloat162 b1 = __floats2bfloat162_rn(p.scale * w[2], p.scale * w[3]);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(p.scale * w[4], p.scale * w[5]);
+            __nv_bfloat162 b3 = __floats2bfloat162_rn(p.scale * w[6], p.scale * w[7]);
             pk.x = *reinterpret_cast<uint32_t*>(&b0);
             pk.y = *reinterpret_cast<uint32_t*>(&b1);
             pk.z = *reinterpret_cast<uint32_t*>(&b2);
             pk.w = *reinterpret_cast<uint32_t*>(&b3);
-            *reinterpret_cast<uint4*>(dst + cc + j) = pk;
+            const uint32_t jc = (uint32_t)((cc & 63) >> 3) + (uint32_t)k;
+            *reinterpret_cast<uint4*>(sm + box + ((jc ^ tx) << 4)) = pk;
           }
         }
       }
+    }
+    fence_proxy_async_smem();
+    cta_sync();
+    if (tid == 0) {
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) {
+        tma_store_2d(&twq_st, sm + ST_W + kb * 8192, kb * 32, item * 128);
+        tma_store_2d(&tu0_st, sm + ST_U + kb * 8192, kb * 32, item * 64);
+        if (need_out) tma_store_2d(&twq_st, sm + ST_Q + kb * 8192, kb * 32, item * 128 + 64);
+      }
+      if (need_out) {
+        tma_store_2d(&to0_st, sm + ST_O, 0, item * 64);
+        tma_store_2d(&to0_st, sm + ST_O + 8192, 64, item * 64);
+      }
+      bulk_commit();
     }
     cta_sync();
     if (misc->abort) break;
@@ -584,9 +619,10 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
       if (p.status) atomicOr(p.status, KDA_STATUS_TIMEOUT);
       mma_commit(&misc->bar_drain);
       mbar_wait(&misc->bar_drain, 0, 100000000ull);
-      if (tma_out) mbar_wait(&misc->bar_tma, tma_par, 100000000ull);
     }
+    if (tid == kLoader && tma_out) mbar_wait(&misc->bar_tma, tma_par, 100000000ull);
   }
+  if (tid == 0) bulk_wait0();
   cta_sync();
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
@@ -738,7 +774,6 @@ chunk_state_kernel(const __grid_constant__ ChunkParams p,
     const int n = min(C, t_end - t0);
     const uint32_t par = (uint32_t)j & 1u;
     const uint32_t st = (uint32_t)(j & 1) * S_STAGE;
-    if (j + 1 < nch) load_regs(j + 1, nu0, no0, ndec);
     // ================= X = [W ; Q''] S
     if (tid == 0) {
       if (!mbar_wait(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u)) {
@@ -756,6 +791,7 @@ chunk_state_kernel(const __grid_constant__ ChunkParams p,
         mma_commit(&misc->bar_x);
       }
     }
+    if (j + 1 < nch) load_regs(j + 1, nu0, no0, ndec);  // next chunk's register operands
     if (!mbar_wait(&misc->bar_x, par)) misc->abort = 1;
     tc_fence_after();
     // ================= U = U0 - W S (token rows), kept as U^T for the next product
@@ -910,18 +946,21 @@ bool make_map_beta(CUtensorMap* m, const float* ptr, int T, int H) {
   return r == CUDA_SUCCESS;
 }
 
-// fp32 [rows][cols] workspace array as a 2-D tensor (cols, rows); box (32, 128) with the
-// 128-byte swizzle: one K-block of a 128-row operand per load.
-bool make_map_ws(CUtensorMap* m, const float* ptr, uint64_t rows, uint64_t cols) {
+// [rows][cols] workspace array (fp32, or bf16 when bf16) as a 2-D tensor (cols, rows); box of
+// 128 bytes x box_rows with the 128-byte swizzle: one K-block of an operand per copy.
+bool make_map_ws(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                 bool bf16 = false) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
+  const uint64_t es_bytes = bf16 ? 2 : 4;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
-  cuuint32_t box[2] = {32, 128};
+  cuuint64_t strides[1] = {(cuuint64_t)(cols * es_bytes)};
+  cuuint32_t box[2] = {(cuuint32_t)(128 / es_bytes), box_rows};
   cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides,
-                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                   const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -969,15 +1008,17 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   ws.o0 = (__nv_bfloat16*)(base + (size_t)n_items * (kWqBytes + kKbtBytes + kU0Bytes));
   ws.dec = (float*)(base + (size_t)n_items * (kWqBytes + kKbtBytes + kU0Bytes + kO0Bytes));
 
-  CUtensorMap mq, mk, mv, mg, mb, mwq, mkbt;
+  CUtensorMap mq, mk, mv, mg, mb, mwq, mkbt, swq, su0, so0;
   const void* qp = p.q ? p.q : p.k;
+  const uint64_t rows128 = (uint64_t)n_items * 128, rows64 = (uint64_t)n_items * 64;
   if (!make_map3(&mq, qp, p.total_tokens, p.H, 64, false) ||
       !make_map3(&mk, p.k, p.total_tokens, p.H, 64, false) ||
       !make_map3(&mv, p.v, p.total_tokens, p.H, 64, false) ||
       !make_map3(&mg, p.g, p.total_tokens, p.H, 32, true) ||
       !make_map_beta(&mb, p.beta, p.total_tokens, p.H) ||
-      !make_map_ws(&mwq, ws.wq, (uint64_t)n_items * 128, 128) ||
-      !make_map_ws(&mkbt, ws.kbt, (uint64_t)n_items * 128, 64))
+      !make_map_ws(&mwq, ws.wq, rows128, 128, 128) || !make_map_ws(&mkbt, ws.kbt, rows128, 64, 128) ||
+      !make_map_ws(&swq, ws.wq, rows128, 128, 64) || !make_map_ws(&su0, ws.u0, rows64, 128, 64) ||
+      !make_map_ws(&so0, ws.o0, rows64, 128, 64, true))
     return set_error(KDA_ERR_CUDA, "tensor-core chunk path: cuTensorMapEncodeTiled failed");
   cudaError_t e =
       cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
@@ -988,7 +1029,8 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
     return set_error(KDA_ERR_CUDA, std::string("tensor-core chunk path attribute: ") +
                                        cudaGetErrorString(e));
   const int grid1 = (int)std::min<int64_t>(n_items, sm_count());
-  chunk_prep_kernel<<<grid1, kThreads, P_SMEM, s>>>(p, mq, mk, mv, mg, mb, ws, (int)n_items);
+  chunk_prep_kernel<<<grid1, kThreads, P_SMEM, s>>>(p, mq, mk, mv, mg, mb, swq, su0, so0, ws,
+                                                     (int)n_items);
   count_launches(1);
   kda_status st = check_launch("tensor-core chunk prep kernel");
   if (st != KDA_OK) return st;

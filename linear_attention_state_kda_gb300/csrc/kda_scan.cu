@@ -329,14 +329,35 @@ scan_tc(Tree t, int d, const int32_t* seq_off, const float* init, float* outp,
   }
 }
 
+// The package moves between tree levels are plain copies: 16-byte accesses, kMoveParts CTAs
+// per package.
+constexpr int kMoveParts = 8;
+
 // a[i] <- tmp[pair] after an up-sweep level
 __global__ void scan_up_move(Tree t, int d) {
-  const int pair = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  const int pair = blockIdx.x / kMoveParts, part = blockIdx.x % kMoveParts;
+  const int h = blockIdx.y, s = blockIdx.z;
   const int i = (2 * pair + 2) * d - 1;
-  float4* R = reinterpret_cast<float4*>(t.node(s, i, h));
-  const float4* X = reinterpret_cast<const float4*>(t.tnode(s, pair, h));
-  const int64_t n = pkg_floats(t.dk, t.dv) / 4;
-  for (int64_t e = threadIdx.x; e < n; e += blockDim.x) R[e] = X[e];
+  const int64_t per = pkg_floats(t.dk, t.dv) / 4 / kMoveParts;
+  float4* R = reinterpret_cast<float4*>(t.node(s, i, h)) + part * per;
+  const float4* X = reinterpret_cast<const float4*>(t.tnode(s, pair, h)) + part * per;
+  for (int64_t e = threadIdx.x; e < per; e += blockDim.x) R[e] = X[e];
+}
+
+// a[i-d] <- a[i], a[i] <- tmp[pair] after a down-sweep level
+__global__ void scan_down_move(Tree t, int d) {
+  const int pair = blockIdx.x / kMoveParts, part = blockIdx.x % kMoveParts;
+  const int h = blockIdx.y, s = blockIdx.z;
+  const int i = (2 * pair + 2) * d - 1;
+  const int64_t per = pkg_floats(t.dk, t.dv) / 4 / kMoveParts;
+  float4* L = reinterpret_cast<float4*>(t.node(s, i - d, h)) + part * per;
+  float4* R = reinterpret_cast<float4*>(t.node(s, i, h)) + part * per;
+  const float4* X = reinterpret_cast<const float4*>(t.tnode(s, pair, h)) + part * per;
+  for (int64_t e = threadIdx.x; e < per; e += blockDim.x) {
+    const float4 r = R[e];
+    L[e] = r;
+    R[e] = X[e];
+  }
 }
 
 }  // namespace tc
@@ -373,7 +394,8 @@ kda_status run_tc(int n_seqs, int n_segs, const int32_t* seq_off, int max_segs, 
   for (int d = 1; d < t.P2; d <<= 1) {
     tc::scan_tc<0><<<dim3(4, t.P2 / (2 * d), zh), 256, smem, s>>>(t, d, seq_off, init, nullptr,
                                                                   status);
-    tc::scan_up_move<<<dim3(t.P2 / (2 * d), H, n_seqs), kThreads, 0, s>>>(t, d);
+    tc::scan_up_move<<<dim3(t.P2 / (2 * d) * tc::kMoveParts, H, n_seqs), kThreads, 0, s>>>(t,
+                                                                                         d);
     launches += 2;
   }
   if (final_state && init) {
@@ -387,7 +409,8 @@ kda_status run_tc(int n_seqs, int n_segs, const int32_t* seq_off, int max_segs, 
   for (int d = t.P2 / 2; d >= 1; d >>= 1) {
     tc::scan_tc<1><<<dim3(4, t.P2 / (2 * d), zh), 256, smem, s>>>(t, d, seq_off, init, nullptr,
                                                                   status);
-    scan_down_move<<<dim3(t.P2 / (2 * d), H, n_seqs), kThreads, 0, s>>>(t, d);
+    tc::scan_down_move<<<dim3(t.P2 / (2 * d) * tc::kMoveParts, H, n_seqs), kThreads, 0, s>>>(t,
+                                                                                           d);
     launches += 2;
   }
   if (init)
