@@ -42,23 +42,24 @@ using namespace ptx;
 
 constexpr int C = kChunk;  // 64 tokens per chunk
 constexpr int DK = 128;
-constexpr int TW = 32;     // state columns per state-kernel CTA
 constexpr int kThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---------------------------------------------------------------- workspace record
 // Per item (chunk slot, head):
-//   wq  [128][128] fp32  rows 0..63 W, rows 64..127 Q''
-//   kbt [128][64]  fp32  Kb'^T
-//   u0  [64][128]  fp32  U0
-//   o0  [64][128]  bf16  O0
+//   wq  [128][128] fp32  rows 0..63 W, rows 64..127 Q''   (row = token, column = channel)
+//   kbt [128][64]  fp32  Kb'^T                            (row = channel, column = token)
+//   u0  [16][128][4] fp32 U0^T, tokens 4b .. 4b+3 of value column n at [b][n]
+//   o0  [8][128][8]  bf16 O0^T, tokens 8b .. 8b+7 of value column n at [b][n]
+// (U0^T and O0^T are interleaved so that 32 consecutive value columns read one token group as
+// one contiguous 512-byte run.)
 //   dec [128]      fp32  e^gamma_C
 // Chunk j of range i (starting at token b_i) has slot floor(b_i / C) + i + j: distinct for
 // distinct chunks of valid ordered ranges, and below floor(T / C) + n_ranges.
 constexpr size_t kWqBytes = 128 * 128 * 4;
 constexpr size_t kKbtBytes = 128 * 64 * 4;
-constexpr size_t kU0Bytes = 64 * 128 * 4;
-constexpr size_t kO0Bytes = 64 * 128 * 2;
+constexpr size_t kU0Bytes = 128 * 64 * 4;
+constexpr size_t kO0Bytes = 128 * 64 * 2;
 constexpr size_t kDecBytes = 128 * 4;
 constexpr size_t kItemBytes = kWqBytes + kKbtBytes + kU0Bytes + kO0Bytes + kDecBytes;
 
@@ -128,6 +129,10 @@ constexpr uint32_t P_BE = P_KB + 32768;  // [K'^T ; V^T] [256][64 tok] fp32 (2 K
 constexpr uint32_t P_BE_KB = 32768;
 constexpr uint32_t P_TBT = P_BE + 65536;  // TB^T [64][64] fp32 (2 K-blocks of 8 KiB)
 constexpr uint32_t P_TBT_KB = 8192;
+// After the solve, the Kb buffer holds TB and P row-major ([t][t'], K-major over t'): the B
+// operands of U0^T = V^T TB^T and O0^T = V^T P^T.
+constexpr uint32_t P_TBN = P_KB;
+constexpr uint32_t P_PN = P_KB + 16384;
 constexpr uint32_t P_XTRA = P_TBT + 16384;
 constexpr int LA = 68;                    // padded row length of the solve scratch
 constexpr uint32_t SCR_A = P_KB;          // beta_r A_kk [64][68] (Kb is dead by then)
@@ -135,8 +140,8 @@ constexpr uint32_t SCR_X = P_XTRA;        // (I + A_kk)^-1 [64][68]
 constexpr uint32_t SCR_P = P_XTRA + 64 * LA * 4;  // 8 warps x [16][8]
 constexpr uint32_t P_MISC = SCR_P + 8 * 128 * 4;
 // Workspace-record staging for the bulk-tensor stores, over Kb, [K'^T ; V^T] and TB^T (all
-// dead once R is complete): W, Q'' and U0 as 4 boxes of [64 rows][32] fp32, O0 as 2 boxes of
-// [64 rows][64] bf16, each in the 128-byte swizzle.
+// dead once the last products are complete): W and Q'' as 4 boxes of [64 rows][32] fp32 in the
+// 128-byte swizzle, U0^T and O0^T in their interleaved record layouts.
 constexpr uint32_t ST_W = P_KB;
 constexpr uint32_t ST_Q = P_KB + 32768;
 constexpr uint32_t ST_U = P_KB + 65536;
@@ -150,7 +155,9 @@ static_assert(P_KB % 1024 == 0 && P_BE % 1024 == 0 && P_TBT % 1024 == 0, "alignm
 constexpr uint32_t TM_XA = 0;    // 128: [Kh ; Qh] (lanes = tokens), the A operand of A1
 constexpr uint32_t TM_A1 = 128;  // 64: [Kh ; Qh] Kb^T -> [0 ; Aqk], the A operand of P
 constexpr uint32_t TM_E = 192;   // 64: [TB ; 0] + [0 ; Aqk] TB = [TB ; P], the A operand of E
-constexpr uint32_t TM_R = 256;   // 256: [TB ; P] [K' | V] = [W | U0 ; P K' | P V]
+constexpr uint32_t TM_R = 256;   // 128: [TB ; P] K' = [W ; P K']
+constexpr uint32_t TM_U0T = 384;  // 64: V^T TB^T = U0^T (lanes = value columns)
+constexpr uint32_t TM_O0T = 448;  // 64: V^T P^T = (P V)^T
 
 struct PrepMisc {
   uint64_t bar_tma, bar_a, bar_p, bar_e, bar_drain;
@@ -508,6 +515,10 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         *f32at(sm, P_TBT + sw128_off32(chh * 32 + j, r, P_TBT_KB)) = v[j];
+#pragma unroll
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(sm + P_TBN + sw128_off32(r, chh * 32 + j, 8192)) =
+            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
     } else {
       float z[16];
 #pragma unroll
@@ -518,80 +529,103 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
     tmem_st_wait();
     fence_proxy_async_smem();
     cta_sync();
-    // ================= E = [TB ; 0] + [0 ; Aqk] TB, then R = E [K' | V]
+    // ================= E = [TB ; 0] + [0 ; Aqk] TB (and U0^T = V^T TB^T); then P row-major;
+    // then R = E K' (and O0^T = V^T P^T)
     if (tid == 0 && !misc->abort) {
-      const uint32_t idp = idesc_make(kFmtTF32, 128, 64, false, false);
+      const uint32_t id64 = idesc_make(kFmtTF32, 128, 64, false, false);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
-        const uint64_t b =
-            sdesc_sw128(sbase + P_TBT + (s >> 2) * P_TBT_KB + (s & 3) * 32, 16, 1024);
-        mma_tf32_ts(tbase + TM_E, tbase + TM_A1 + s * 8, b, idp, 1);
+        const uint32_t kb = (s >> 2) * P_TBT_KB + (s & 3) * 32;
+        mma_tf32_ts(tbase + TM_E, tbase + TM_A1 + s * 8, sdesc_sw128(sbase + P_TBT + kb, 16, 1024),
+                    id64, 1);
+        mma_tf32(tbase + TM_U0T,
+                 sdesc_sw128(sbase + P_BE + (s >> 2) * P_BE_KB + 16384 + (s & 3) * 32, 16, 1024),
+                 sdesc_sw128(sbase + P_TBN + kb, 16, 1024), id64, s > 0);
       }
       mma_commit(&misc->bar_p);
-      if (!mbar_wait(&misc->bar_p, par)) {
-        misc->abort = 1;
-      } else {
-        tc_fence_after();
-        const uint32_t ide = idesc_make(kFmtTF32, 128, 256, false, false);
+    }
+    if (!mbar_wait(&misc->bar_p, par)) misc->abort = 1;
+    tc_fence_after();
+    if (qd >= 2 && need_out) {  // P rows (E lanes 64..127) -> row-major [t][t'] for O0^T
+      const int t = (qd - 2) * 32 + lane;
+      float v[32];
+      tmem_ld32(tbase + lane_base + TM_E + chh * 32, v);
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          const uint64_t b =
-              sdesc_sw128(sbase + P_BE + (s >> 2) * P_BE_KB + (s & 3) * 32, 16, 1024);
-          mma_tf32_ts(tbase + TM_R, tbase + TM_E + s * 8, b, ide, s > 0);
-        }
-        mma_commit(&misc->bar_e);
+      for (int j = 0; j < 32; j += 4)
+        *reinterpret_cast<float4*>(sm + P_PN + sw128_off32(t, chh * 32 + j, 8192)) =
+            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+    }
+    fence_proxy_async_smem();
+    cta_sync();
+    if (tid == 0 && !misc->abort) {
+      const uint32_t id64 = idesc_make(kFmtTF32, 128, 64, false, false);
+      const uint32_t id128 = idesc_make(kFmtTF32, 128, 128, false, false);
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t kbe = (s >> 2) * P_BE_KB + (s & 3) * 32;
+        mma_tf32_ts(tbase + TM_R, tbase + TM_E + s * 8, sdesc_sw128(sbase + P_BE + kbe, 16, 1024),
+                    id128, s > 0);
+        if (need_out)
+          mma_tf32(tbase + TM_O0T, sdesc_sw128(sbase + P_BE + kbe + 16384, 16, 1024),
+                   sdesc_sw128(sbase + P_PN + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024), id64,
+                   s > 0);
       }
+      mma_commit(&misc->bar_e);
     }
     __syncthreads();
     if (misc->abort) break;
     if (!mbar_wait(&misc->bar_e, par)) misc->abort = 1;
     tc_fence_after();
     // ================= workspace record: rows staged in shared memory in the boxes'
-    // 128-byte swizzle (16-byte chunk j of row t at ((j ^ (t & 7)) << 4)), then bulk stores
+    // 128-byte swizzle (16-byte chunk j of row r at ((j ^ (r & 7)) << 4)), then bulk stores
     {
+      // W (token rows 0..63) or Q'' = scale (Q' - P K') (rows 64..127): 64 columns per thread
       const int t = (qd & 1) * 32 + lane;
-      const uint32_t rsw = (uint32_t)t * 128u;
-      const uint32_t tx = (uint32_t)(t & 7);
-      if (qd < 2 || (need_out && chh == 0)) {  // fp32 rows: W, U0 or Q'' = scale (Q' - P K')
-        const uint32_t dst = qd < 2 ? (chh == 0 ? ST_W : ST_U) : ST_Q;
-        const uint32_t src = qd < 2 ? TM_R + chh * 128 : TM_R;
+      if (qd < 2 || need_out) {
+        const uint32_t dst = qd < 2 ? ST_W : ST_Q;
 #pragma unroll 1
-        for (int cc = 0; cc < 128; cc += 32) {
+        for (int cc = chh * 64; cc < chh * 64 + 64; cc += 32) {
           float v[32];
-          tmem_ld32(tbase + lane_base + src + cc, v);
+          tmem_ld32(tbase + lane_base + TM_R + cc, v);
           if (qd >= 2) {
             float qh[32];
             tmem_ld32(tbase + lane_base + TM_XA + cc, qh);
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = p.scale * (qh[j] * misc->erho[cc + j] - v[j]);
           }
-          const uint32_t box = dst + (uint32_t)(cc >> 5) * 8192u + rsw;
+          const uint32_t box = dst + (uint32_t)(cc >> 5) * 8192u + (uint32_t)t * 128u;
 #pragma unroll
           for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<float4*>(sm + box + (((uint32_t)j ^ tx) << 4)) =
+            *reinterpret_cast<float4*>(sm + box + (((uint32_t)j ^ (uint32_t)(t & 7)) << 4)) =
                 make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         }
-      } else if (need_out) {  // O0 = scale P V (bf16)
-#pragma unroll 1
-        for (int cc = 0; cc < 128; cc += 32) {
-          float v[32];
-          tmem_ld32(tbase + lane_base + TM_R + 128 + cc, v);
-          const uint32_t box = ST_O + (uint32_t)(cc >> 6) * 8192u + rsw;
+      }
+      // U0^T and O0^T: value column n = TMEM lane, tokens chh * 32 .. + 31, interleaved
+      const int nn = qd * 32 + lane;
+      {
+        float v[32];
+        tmem_ld32(tbase + lane_base + TM_U0T + chh * 32, v);
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const float* w = v + 8 * k;
-            uint4 pk;
-            __nv_bfloat162 b0 = __floats2bfloat162_rn(p.scale * w[0], p.scale * w[1]);
-            __nv_bfloat162 b1 = __floats2bfloat162_rn(p.scale * w[2], p.scale * w[3]);
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(p.scale * w[4], p.scale * w[5]);
-            __nv_bfloat162 b3 = __floats2bfloat162_rn(p.scale * w[6], p.scale * w[7]);
-            pk.x = *reinterpret_cast<uint32_t*>(&b0);
-            pk.y = *reinterpret_cast<uint32_t*>(&b1);
-            pk.z = *reinterpret_cast<uint32_t*>(&b2);
-            pk.w = *reinterpret_cast<uint32_t*>(&b3);
-            const uint32_t jc = (uint32_t)((cc & 63) >> 3) + (uint32_t)k;
-            *reinterpret_cast<uint4*>(sm + box + ((jc ^ tx) << 4)) = pk;
-          }
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<float4*>(sm + ST_U + ((uint32_t)(chh * 8 + j) * 128u + nn) * 16u) =
+              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+      }
+      if (need_out) {
+        float v[32];
+        tmem_ld32(tbase + lane_base + TM_O0T + chh * 32, v);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float* w = v + 8 * k;
+          uint4 pk;
+          __nv_bfloat162 b0 = __floats2bfloat162_rn(p.scale * w[0], p.scale * w[1]);
+          __nv_bfloat162 b1 = __floats2bfloat162_rn(p.scale * w[2], p.scale * w[3]);
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(p.scale * w[4], p.scale * w[5]);
+          __nv_bfloat162 b3 = __floats2bfloat162_rn(p.scale * w[6], p.scale * w[7]);
+          pk.x = *reinterpret_cast<uint32_t*>(&b0);
+          pk.y = *reinterpret_cast<uint32_t*>(&b1);
+          pk.z = *reinterpret_cast<uint32_t*>(&b2);
+          pk.w = *reinterpret_cast<uint32_t*>(&b3);
+          *reinterpret_cast<uint4*>(sm + ST_O + ((uint32_t)(chh * 4 + k) * 128u + nn) * 16u) = pk;
         }
       }
     }
@@ -601,13 +635,10 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
 #pragma unroll
       for (int kb = 0; kb < 4; ++kb) {
         tma_store_2d(&twq_st, sm + ST_W + kb * 8192, kb * 32, item * 128);
-        tma_store_2d(&tu0_st, sm + ST_U + kb * 8192, kb * 32, item * 64);
         if (need_out) tma_store_2d(&twq_st, sm + ST_Q + kb * 8192, kb * 32, item * 128 + 64);
       }
-      if (need_out) {
-        tma_store_2d(&to0_st, sm + ST_O, 0, item * 64);
-        tma_store_2d(&to0_st, sm + ST_O + 8192, 64, item * 64);
-      }
+      tma_store_3d(&tu0_st, sm + ST_U, 0, 0, item * 16);
+      if (need_out) tma_store_3d(&to0_st, sm + ST_O, 0, 0, item * 8);
       bulk_commit();
     }
     cta_sync();
@@ -628,41 +659,62 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
 }
 
 // ============================================================================ kernel 2: state
+// One CTA per (range, head, 128-column tile of the state): the value columns in prefill /
+// replay, the M or the D half of the augmented state in package mode. The state lives in TMEM
+// transposed, S^T (lane = state column n, 32-bit column = key channel c), as the A operand of
+//   X^T = S^T [W ; Q'']^T   (N = 128: columns 0..63 give U^T, 64..127 the outputs)
+//   Y^T = U^T Kb'           (U^T written to TMEM by the threads, N = 128 channels)
+// whose B operands are the chunk's workspace rows exactly as TMA stages them. Every product is
+// N = 128 wide, and nothing the threads write feeds an MMA through shared memory.
 constexpr uint32_t S_STAGE = 98304;     // one chunk's [W ; Q''] (64 KiB) and Kb'^T (32 KiB)
 constexpr uint32_t S_WQ = 0;            // 4 K-blocks of [128][32] fp32
 constexpr uint32_t S_KBT = 65536;       // 2 K-blocks of [128][32] fp32
-constexpr uint32_t S_SH = 2 * S_STAGE;  // S^T [32 cols][128 ch] fp32 (4 K-blocks of 4 KiB)
-constexpr uint32_t S_UT = S_SH + 16384;  // U^T [32 cols][64 tok] fp32 (2 K-blocks of 4 KiB)
-constexpr uint32_t S_MISC = S_UT + 8192;
-constexpr uint32_t S_SMEM = S_MISC + 128 + 1024;
-constexpr uint32_t TS_X = 0;   // 32 columns: [W ; Q''] S
-constexpr uint32_t TS_Y = 32;  // 32 columns: Kb'^T U
+constexpr uint32_t S_DEC = 2 * S_STAGE;  // 3 x [128] fp32: the chunk decays (ring of 3)
+constexpr uint32_t S_OST = S_DEC + 2048;  // 8 warps x [32 tokens][32 columns] bf16
+constexpr uint32_t S_MISC = S_OST + 8 * 2048;
+constexpr uint32_t S_SMEM = S_MISC + 256 + 1024;
+constexpr uint32_t TS_S = 0;     // 128: S^T
+constexpr uint32_t TS_X = 128;   // 128: X^T
+constexpr uint32_t TS_Y = 256;   // 128: Y^T
+constexpr uint32_t TS_U = 384;   // 64: U^T
+constexpr int kStateThreads = kThreads + 32;  // 8 compute warps + 1 issuer warp
 
 struct StateMisc {
-  uint64_t full[2], bar_x, bar_y, bar_drain;
+  uint64_t full[2];     // TMA: chunk j's record landed in stage j & 1 (and decay slot j % 3)
+  uint64_t s_ready[2];  // compute warps: S^T channels 64 h .. 64 h + 63 written
+  uint64_t u_ready[2];  // compute warps: U^T tokens 32 h .. 32 h + 31 written
+  uint64_t bar_x, bar_y, bar_drain;
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(StateMisc) <= 128, "misc overflow");
+static_assert(sizeof(StateMisc) <= 256, "misc overflow");
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Shared-memory descriptor advanced by a byte offset (the start-address field is the low 14
+// bits of address >> 4; no carry for offsets that keep the operand inside shared memory).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
+// Compute warp w (0..7): TMEM lane quarter w % 4, so state column n = 32 (w % 4) + lane of the
+// tile; half h = w / 4 of the channels (S update) and of the tokens (U and outputs). The issuer
+// warp (8) waits on the per-half barriers and issues the MMAs and the TMA loads. The compute
+// warps synchronise with it through mbarriers only.
+__global__ void __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const __grid_constant__ ChunkParams p,
                    const __grid_constant__ CUtensorMap twq,
-                   const __grid_constant__ CUtensorMap tkbt, const Ws ws) {
+                   const __grid_constant__ CUtensorMap tkbt,
+                   const __grid_constant__ CUtensorMap tdec,
+                   const __grid_constant__ CUtensorMap tout, const Ws ws) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   StateMisc* misc = reinterpret_cast<StateMisc*>(sm + S_MISC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int qd = warp & 3, chh = warp >> 2;
+  const bool issuer = warp == 8;
+  const int qd = warp & 3, hf = (warp >> 2) & 1;
   const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
   const int tile = blockIdx.x, h = blockIdx.y, ridx = blockIdx.z;
   const int H = p.H;
   const bool pkg = p.package != 0;
-  const int j0 = tile * TW;
-  const bool mcols = pkg && j0 < DK;
-  const int vcol0 = pkg ? j0 - DK : j0;
-  const int c = qd * 32 + lane;  // state row (key channel); token row of U (c < 64) / O (c - 64)
-  const int col0 = chh * 16;     // 16 of the tile's columns
+  const bool mcols = pkg && tile == 0;      // package mode: tile 0 = M, tile 1 = D
+  const int n = qd * 32 + lane;              // state column of this thread within the tile
 
   int t_begin = 0, t_end = p.total_tokens;
   if (p.offsets) {
@@ -677,221 +729,281 @@ chunk_state_kernel(const __grid_constant__ ChunkParams p,
   const int slot0 = t_begin / C + ridx;
 
   if (warp == 0) {
-    tmem_alloc(&misc->tmem_base, 64);
+    tmem_alloc(&misc->tmem_base, 512);
     tmem_relinquish();
   }
   if (tid == 0) {
     mbar_init(&misc->full[0], 1);
     mbar_init(&misc->full[1], 1);
+    mbar_init(&misc->s_ready[0], 4);
+    mbar_init(&misc->s_ready[1], 4);
+    mbar_init(&misc->u_ready[0], 4);
+    mbar_init(&misc->u_ready[1], 4);
     mbar_init(&misc->bar_x, 1);
     mbar_init(&misc->bar_y, 1);
     mbar_init(&misc->bar_drain, 1);
     misc->abort = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&twq);
-    tma_prefetch_desc(&tkbt);
   }
-  // state tile in registers: row c, columns col0 .. col0 + 15
-  float s[16];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const int col = col0 + j;
-    float x = 0.0f;
-    if (pkg) x = (mcols && c == j0 + col) ? 1.0f : 0.0f;
-    else if (p.init) x = p.init[(((int64_t)ridx * H + h) * DK + c) * DK + j0 + col];
-    s[j] = x;
-  }
-  auto store_sh = [&]() {  // S^T as the K-major B operand: element (row = column, k = c)
-#pragma unroll
-    for (int j = 0; j < 16; ++j) *f32at(sm, S_SH + sw128_off32(col0 + j, c, 4096)) = s[j];
-  };
-  store_sh();
-  fence_proxy_async_smem();
   cta_sync();
   const uint32_t tbase = misc->tmem_base;
   const uint32_t sbase = smem_u32(sm);
 
-  auto issue_tma = [&](int j) {  // chunk j into stage j & 1
-    const int item = (slot0 + j) * H + h;
-    uint8_t* st = sm + (j & 1) * S_STAGE;
-    uint64_t* bar = &misc->full[j & 1];
-    mbar_arrive_expect_tx(bar, S_STAGE);
+  if (issuer) {
+    // ------------------------------------------------------------ issuer warp (lane 0)
+    if (lane == 0) {
+      tma_prefetch_desc(&twq);
+      tma_prefetch_desc(&tkbt);
+      tma_prefetch_desc(&tdec);
+      auto issue_tma = [&](int j) {  // chunk j into stage j & 1 and decay slot j % 3
+        const int item = (slot0 + j) * H + h;
+        uint8_t* st = sm + (j & 1) * S_STAGE;
+        uint64_t* bar = &misc->full[j & 1];
+        mbar_arrive_expect_tx(bar, S_STAGE + 512);
 #pragma unroll
-    for (int kb = 0; kb < 4; ++kb)
-      tma_load_2d(st + S_WQ + kb * 16384, &twq, bar, kb * 32, item * 128);
+        for (int kb = 0; kb < 4; ++kb)
+          tma_load_2d(st + S_WQ + kb * 16384, &twq, bar, kb * 32, item * 128);
 #pragma unroll
-    for (int kb = 0; kb < 2; ++kb)
-      tma_load_2d(st + S_KBT + kb * 16384, &tkbt, bar, kb * 32, item * 128);
-  };
-  int tma_last = -1;  // thread 0: last chunk whose loads were issued
-  if (tid == 0) {
-    for (int j = 0; j < 2 && j < nch; ++j) {
-      issue_tma(j);
-      tma_last = j;
-    }
-  }
-  // per-chunk register operands (prefetched one chunk ahead)
-  auto load_regs = [&](int j, float* u0, uint4* o0, float& dec) {
-    const int64_t item = (int64_t)(slot0 + j) * H + h;
-    dec = __ldg(ws.dec + item * DK + c);
-    if (qd < 2) {
-      if (!mcols) {
-        const float4* src =
-            reinterpret_cast<const float4*>(ws.u0 + (item * 64 + c) * 128 + vcol0 + col0);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float4 t4 = __ldg(src + i);
-          u0[4 * i] = t4.x;
-          u0[4 * i + 1] = t4.y;
-          u0[4 * i + 2] = t4.z;
-          u0[4 * i + 3] = t4.w;
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) u0[i] = 0.0f;
+        for (int kb = 0; kb < 2; ++kb)
+          tma_load_2d(st + S_KBT + kb * 16384, &tkbt, bar, kb * 32, item * 128);
+        tma_load_2d(sm + S_DEC + (j % 3) * 512, &tdec, bar, 0, item);
+        // the compute warps read this chunk's U0^T / O0^T rows with plain loads one chunk
+        // ahead; bring them into L2 now
+        if (!mcols) bulk_prefetch_l2(ws.u0 + (int64_t)item * 8192, 32768);
+        if (!pkg) bulk_prefetch_l2(ws.o0 + (int64_t)item * 8192, 16384);
+      };
+      int tma_last = -1;
+      for (int j = 0; j < 2 && j < nch; ++j) {
+        issue_tma(j);
+        tma_last = j;
       }
-    } else if (!pkg) {
-      const uint4* src =
-          reinterpret_cast<const uint4*>(ws.o0 + (item * 64 + (c - 64)) * 128 + j0 + col0);
-      o0[0] = __ldg(src);
-      o0[1] = __ldg(src + 1);
-    }
-  };
-  float u0[16], nu0[16], dec = 0.0f, ndec = 0.0f;
-  uint4 o0[2], no0[2];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    u0[i] = 0.0f;
-    nu0[i] = 0.0f;
-  }
-  o0[0] = o0[1] = no0[0] = no0[1] = make_uint4(0, 0, 0, 0);
-  if (nch > 0) load_regs(0, u0, o0, dec);
-  __syncthreads();
-
-  bool ok = true;
-  for (int j = 0; j < nch; ++j) {
-    const int t0 = t_begin + j * C;
-    const int n = min(C, t_end - t0);
-    const uint32_t par = (uint32_t)j & 1u;
-    const uint32_t st = (uint32_t)(j & 1) * S_STAGE;
-    // ================= X = [W ; Q''] S
-    if (tid == 0) {
-      if (!mbar_wait(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u)) {
-        misc->abort = 1;
-      } else {
-        tc_fence_after();
-        const uint32_t idx = idesc_make(kFmtTF32, 128, 32, false, false);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const uint64_t a =
-              sdesc_sw128(sbase + st + S_WQ + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-          const uint64_t b = sdesc_sw128(sbase + S_SH + (k >> 2) * 4096 + (k & 3) * 32, 16, 1024);
-          mma_tf32(tbase + TS_X, a, b, idx, k > 0);
-        }
-        mma_commit(&misc->bar_x);
-      }
-    }
-    if (j + 1 < nch) load_regs(j + 1, nu0, no0, ndec);  // next chunk's register operands
-    if (!mbar_wait(&misc->bar_x, par)) misc->abort = 1;
-    tc_fence_after();
-    // ================= U = U0 - W S (token rows), kept as U^T for the next product
-    float x[16];
-    tmem_ld16(tbase + lane_base + TS_X + col0, x);
-    if (qd < 2) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i)
-        *f32at(sm, S_UT + sw128_off32(col0 + i, c, 4096)) = u0[i] - x[i];
-    }
-    fence_proxy_async_smem();
-    cta_sync();
-    if (misc->abort) {
-      ok = false;
-      break;
-    }
-    // ================= Y = Kb'^T U; outputs O = Q'' S + O0 meanwhile
-    if (tid == 0) {
-      const uint32_t idy = idesc_make(kFmtTF32, 128, 32, false, false);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const uint64_t a =
-            sdesc_sw128(sbase + st + S_KBT + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-        const uint64_t b = sdesc_sw128(sbase + S_UT + (k >> 2) * 4096 + (k & 3) * 32, 16, 1024);
-        mma_tf32(tbase + TS_Y, a, b, idy, k > 0);
-      }
-      mma_commit(&misc->bar_y);
-    }
-    if (qd >= 2 && !pkg && p.o) {
-      const int r = c - 64;
-      if (r < n) {
-        __nv_bfloat16* o = (__nv_bfloat16*)p.o + ((int64_t)(t0 + r) * H + h) * DK + j0 + col0;
+      const uint32_t idesc = idesc_make(kFmtTF32, 128, 128, false, false);
+      bool ok = true;
+      for (int j = 0; j < nch && ok; ++j) {
+        const uint32_t par = (uint32_t)j & 1u;
+        const uint32_t st = (uint32_t)(j & 1) * S_STAGE;
+        const uint64_t d_wq = sdesc_sw128(sbase + st + S_WQ, 16, 1024);
+        const uint64_t d_kbt = sdesc_sw128(sbase + st + S_KBT, 16, 1024);
+        ok = mbar_wait(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u);
+        // X^T = S^T [W ; Q'']^T, channel half by channel half as S^T is written
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          float ob[8];
-          unpack8(o0[hh], ob);
-          const float* xx = x + 8 * hh;
-          uint4 pk;
-          __nv_bfloat162 b0 = __floats2bfloat162_rn(xx[0] + ob[0], xx[1] + ob[1]);
-          __nv_bfloat162 b1 = __floats2bfloat162_rn(xx[2] + ob[2], xx[3] + ob[3]);
-          __nv_bfloat162 b2 = __floats2bfloat162_rn(xx[4] + ob[4], xx[5] + ob[5]);
-          __nv_bfloat162 b3 = __floats2bfloat162_rn(xx[6] + ob[6], xx[7] + ob[7]);
-          pk.x = *reinterpret_cast<uint32_t*>(&b0);
-          pk.y = *reinterpret_cast<uint32_t*>(&b1);
-          pk.z = *reinterpret_cast<uint32_t*>(&b2);
-          pk.w = *reinterpret_cast<uint32_t*>(&b3);
-          *reinterpret_cast<uint4*>(o + 8 * hh) = pk;
+          ok = ok && mbar_wait(&misc->s_ready[hh], par);
+          tc_fence_after();
+          if (ok) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int ks = hh * 8 + k;  // K-step: channels 8 ks .. 8 ks + 7
+              mma_tf32_ts(tbase + TS_X, tbase + TS_S + ks * 8,
+                          desc_add(d_wq, (ks >> 2) * 16384 + (ks & 3) * 32), idesc, ks > 0);
+            }
+          }
+        }
+        if (!ok) break;
+        mma_commit(&misc->bar_x);
+        // Y^T = U^T Kb', token half by token half as U^T is written
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          ok = ok && mbar_wait(&misc->u_ready[hh], par);
+          tc_fence_after();
+          if (ok) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int ks = hh * 4 + k;  // K-step: tokens 8 ks .. 8 ks + 7
+              mma_tf32_ts(tbase + TS_Y, tbase + TS_U + ks * 8,
+                          desc_add(d_kbt, (ks >> 2) * 16384 + (ks & 3) * 32), idesc, ks > 0);
+            }
+          }
+        }
+        if (!ok) break;
+        mma_commit(&misc->bar_y);
+        // the stage is free once Y has completed: load chunk j + 2 into it
+        if (j + 2 < nch) {
+          ok = mbar_wait(&misc->bar_y, par);
+          if (ok) {
+            issue_tma(j + 2);
+            tma_last = j + 2;
+          }
         }
       }
-    }
-    if (!mbar_wait(&misc->bar_y, par)) misc->abort = 1;
-    tc_fence_after();
-    // ================= S = Diag(e^gamma_C) S + Y; this chunk's stage is free
-    if (tid == 0 && j + 2 < nch && !misc->abort) {
-      issue_tma(j + 2);
-      tma_last = j + 2;
-    }
-    {
-      float y[16];
-      tmem_ld16(tbase + lane_base + TS_Y + col0, y);
-#pragma unroll
-      for (int i = 0; i < 16; ++i) s[i] = fmaf(dec, s[i], y[i]);
-      store_sh();
-    }
-    fence_proxy_async_smem();
-    cta_sync();
-    if (misc->abort) {
-      ok = false;
-      break;
-    }
-#pragma unroll
-    for (int i = 0; i < 16; ++i) u0[i] = nu0[i];
-    o0[0] = no0[0];
-    o0[1] = no0[1];
-    dec = ndec;
-  }
-  if (misc->abort) ok = false;
-  if (!ok) {
-    if (tid == 0) {
-      if (p.status) atomicOr(p.status, KDA_STATUS_TIMEOUT);
-      mma_commit(&misc->bar_drain);
-      mbar_wait(&misc->bar_drain, 0, 100000000ull);
-      // the last two issued loads are the only ones that can still be in flight
-      for (int j = tma_last > 0 ? tma_last - 1 : 0; j <= tma_last; ++j)
-        mbar_wait(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u, 100000000ull);
+      if (!ok) {
+        misc->abort = 1;
+        mma_commit(&misc->bar_drain);
+        mbar_wait(&misc->bar_drain, 0, 100000000ull);
+        for (int j = tma_last > 0 ? tma_last - 1 : 0; j <= tma_last; ++j)
+          mbar_wait(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u, 100000000ull);
+      }
     }
   } else {
+    // ------------------------------------------------------------ compute warps
     const int64_t sh = (int64_t)ridx * H + h;
-    float* dst = nullptr;
-    if (pkg) dst = mcols ? p.M + (sh * DK + c) * DK + j0 : p.D + (sh * DK + c) * DK + vcol0;
-    else if (p.final_state) dst = p.final_state + (sh * DK + c) * DK + j0;
-    if (dst) {
+    const int vcol = pkg ? (mcols ? -1 : n) : n;  // value column of U0 / outputs (-1: none)
+    {  // S^T rows n, channels 64 hf .. 64 hf + 63
+      float v[32];
+#pragma unroll 1
+      for (int cc = hf * 64; cc < hf * 64 + 64; cc += 32) {
 #pragma unroll
-      for (int j = 0; j < 16; j += 4)
-        *reinterpret_cast<float4*>(dst + col0 + j) =
-            make_float4(s[j], s[j + 1], s[j + 2], s[j + 3]);
+        for (int i = 0; i < 32; ++i) {
+          const int c = cc + i;
+          float x = 0.0f;
+          if (pkg) x = (mcols && c == n) ? 1.0f : 0.0f;
+          else if (p.init) x = p.init[(sh * DK + c) * DK + n];
+          v[i] = x;
+        }
+        tmem_st32(tbase + lane_base + TS_S + cc, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&misc->s_ready[hf]);
+    }
+    // per-chunk register operands, loaded one chunk ahead: U0^T[n][32 hf ..] (32 fp32) and
+    // O0^T[n][32 hf ..] (32 bf16)
+    auto load_regs = [&](int j, float4* u0, uint4* o0) {
+      const int64_t item = (int64_t)(slot0 + j) * H + h;
+      if (vcol >= 0) {
+        const float4* src = reinterpret_cast<const float4*>(ws.u0 + item * 8192) + hf * 8 * 128 + vcol;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) u0[i] = __ldg(src + i * 128);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) u0[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      if (!pkg) {
+        const uint4* src = reinterpret_cast<const uint4*>(ws.o0 + item * 8192) + hf * 4 * 128 + n;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) o0[i] = __ldg(src + i * 128);
+      }
+    };
+    float4 u0[8];
+    uint4 o0[4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) u0[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o0[i] = make_uint4(0, 0, 0, 0);
+    if (nch > 0) load_regs(0, u0, o0);
+
+    for (int j = 0; j < nch; ++j) {
+      const int t0 = t_begin + j * C;
+      const int nvalid = min(C, t_end - t0);
+      const uint32_t par = (uint32_t)j & 1u;
+      // ================= U^T = U0^T - (W S)^T (tokens 32 hf ..), then the outputs
+      if (!mbar_wait_relaxed(&misc->bar_x, par)) misc->abort = 1;
+      tc_fence_after();
+      {
+        float x[32];
+        tmem_ld32(tbase + lane_base + TS_X + hf * 32, x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          x[4 * i] = u0[i].x - x[4 * i];
+          x[4 * i + 1] = u0[i].y - x[4 * i + 1];
+          x[4 * i + 2] = u0[i].z - x[4 * i + 2];
+          x[4 * i + 3] = u0[i].w - x[4 * i + 3];
+        }
+        tmem_st32(tbase + lane_base + TS_U + hf * 32, x);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_relaxed(&misc->u_ready[hf]);
+      }
+      // output values of tokens 32 hf .. 32 hf + 31: O^T[n][t] = (Q'' S)^T + O0^T
+      uint32_t ob16[16];
+      if (!pkg && p.o) {
+        float x[32];
+        tmem_ld32(tbase + lane_base + TS_X + 64 + hf * 32, x);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float ob[8];
+          unpack8(o0[k], ob);
+#pragma unroll
+          for (int e = 0; e < 8; e += 2) {
+            __nv_bfloat162 b = __floats2bfloat162_rn(x[8 * k + e] + ob[e], x[8 * k + e + 1] + ob[e + 1]);
+            ob16[4 * k + e / 2] = *reinterpret_cast<uint32_t*>(&b);
+          }
+        }
+      }
+      // outputs: through this warp's staging area and a bulk store while Y is on the tensor
+      // core; partial blocks of a range's last chunk with plain stores
+      if (!pkg && p.o) {
+        if (nvalid >= hf * 32 + 32) {
+          // this warp's 32 x 32 output block through its staging area and one bulk store
+          uint8_t* ost = sm + S_OST + warp * 2048;
+          if (lane == 0) bulk_wait_read0();  // the previous block has left the staging area
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&ob16[i]);
+            *reinterpret_cast<__nv_bfloat16*>(ost + (2 * i) * 64 + lane * 2) = b.x;
+            *reinterpret_cast<__nv_bfloat16*>(ost + (2 * i + 1) * 64 + lane * 2) = b.y;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(&tout, ost, qd * 32, h, t0 + hf * 32);
+            bulk_commit();
+          }
+        } else {
+          __nv_bfloat16* o = (__nv_bfloat16*)p.o + ((int64_t)t0 * H + h) * DK + n;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int t = hf * 32 + 2 * i;
+            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&ob16[i]);
+            if (t < nvalid) o[(int64_t)t * H * DK] = b.x;
+            if (t + 1 < nvalid) o[(int64_t)(t + 1) * H * DK] = b.y;
+          }
+        }
+      }
+      // ================= S^T = S^T Diag(e^gamma_C) + Y^T (channels 64 hf ..)
+      if (!mbar_wait_relaxed(&misc->bar_y, par)) misc->abort = 1;
+      tc_fence_after();
+      {
+        const float* dec = f32at(sm, S_DEC + (j % 3) * 512);
+#pragma unroll 1
+        for (int cc = hf * 64; cc < hf * 64 + 64; cc += 32) {
+          uint32_t y[32], sr[32];
+          tmem_ld32_nowait(tbase + lane_base + TS_Y + cc, y);
+          tmem_ld32_nowait(tbase + lane_base + TS_S + cc, sr);
+          tmem_ld_wait();
+          float s[32];
+#pragma unroll
+          for (int i = 0; i < 32; i += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dec + cc + i);
+            s[i] = fmaf(d4.x, __uint_as_float(sr[i]), __uint_as_float(y[i]));
+            s[i + 1] = fmaf(d4.y, __uint_as_float(sr[i + 1]), __uint_as_float(y[i + 1]));
+            s[i + 2] = fmaf(d4.z, __uint_as_float(sr[i + 2]), __uint_as_float(y[i + 2]));
+            s[i + 3] = fmaf(d4.w, __uint_as_float(sr[i + 3]), __uint_as_float(y[i + 3]));
+          }
+          tmem_st32_nowait(tbase + lane_base + TS_S + cc, s);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && j + 1 < nch) mbar_arrive_relaxed(&misc->s_ready[hf]);
+      }
+      // the next chunk's register operands (this chunk's are consumed), loaded while the next
+      // chunk's X is on the tensor core (the issuer has brought them into L2)
+      if (j + 1 < nch) load_regs(j + 1, u0, o0);
+      if (misc->abort) break;
     }
   }
+  if (!issuer && lane == 0) bulk_wait0();  // this warp's output stores have completed
   cta_sync();
-  if (warp == 0) tmem_dealloc(tbase, 64);
+  if (!issuer && !misc->abort) {  // exit state rows c of column n (coalesced across lanes)
+    const int64_t sh = (int64_t)ridx * H + h;
+    float* dst = nullptr;
+    if (pkg) dst = mcols ? p.M + sh * DK * DK + n : p.D + sh * DK * DK + n;
+    else if (p.final_state) dst = p.final_state + sh * DK * DK + n;
+    if (dst) {
+#pragma unroll 1
+      for (int cc = hf * 64; cc < hf * 64 + 64; cc += 32) {
+        float s[32];
+        tmem_ld32(tbase + lane_base + TS_S + cc, s);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dst[(int64_t)(cc + i) * DK] = s[i];
+      }
+    }
+  }
+  if (misc->abort && tid == 0 && p.status) atomicOr(p.status, KDA_STATUS_TIMEOUT);
+  cta_sync();
+  if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
 // ---------------------------------------------------------------- host side
@@ -964,6 +1076,50 @@ bool make_map_ws(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, 
   return r == CUDA_SUCCESS;
 }
 
+// Interleaved record array [groups][128][w] (fp32 w = 4, or bf16 w = 8) as a 3-D tensor
+// (w, 128, groups); box (w, 128, 64 / w): one item's U0^T or O0^T.
+bool make_map_ileave(CUtensorMap* m, const void* ptr, uint64_t groups, uint32_t w, bool bf16) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)w, 128, (cuuint64_t)groups};
+  cuuint64_t strides[2] = {16, 2048};
+  cuuint32_t box[3] = {w, 128, 64 / w};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                   const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// o [T, H, 128] bf16 as a 3-D tensor (128, H, T); box (32, 1, 32): one warp's output block.
+bool make_map_out(CUtensorMap* m, const void* ptr, int T, int H) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)H * DK * 2};
+  cuuint32_t box[3] = {32, 1, 32};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// dec [items][128] fp32 as a 2-D tensor (128, items); box (128, 1): one item's decays.
+bool make_map_dec(CUtensorMap* m, const float* ptr, uint64_t items) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)DK, (cuuint64_t)items};
+  cuuint64_t strides[1] = {(cuuint64_t)DK * 4};
+  cuuint32_t box[2] = {(cuuint32_t)DK, 1};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(ptr), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int64_t n_items_of(int n_ranges, int total_tokens, int H) {
   return ((int64_t)total_tokens / C + n_ranges) * H;
 }
@@ -1008,17 +1164,20 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   ws.o0 = (__nv_bfloat16*)(base + (size_t)n_items * (kWqBytes + kKbtBytes + kU0Bytes));
   ws.dec = (float*)(base + (size_t)n_items * (kWqBytes + kKbtBytes + kU0Bytes + kO0Bytes));
 
-  CUtensorMap mq, mk, mv, mg, mb, mwq, mkbt, swq, su0, so0;
+  CUtensorMap mq, mk, mv, mg, mb, mwq, mkbt, mdec, swq, su0, so0, mo;
   const void* qp = p.q ? p.q : p.k;
-  const uint64_t rows128 = (uint64_t)n_items * 128, rows64 = (uint64_t)n_items * 64;
+  const uint64_t rows128 = (uint64_t)n_items * 128;
   if (!make_map3(&mq, qp, p.total_tokens, p.H, 64, false) ||
       !make_map3(&mk, p.k, p.total_tokens, p.H, 64, false) ||
       !make_map3(&mv, p.v, p.total_tokens, p.H, 64, false) ||
       !make_map3(&mg, p.g, p.total_tokens, p.H, 32, true) ||
       !make_map_beta(&mb, p.beta, p.total_tokens, p.H) ||
       !make_map_ws(&mwq, ws.wq, rows128, 128, 128) || !make_map_ws(&mkbt, ws.kbt, rows128, 64, 128) ||
-      !make_map_ws(&swq, ws.wq, rows128, 128, 64) || !make_map_ws(&su0, ws.u0, rows64, 128, 64) ||
-      !make_map_ws(&so0, ws.o0, rows64, 128, 64, true))
+      !make_map_dec(&mdec, ws.dec, (uint64_t)n_items) ||
+      !make_map_ws(&swq, ws.wq, rows128, 128, 64) ||
+      !make_map_ileave(&su0, ws.u0, (uint64_t)n_items * 16, 4, false) ||
+      !make_map_ileave(&so0, ws.o0, (uint64_t)n_items * 8, 8, true) ||
+      !make_map_out(&mo, p.o ? p.o : p.k, p.total_tokens, p.H))
     return set_error(KDA_ERR_CUDA, "tensor-core chunk path: cuTensorMapEncodeTiled failed");
   cudaError_t e =
       cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
@@ -1034,9 +1193,8 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   count_launches(1);
   kda_status st = check_launch("tensor-core chunk prep kernel");
   if (st != KDA_OK) return st;
-  const int cols = p.package ? (p.dk + p.dv) : p.dv;
-  dim3 grid2(cols / TW, p.H, p.n_ranges);
-  chunk_state_kernel<<<grid2, kThreads, S_SMEM, s>>>(p, mwq, mkbt, ws);
+  dim3 grid2(p.package ? 2 : 1, p.H, p.n_ranges);
+  chunk_state_kernel<<<grid2, kStateThreads, S_SMEM, s>>>(p, mwq, mkbt, mdec, mo, ws);
   count_launches(1);
   return check_launch("tensor-core chunk state kernel");
 }
