@@ -91,7 +91,8 @@ KDA_API uint64_t kda_launch_count(void);
  * 0 when such a call needs none (fp32 inputs, dk = dv = 64, or H not a multiple of 4, all
  * served by the CUDA-core kernel). The tensor-core path precomputes every state-independent
  * factor of each (64-token chunk, head) into one record of 147,968 bytes; it keeps
- * (total_tokens / 64 + n_ranges) * H records.
+ * R = (total_tokens / 64 + n_ranges) * H records, then a 4-byte ready flag per record
+ * (rounded up to a multiple of 256 bytes): R * 147968 + roundup(4 R, 256) bytes.
  */
 KDA_API size_t kda_chunk_workspace(kda_dtype dt, int n_ranges, int total_tokens, int H, int dk,
                                    int dv);

@@ -170,15 +170,24 @@ struct PrepMisc {
 };
 static_assert(sizeof(PrepMisc) <= 2048, "misc overflow");
 
-__global__ void __launch_bounds__(kThreads, 1)
-chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ CUtensorMap tmq,
-                  const __grid_constant__ CUtensorMap tmk,
-                  const __grid_constant__ CUtensorMap tmv,
-                  const __grid_constant__ CUtensorMap tmg,
-                  const __grid_constant__ CUtensorMap tmb,
-                  const __grid_constant__ CUtensorMap twq_st,
-                  const __grid_constant__ CUtensorMap tu0_st,
-                  const __grid_constant__ CUtensorMap to0_st, const Ws ws, const int n_items) {
+// The prep CTA's 256 threads synchronise on named barrier 1 (a fused launch runs them next to
+// a ninth, idle warp).
+__device__ __forceinline__ void pbar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void psync() {
+  tc_fence_before();
+  pbar();
+  tc_fence_after();
+}
+
+// Processes items first, first + stride, ... (those holding a chunk). With `flags`, sets
+// flags[item] (release, gpu scope) once the item's record is complete in global memory.
+__device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap& tmq,
+                                         const CUtensorMap& tmk, const CUtensorMap& tmv,
+                                         const CUtensorMap& tmg, const CUtensorMap& tmb,
+                                         const CUtensorMap& twq_st, const CUtensorMap& tu0_st,
+                                         const CUtensorMap& to0_st, const Ws& ws,
+                                         const int n_items, const int first, const int stride,
+                                         uint32_t* flags) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   PrepMisc* misc = reinterpret_cast<PrepMisc*>(sm + P_MISC);
@@ -207,7 +216,7 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
     tma_prefetch_desc(&tmb);
     if (need_out) tma_prefetch_desc(&tmq);
   }
-  cta_sync();
+  psync();
   const uint32_t tbase = misc->tmem_base;
   const uint32_t sbase = smem_u32(sm);
 
@@ -229,7 +238,7 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
   // thread 0: finds this CTA's next item holding a chunk, from `from` on, and issues its loads
   auto advance = [&](int from) {
     int it = from, t0 = 0, n = 0, hh = 0;
-    while (it < n_items && !item_chunk(p, it, t0, n, hh)) it += gridDim.x;
+    while (it < n_items && !item_chunk(p, it, t0, n, hh)) it += stride;
     misc->nxt[0] = it;
     misc->nxt[1] = t0;
     misc->nxt[2] = n;
@@ -242,8 +251,9 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
   constexpr int kLoader = 32;
   bool tma_out = false;  // loader: a load is in flight, completing phase parity tma_par
   uint32_t tma_par = 0;
-  if (tid == kLoader) tma_out = advance(blockIdx.x);
-  cta_sync();
+  int prev_item = -1;    // loader: item whose record's store group is the latest but one
+  if (tid == kLoader) tma_out = advance(first);
+  psync();
 
   uint32_t k_it = 0;
   for (;;) {
@@ -269,7 +279,7 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
       }
       misc->part[half][c] = acc;
       if (tid < C) misc->beta[tid] = (tid < n) ? f32at(sm, P_STG_B)[tid * 4 + (h & 3)] : 0.0f;
-      __syncthreads();
+      pbar();
       const float p0 = misc->part[0][c], p1 = misc->part[1][c];
       const float rho2 = 0.5f * (p0 + p1);  // log2 units
       if (half == 0) {
@@ -286,8 +296,8 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
         *f32at(sm, gbase + (uint32_t)i * 128u + ((xg ^ (uint32_t)(i & 7)) << 4)) = gam - rho2;
       }
     }
-    if (tid == 0) bulk_wait_read0();  // the previous record has left the staging buffers
-    __syncthreads();
+    if (tid == kLoader) bulk_wait_read0();  // the previous record has left the staging buffers
+    pbar();
     // ================= operands (row role: token t; key rows in warps 0,1,4,5, query rows
     // and values in warps 2,3,6,7; channel half chh)
     {
@@ -380,7 +390,7 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
     }
     tmem_st_wait();
     fence_proxy_async_smem();
-    cta_sync();
+    psync();
     // ================= A1 = [Kh; Qh] Kb^T; the staging is free: load the next item
     if (tid == 0 && !misc->abort) {
       const uint32_t ida = idesc_make(kFmtTF32, 128, 64, false, false);
@@ -393,7 +403,7 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
       mma_commit(&misc->bar_a);
     }
     if (tid == kLoader && !misc->abort) {
-      tma_out = advance(item + gridDim.x);
+      tma_out = advance(item + stride);
       tma_par = par ^ 1u;
     }
     if (!mbar_wait(&misc->bar_a, par)) misc->abort = 1;
@@ -424,7 +434,7 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
       tmem_st16(tbase + lane_base + TM_A1 + chh * 32 + 16, v + 16);
       tmem_st_wait();
     }
-    cta_sync();
+    psync();
     // ================= T = (I + A_kk)^-1 in 16 x 16 blocks
     {
       const float* Akk = f32at(sm, SCR_A);
@@ -452,7 +462,7 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
           X[(I * 16 + rr) * LA + J * 16 + cc] = 0.0f;
         }
       }
-      __syncthreads();
+      pbar();
       // off-diagonal blocks by distance d: X_IJ = -X_II sum_{L=J}^{I-1} A_IL X_LJ (J = I - d).
       // Warp w < 2 (4 - d) owns block J = w / 2 and its 8-column half w % 2; both 16 x 16
       // block products run as warp-level 3xTF32 MMAs (fp32-level accuracy), the partial
@@ -493,7 +503,7 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
           xr[8 * LA + 1] = -e[3];
           __syncwarp();
         }
-        __syncthreads();
+        pbar();
       }
     }
     // ================= TB = T Diag(beta): TMEM E lanes 0..63 (lanes 64..127 zero) and TB^T
@@ -528,7 +538,7 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
     }
     tmem_st_wait();
     fence_proxy_async_smem();
-    cta_sync();
+    psync();
     // ================= E = [TB ; 0] + [0 ; Aqk] TB (and U0^T = V^T TB^T); then P row-major;
     // then R = E K' (and O0^T = V^T P^T)
     if (tid == 0 && !misc->abort) {
@@ -556,7 +566,7 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
             make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
     }
     fence_proxy_async_smem();
-    cta_sync();
+    psync();
     if (tid == 0 && !misc->abort) {
       const uint32_t id64 = idesc_make(kFmtTF32, 128, 64, false, false);
       const uint32_t id128 = idesc_make(kFmtTF32, 128, 128, false, false);
@@ -572,7 +582,7 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
       }
       mma_commit(&misc->bar_e);
     }
-    __syncthreads();
+    pbar();
     if (misc->abort) break;
     if (!mbar_wait(&misc->bar_e, par)) misc->abort = 1;
     tc_fence_after();
@@ -630,8 +640,8 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
       }
     }
     fence_proxy_async_smem();
-    cta_sync();
-    if (tid == 0) {
+    psync();
+    if (tid == kLoader) {
 #pragma unroll
       for (int kb = 0; kb < 4; ++kb) {
         tma_store_2d(&twq_st, sm + ST_W + kb * 8192, kb * 32, item * 128);
@@ -640,8 +650,19 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
       tma_store_3d(&tu0_st, sm + ST_U, 0, 0, item * 16);
       if (need_out) tma_store_3d(&to0_st, sm + ST_O, 0, 0, item * 8);
       bulk_commit();
+      // the previous item's record is complete once its store group is: publish it (its
+      // generic stores, Kb'^T and the decays, were ordered before this thread's release by
+      // the barriers since)
+      if (flags) {
+        if (prev_item >= 0) {
+          bulk_wait1();
+          fence_proxy_async_global();
+          st_release_gpu(flags + prev_item, 1u);
+        }
+        prev_item = item;
+      }
     }
-    cta_sync();
+    psync();
     if (misc->abort) break;
     ++k_it;
   }
@@ -653,9 +674,28 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
     }
     if (tid == kLoader && tma_out) mbar_wait(&misc->bar_tma, tma_par, 100000000ull);
   }
-  if (tid == 0) bulk_wait0();
-  cta_sync();
+  if (tid == kLoader) {
+    bulk_wait0();
+    if (flags && prev_item >= 0 && !misc->abort) {
+      fence_proxy_async_global();
+      st_release_gpu(flags + prev_item, 1u);
+    }
+  }
+  psync();
   if (warp == 0) tmem_dealloc(tbase, 512);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ CUtensorMap tmq,
+                  const __grid_constant__ CUtensorMap tmk,
+                  const __grid_constant__ CUtensorMap tmv,
+                  const __grid_constant__ CUtensorMap tmg,
+                  const __grid_constant__ CUtensorMap tmb,
+                  const __grid_constant__ CUtensorMap twq_st,
+                  const __grid_constant__ CUtensorMap tu0_st,
+                  const __grid_constant__ CUtensorMap to0_st, const Ws ws, const int n_items) {
+  prep_run(p, tmq, tmk, tmv, tmg, tmb, twq_st, tu0_st, to0_st, ws, n_items, blockIdx.x, gridDim.x,
+           nullptr);
 }
 
 // ============================================================================ kernel 2: state
@@ -697,12 +737,11 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { retur
 // tile; half h = w / 4 of the channels (S update) and of the tokens (U and outputs). The issuer
 // warp (8) waits on the per-half barriers and issues the MMAs and the TMA loads. The compute
 // warps synchronise with it through mbarriers only.
-__global__ void __launch_bounds__(kStateThreads, 1)
-chunk_state_kernel(const __grid_constant__ ChunkParams p,
-                   const __grid_constant__ CUtensorMap twq,
-                   const __grid_constant__ CUtensorMap tkbt,
-                   const __grid_constant__ CUtensorMap tdec,
-                   const __grid_constant__ CUtensorMap tout, const Ws ws) {
+// With `flags`, waits (acquire) for each item's record before reading it.
+__device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMap& twq,
+                                          const CUtensorMap& tkbt, const CUtensorMap& tdec,
+                                          const CUtensorMap& tout, const Ws& ws, const int tile,
+                                          const int h, const int ridx, const uint32_t* flags) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   StateMisc* misc = reinterpret_cast<StateMisc*>(sm + S_MISC);
@@ -710,7 +749,6 @@ chunk_state_kernel(const __grid_constant__ ChunkParams p,
   const bool issuer = warp == 8;
   const int qd = warp & 3, hf = (warp >> 2) & 1;
   const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
-  const int tile = blockIdx.x, h = blockIdx.y, ridx = blockIdx.z;
   const int H = p.H;
   const bool pkg = p.package != 0;
   const bool mcols = pkg && tile == 0;      // package mode: tile 0 = M, tile 1 = D
@@ -755,8 +793,12 @@ chunk_state_kernel(const __grid_constant__ ChunkParams p,
       tma_prefetch_desc(&twq);
       tma_prefetch_desc(&tkbt);
       tma_prefetch_desc(&tdec);
-      auto issue_tma = [&](int j) {  // chunk j into stage j & 1 and decay slot j % 3
+      auto issue_tma = [&](int j) -> bool {  // chunk j into stage j & 1 and decay slot j % 3
         const int item = (slot0 + j) * H + h;
+        if (flags) {  // the record is published by the prep CTA that wrote it
+          if (!wait_flag(flags + item)) return false;
+          fence_proxy_async_global();
+        }
         uint8_t* st = sm + (j & 1) * S_STAGE;
         uint64_t* bar = &misc->full[j & 1];
         mbar_arrive_expect_tx(bar, S_STAGE + 512);
@@ -771,14 +813,15 @@ chunk_state_kernel(const __grid_constant__ ChunkParams p,
         // ahead; bring them into L2 now
         if (!mcols) bulk_prefetch_l2(ws.u0 + (int64_t)item * 8192, 32768);
         if (!pkg) bulk_prefetch_l2(ws.o0 + (int64_t)item * 8192, 16384);
+        return true;
       };
       int tma_last = -1;
-      for (int j = 0; j < 2 && j < nch; ++j) {
-        issue_tma(j);
-        tma_last = j;
+      bool ok = true;
+      for (int j = 0; j < 2 && j < nch && ok; ++j) {
+        ok = issue_tma(j);
+        if (ok) tma_last = j;
       }
       const uint32_t idesc = idesc_make(kFmtTF32, 128, 128, false, false);
-      bool ok = true;
       for (int j = 0; j < nch && ok; ++j) {
         const uint32_t par = (uint32_t)j & 1u;
         const uint32_t st = (uint32_t)(j & 1) * S_STAGE;
@@ -819,11 +862,8 @@ chunk_state_kernel(const __grid_constant__ ChunkParams p,
         mma_commit(&misc->bar_y);
         // the stage is free once Y has completed: load chunk j + 2 into it
         if (j + 2 < nch) {
-          ok = mbar_wait(&misc->bar_y, par);
-          if (ok) {
-            issue_tma(j + 2);
-            tma_last = j + 2;
-          }
+          ok = mbar_wait(&misc->bar_y, par) && issue_tma(j + 2);
+          if (ok) tma_last = j + 2;
         }
       }
       if (!ok) {
@@ -860,6 +900,11 @@ chunk_state_kernel(const __grid_constant__ ChunkParams p,
     // O0^T[n][32 hf ..] (32 bf16)
     auto load_regs = [&](int j, float4* u0, uint4* o0) {
       const int64_t item = (int64_t)(slot0 + j) * H + h;
+      if (flags) {
+        // The issuer acquired the record's flag before its arrive on this chunk's stage
+        // barrier (a release): acquiring that phase orders these loads after the record.
+        if (!mbar_wait(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u)) misc->abort = 1;
+      }
       if (vcol >= 0) {
         const float4* src = reinterpret_cast<const float4*>(ws.u0 + item * 8192) + hf * 8 * 128 + vcol;
 #pragma unroll
@@ -1006,6 +1051,49 @@ chunk_state_kernel(const __grid_constant__ ChunkParams p,
   if (warp == 0) tmem_dealloc(tbase, 512);
 }
 
+__global__ void __launch_bounds__(kStateThreads, 1)
+chunk_state_kernel(const __grid_constant__ ChunkParams p,
+                   const __grid_constant__ CUtensorMap twq,
+                   const __grid_constant__ CUtensorMap tkbt,
+                   const __grid_constant__ CUtensorMap tdec,
+                   const __grid_constant__ CUtensorMap tout, const Ws ws) {
+  state_run(p, twq, tkbt, tdec, tout, ws, blockIdx.x, blockIdx.y, blockIdx.z, nullptr);
+}
+
+// ============================================================================ fused launch
+// One cooperative launch of exactly one CTA per SM for inputs with few (range, head) pairs:
+// CTAs 0 .. n_state - 1 run the state kernel's work for (tile, head, range), the others the
+// prep kernel's items; a state CTA reads an item's record once its prep CTA has published it
+// (flags[item] = 1, release / acquire at gpu scope; every wait bounded). The serial state
+// walk then follows the parallel prep work instead of waiting for all of it.
+constexpr uint32_t F_SMEM = P_SMEM > S_SMEM ? P_SMEM : S_SMEM;
+
+__global__ void __launch_bounds__(kStateThreads, 1)
+chunk_fused_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ CUtensorMap tmq,
+                   const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv,
+                   const __grid_constant__ CUtensorMap tmg,
+                   const __grid_constant__ CUtensorMap tmb,
+                   const __grid_constant__ CUtensorMap twq_st,
+                   const __grid_constant__ CUtensorMap tu0_st,
+                   const __grid_constant__ CUtensorMap to0_st,
+                   const __grid_constant__ CUtensorMap twq,
+                   const __grid_constant__ CUtensorMap tkbt,
+                   const __grid_constant__ CUtensorMap tdec,
+                   const __grid_constant__ CUtensorMap tout, const Ws ws, const int n_items,
+                   const int n_state, uint32_t* flags) {
+  const int b = blockIdx.x;
+  if (b < n_state) {
+    const int tiles = p.package ? 2 : 1;
+    state_run(p, twq, tkbt, tdec, tout, ws, b % tiles, (b / tiles) % p.H, b / (tiles * p.H),
+              flags);
+  } else {
+    if (threadIdx.x >= kThreads) return;  // the prep work uses 8 warps
+    prep_run(p, tmq, tmk, tmv, tmg, tmb, twq_st, tu0_st, to0_st, ws, n_items, b - n_state,
+             (int)gridDim.x - n_state, flags);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
@@ -1124,6 +1212,12 @@ int64_t n_items_of(int n_ranges, int total_tokens, int H) {
   return ((int64_t)total_tokens / C + n_ranges) * H;
 }
 
+bool cooperative_ok() {
+  int dev = 0, v = 0;
+  return cudaGetDevice(&dev) == cudaSuccess &&
+         cudaDeviceGetAttribute(&v, cudaDevAttrCooperativeLaunch, dev) == cudaSuccess && v != 0;
+}
+
 int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1140,7 +1234,8 @@ bool chunk_tc_shape_ok(kda_dtype dt, int n_ranges, int total_tokens, int H, int 
 }
 
 size_t chunk_tc_workspace_bytes(int n_ranges, int total_tokens, int H) {
-  return (size_t)n_items_of(n_ranges, total_tokens, H) * kItemBytes;
+  const size_t items = (size_t)n_items_of(n_ranges, total_tokens, H);
+  return items * kItemBytes + ((items * 4 + 255) & ~(size_t)255);  // records, then flags
 }
 
 bool chunk_tc_supported(const ChunkParams& p, kda_dtype dt) {
@@ -1153,7 +1248,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   (void)dt;
   if (p.n_ranges == 0) return KDA_OK;
   const int64_t n_items = n_items_of(p.n_ranges, p.total_tokens, p.H);
-  const size_t need = (size_t)n_items * kItemBytes;
+  const size_t need = chunk_tc_workspace_bytes(p.n_ranges, p.total_tokens, p.H);
   if (!workspace || ws_bytes < need || ((uintptr_t)workspace % 256) != 0)
     return set_error(KDA_ERR_WORKSPACE, "tensor-core chunk path: workspace too small");
   uint8_t* base = (uint8_t*)workspace;
@@ -1163,6 +1258,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   ws.u0 = (float*)(base + (size_t)n_items * (kWqBytes + kKbtBytes));
   ws.o0 = (__nv_bfloat16*)(base + (size_t)n_items * (kWqBytes + kKbtBytes + kU0Bytes));
   ws.dec = (float*)(base + (size_t)n_items * (kWqBytes + kKbtBytes + kU0Bytes + kO0Bytes));
+  uint32_t* flags = (uint32_t*)(base + (size_t)n_items * kItemBytes);
 
   CUtensorMap mq, mk, mv, mg, mb, mwq, mkbt, mdec, swq, su0, so0, mo;
   const void* qp = p.q ? p.q : p.k;
@@ -1184,16 +1280,47 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S_SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             F_SMEM);
   if (e != cudaSuccess)
     return set_error(KDA_ERR_CUDA, std::string("tensor-core chunk path attribute: ") +
                                        cudaGetErrorString(e));
-  const int grid1 = (int)std::min<int64_t>(n_items, sm_count());
+  const int tiles = p.package ? 2 : 1;
+  const int64_t n_state = (int64_t)tiles * p.n_ranges * p.H;
+  const int sms = sm_count();
+  // Few serial walks: run them next to the prep work in one cooperative launch (at most a
+  // quarter of the SMs walk, the rest prepare records).
+  if (n_state * 4 <= sms && cooperative_ok()) {
+    e = cudaMemsetAsync(flags, 0, (size_t)n_items * 4, s);
+    if (e != cudaSuccess)
+      return set_error(KDA_ERR_CUDA, std::string("tensor-core chunk path flags: ") +
+                                         cudaGetErrorString(e));
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)sms);
+    cfg.blockDim = dim3(kStateThreads);
+    cfg.dynamicSmemBytes = F_SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, chunk_fused_kernel, p, mq, mk, mv, mg, mb, swq, su0, so0, mwq,
+                           mkbt, mdec, mo, ws, (int)n_items, (int)n_state, flags);
+    if (e == cudaSuccess) {
+      count_launches(1);
+      return check_launch("tensor-core chunk fused kernel");
+    }
+    (void)cudaGetLastError();  // not co-resident here: two launches instead
+  }
+  const int grid1 = (int)std::min<int64_t>(n_items, sms);
   chunk_prep_kernel<<<grid1, kThreads, P_SMEM, s>>>(p, mq, mk, mv, mg, mb, swq, su0, so0, ws,
                                                      (int)n_items);
   count_launches(1);
   kda_status st = check_launch("tensor-core chunk prep kernel");
   if (st != KDA_OK) return st;
-  dim3 grid2(p.package ? 2 : 1, p.H, p.n_ranges);
+  dim3 grid2(tiles, p.H, p.n_ranges);
   chunk_state_kernel<<<grid2, kStateThreads, S_SMEM, s>>>(p, mwq, mkbt, mdec, mo, ws);
   count_launches(1);
   return check_launch("tensor-core chunk state kernel");

@@ -171,6 +171,35 @@ __device__ __forceinline__ void bulk_wait_read0() {
 __device__ __forceinline__ void bulk_wait0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
+// Waits until all but the most recently committed bulk-store group of this thread completed.
+__device__ __forceinline__ void bulk_wait1() {
+  asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- cross-CTA flags
+// Orders this thread's generic-proxy accesses of global memory with its async-proxy ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Waits until *flag is non-zero (acquire). Gives up after `limit_ns` and returns false.
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag,
+                                          uint64_t limit_ns = 4000000000ull) {
+  if (ld_acquire_gpu(flag) != 0) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(64);
+    if (ld_acquire_gpu(flag) != 0) return true;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
 
 // ---------------------------------------------------------------- tcgen05
 // Allocates `ncols` TMEM columns (power of two >= 32); the base address lands in *dst.

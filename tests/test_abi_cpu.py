@@ -88,10 +88,13 @@ def test_prefill_argument_checks(L):
 def test_chunk_workspace_query(L):
     from linear_attention_state_kda_gb300 import kda
     bf, f32 = torch.bfloat16, torch.float32
-    # one record of 147,968 bytes per (chunk slot, head); slots = T // 64 + ranges
-    assert kda.chunk_workspace(bf, 1, 16384, 32, 128, 128) == (256 + 1) * 32 * 147968
-    assert kda.chunk_workspace(bf, 8, 16384, 32, 128, 128) == (256 + 8) * 32 * 147968
-    assert kda.chunk_workspace(bf, 3, 100, 4, 128, 128) == (1 + 3) * 4 * 147968
+    # one record of 147,968 bytes per (chunk slot, head), slots = T // 64 + ranges, then a
+    # 4-byte flag per record rounded up to 256 bytes
+    def need(items):
+        return items * 147968 + (items * 4 + 255) // 256 * 256
+    assert kda.chunk_workspace(bf, 1, 16384, 32, 128, 128) == need((256 + 1) * 32)
+    assert kda.chunk_workspace(bf, 8, 16384, 32, 128, 128) == need((256 + 8) * 32)
+    assert kda.chunk_workspace(bf, 3, 100, 4, 128, 128) == need((1 + 3) * 4)
     # paths that need none: fp32, d = 64, H not a multiple of 4, nothing to do
     assert kda.chunk_workspace(f32, 1, 16384, 32, 128, 128) == 0
     assert kda.chunk_workspace(bf, 1, 16384, 32, 64, 64) == 0
