@@ -184,8 +184,7 @@ __device__ __forceinline__ void psync() {
 __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap& tmq,
                                          const CUtensorMap& tmk, const CUtensorMap& tmv,
                                          const CUtensorMap& tmg, const CUtensorMap& tmb,
-                                         const CUtensorMap& twq_st, const CUtensorMap& tu0_st,
-                                         const CUtensorMap& to0_st, const Ws& ws,
+                                         const CUtensorMap& twq_st, const Ws& ws,
                                          const int n_items, const int first, const int stride,
                                          uint32_t* flags) {
   extern __shared__ uint8_t smem_raw[];
@@ -326,10 +325,13 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       };
       auto kb_out = [&](int c0, const float* x, const float* kv) {
         float kb[8];
+        const float4 ea = *reinterpret_cast<const float4*>(misc->erho + c0);
+        const float4 eb = *reinterpret_cast<const float4*>(misc->erho + c0 + 4);
+        const float er[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           kb[e] = (valid ? kv[e] : 0.0f) * ex2_approx(-x[e]);
-          kbt_out[(size_t)(c0 + e) * C] = kb[e] * misc->erho[c0 + e];
+          kbt_out[(size_t)(c0 + e) * C] = kb[e] * er[e];
         }
         *reinterpret_cast<float4*>(sm + P_KB + sw128_off32(t, c0, P_KB_KB)) =
             make_float4(kb[0], kb[1], kb[2], kb[3]);
@@ -337,7 +339,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
             make_float4(kb[4], kb[5], kb[6], kb[7]);
       };
       if (qd < 2) {
-#pragma unroll 1
+#pragma unroll 2
         for (int cb = 0; cb < 64; cb += 16) {
           float kh[16];
 #pragma unroll
@@ -346,18 +348,20 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
             float x[8], kv[8];
             load_x(c0, x);
             load_bf8(P_STG_K, c0, kv);
+            const float4 ea = *reinterpret_cast<const float4*>(misc->erho + c0);
+            const float4 eb = *reinterpret_cast<const float4*>(misc->erho + c0 + 4);
+            const float er[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
               kh[u + e] = (valid ? kv[e] : 0.0f) * ex2_approx(x[e]);
-              *f32at(sm, P_BE + sw128_off32(c0 + e, t, P_BE_KB)) =
-                  kh[u + e] * misc->erho[c0 + e];  // K'^T
+              *f32at(sm, P_BE + sw128_off32(c0 + e, t, P_BE_KB)) = kh[u + e] * er[e];  // K'^T
             }
             if (cb < 32) kb_out(c0, x, kv);
           }
           tmem_st16(tbase + lane_base + TM_XA + chh * 64 + cb, kh);
         }
       } else {
-#pragma unroll 1
+#pragma unroll 2
         for (int cb = 0; cb < 64; cb += 16) {
           float qh[16];
 #pragma unroll
@@ -647,8 +651,9 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
         tma_store_2d(&twq_st, sm + ST_W + kb * 8192, kb * 32, item * 128);
         if (need_out) tma_store_2d(&twq_st, sm + ST_Q + kb * 8192, kb * 32, item * 128 + 64);
       }
-      tma_store_3d(&tu0_st, sm + ST_U, 0, 0, item * 16);
-      if (need_out) tma_store_3d(&to0_st, sm + ST_O, 0, 0, item * 8);
+      // U0^T and O0^T records are contiguous: plain bulk copies
+      bulk_store(ws.u0 + (size_t)item * 8192, sm + ST_U, 32768);
+      if (need_out) bulk_store(ws.o0 + (size_t)item * 8192, sm + ST_O, 16384);
       bulk_commit();
       // the previous item's record is complete once its store group is: publish it (its
       // generic stores, Kb'^T and the decays, were ordered before this thread's release by
@@ -691,11 +696,8 @@ chunk_prep_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__
                   const __grid_constant__ CUtensorMap tmv,
                   const __grid_constant__ CUtensorMap tmg,
                   const __grid_constant__ CUtensorMap tmb,
-                  const __grid_constant__ CUtensorMap twq_st,
-                  const __grid_constant__ CUtensorMap tu0_st,
-                  const __grid_constant__ CUtensorMap to0_st, const Ws ws, const int n_items) {
-  prep_run(p, tmq, tmk, tmv, tmg, tmb, twq_st, tu0_st, to0_st, ws, n_items, blockIdx.x, gridDim.x,
-           nullptr);
+                  const __grid_constant__ CUtensorMap twq_st, const Ws ws, const int n_items) {
+  prep_run(p, tmq, tmk, tmv, tmg, tmb, twq_st, ws, n_items, blockIdx.x, gridDim.x, nullptr);
 }
 
 // ============================================================================ kernel 2: state
@@ -1075,8 +1077,6 @@ chunk_fused_kernel(const __grid_constant__ ChunkParams p, const __grid_constant_
                    const __grid_constant__ CUtensorMap tmg,
                    const __grid_constant__ CUtensorMap tmb,
                    const __grid_constant__ CUtensorMap twq_st,
-                   const __grid_constant__ CUtensorMap tu0_st,
-                   const __grid_constant__ CUtensorMap to0_st,
                    const __grid_constant__ CUtensorMap twq,
                    const __grid_constant__ CUtensorMap tkbt,
                    const __grid_constant__ CUtensorMap tdec,
@@ -1089,7 +1089,7 @@ chunk_fused_kernel(const __grid_constant__ ChunkParams p, const __grid_constant_
               flags);
   } else {
     if (threadIdx.x >= kThreads) return;  // the prep work uses 8 warps
-    prep_run(p, tmq, tmk, tmv, tmg, tmb, twq_st, tu0_st, to0_st, ws, n_items, b - n_state,
+    prep_run(p, tmq, tmk, tmv, tmg, tmb, twq_st, ws, n_items, b - n_state,
              (int)gridDim.x - n_state, flags);
   }
 }
@@ -1160,22 +1160,6 @@ bool make_map_ws(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, 
   CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
                    const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
-// Interleaved record array [groups][128][w] (fp32 w = 4, or bf16 w = 8) as a 3-D tensor
-// (w, 128, groups); box (w, 128, 64 / w): one item's U0^T or O0^T.
-bool make_map_ileave(CUtensorMap* m, const void* ptr, uint64_t groups, uint32_t w, bool bf16) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)w, 128, (cuuint64_t)groups};
-  cuuint64_t strides[2] = {16, 2048};
-  cuuint32_t box[3] = {w, 128, 64 / w};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
-                   const_cast<void*>(ptr), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -1260,7 +1244,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   ws.dec = (float*)(base + (size_t)n_items * (kWqBytes + kKbtBytes + kU0Bytes + kO0Bytes));
   uint32_t* flags = (uint32_t*)(base + (size_t)n_items * kItemBytes);
 
-  CUtensorMap mq, mk, mv, mg, mb, mwq, mkbt, mdec, swq, su0, so0, mo;
+  CUtensorMap mq, mk, mv, mg, mb, mwq, mkbt, mdec, swq, mo;
   const void* qp = p.q ? p.q : p.k;
   const uint64_t rows128 = (uint64_t)n_items * 128;
   if (!make_map3(&mq, qp, p.total_tokens, p.H, 64, false) ||
@@ -1271,8 +1255,6 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
       !make_map_ws(&mwq, ws.wq, rows128, 128, 128) || !make_map_ws(&mkbt, ws.kbt, rows128, 64, 128) ||
       !make_map_dec(&mdec, ws.dec, (uint64_t)n_items) ||
       !make_map_ws(&swq, ws.wq, rows128, 128, 64) ||
-      !make_map_ileave(&su0, ws.u0, (uint64_t)n_items * 16, 4, false) ||
-      !make_map_ileave(&so0, ws.o0, (uint64_t)n_items * 8, 8, true) ||
       !make_map_out(&mo, p.o ? p.o : p.k, p.total_tokens, p.H))
     return set_error(KDA_ERR_CUDA, "tensor-core chunk path: cuTensorMapEncodeTiled failed");
   cudaError_t e =
@@ -1306,8 +1288,8 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, chunk_fused_kernel, p, mq, mk, mv, mg, mb, swq, su0, so0, mwq,
-                           mkbt, mdec, mo, ws, (int)n_items, (int)n_state, flags);
+    e = cudaLaunchKernelEx(&cfg, chunk_fused_kernel, p, mq, mk, mv, mg, mb, swq, mwq, mkbt, mdec,
+                           mo, ws, (int)n_items, (int)n_state, flags);
     if (e == cudaSuccess) {
       count_launches(1);
       return check_launch("tensor-core chunk fused kernel");
@@ -1315,7 +1297,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
     (void)cudaGetLastError();  // not co-resident here: two launches instead
   }
   const int grid1 = (int)std::min<int64_t>(n_items, sms);
-  chunk_prep_kernel<<<grid1, kThreads, P_SMEM, s>>>(p, mq, mk, mv, mg, mb, swq, su0, so0, ws,
+  chunk_prep_kernel<<<grid1, kThreads, P_SMEM, s>>>(p, mq, mk, mv, mg, mb, swq, ws,
                                                      (int)n_items);
   count_launches(1);
   kda_status st = check_launch("tensor-core chunk prep kernel");

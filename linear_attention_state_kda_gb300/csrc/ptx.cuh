@@ -160,6 +160,14 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* s
       "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
       : "memory");
 }
+// Contiguous bulk copy shared -> global (both 16-byte aligned, size a multiple of 16), tracked
+// by this thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                   (uint64_t)dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
