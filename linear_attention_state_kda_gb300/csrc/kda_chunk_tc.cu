@@ -141,12 +141,10 @@ constexpr uint32_t SCR_P = P_XTRA + 64 * LA * 4;  // 8 warps x [16][8]
 constexpr uint32_t P_MISC = SCR_P + 8 * 128 * 4;
 // Workspace-record staging for the bulk-tensor stores, over Kb, [K'^T ; V^T] and TB^T (all
 // dead once the last products are complete): W and Q'' as 4 boxes of [64 rows][32] fp32 in the
-// 128-byte swizzle, U0^T and O0^T in their interleaved record layouts.
+// 128-byte swizzle (U0^T and O0^T go straight from registers to their interleaved records).
 constexpr uint32_t ST_W = P_KB;
 constexpr uint32_t ST_Q = P_KB + 32768;
-constexpr uint32_t ST_U = P_KB + 65536;
-constexpr uint32_t ST_O = P_KB + 98304;
-static_assert(ST_O + 16384 <= P_XTRA, "record staging overflow");
+static_assert(ST_Q + 32768 <= P_XTRA, "record staging overflow");
 constexpr uint32_t P_SMEM = P_MISC + 2048 + 1024;
 static_assert(64 * LA * 4 <= 32768, "A_kk scratch must fit in the Kb buffer");
 static_assert(P_KB % 1024 == 0 && P_BE % 1024 == 0 && P_TBT % 1024 == 0, "alignment");
@@ -552,11 +550,16 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
         const uint32_t kb = (s >> 2) * P_TBT_KB + (s & 3) * 32;
         mma_tf32_ts(tbase + TM_E, tbase + TM_A1 + s * 8, sdesc_sw128(sbase + P_TBT + kb, 16, 1024),
                     id64, 1);
+      }
+      mma_commit(&misc->bar_p);
+      // U0^T after the commit: P's readout below overlaps it (bar_e covers it)
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const uint32_t kb = (s >> 2) * P_TBT_KB + (s & 3) * 32;
         mma_tf32(tbase + TM_U0T,
                  sdesc_sw128(sbase + P_BE + (s >> 2) * P_BE_KB + 16384 + (s & 3) * 32, 16, 1024),
                  sdesc_sw128(sbase + P_TBN + kb, 16, 1024), id64, s > 0);
       }
-      mma_commit(&misc->bar_p);
     }
     if (!mbar_wait(&misc->bar_p, par)) misc->abort = 1;
     tc_fence_after();
@@ -614,15 +617,16 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
                 make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
         }
       }
-      // U0^T and O0^T: value column n = TMEM lane, tokens chh * 32 .. + 31, interleaved
+      // U0^T and O0^T: value column n = TMEM lane, tokens chh * 32 .. + 31, stored straight to
+      // the interleaved records (32 lanes = 32 consecutive columns = 512 contiguous bytes)
       const int nn = qd * 32 + lane;
       {
         float v[32];
         tmem_ld32(tbase + lane_base + TM_U0T + chh * 32, v);
+        float4* dst = reinterpret_cast<float4*>(ws.u0 + (size_t)item * 8192) + chh * 8 * 128 + nn;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          *reinterpret_cast<float4*>(sm + ST_U + ((uint32_t)(chh * 8 + j) * 128u + nn) * 16u) =
-              make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+          dst[j * 128] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
       }
       if (need_out) {
         float v[32];
@@ -639,7 +643,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
           pk.y = *reinterpret_cast<uint32_t*>(&b1);
           pk.z = *reinterpret_cast<uint32_t*>(&b2);
           pk.w = *reinterpret_cast<uint32_t*>(&b3);
-          *reinterpret_cast<uint4*>(sm + ST_O + ((uint32_t)(chh * 4 + k) * 128u + nn) * 16u) = pk;
+          reinterpret_cast<uint4*>(ws.o0 + (size_t)item * 8192)[(chh * 4 + k) * 128 + nn] = pk;
         }
       }
     }
@@ -651,9 +655,6 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
         tma_store_2d(&twq_st, sm + ST_W + kb * 8192, kb * 32, item * 128);
         if (need_out) tma_store_2d(&twq_st, sm + ST_Q + kb * 8192, kb * 32, item * 128 + 64);
       }
-      // U0^T and O0^T records are contiguous: plain bulk copies
-      bulk_store(ws.u0 + (size_t)item * 8192, sm + ST_U, 32768);
-      if (need_out) bulk_store(ws.o0 + (size_t)item * 8192, sm + ST_O, 16384);
       bulk_commit();
       // the previous item's record is complete once its store group is: publish it (its
       // generic stores, Kb'^T and the decays, were ordered before this thread's release by
