@@ -2,8 +2,9 @@
 
 One step = one pass of every hot-path call over synthetic inputs already resident in HBM:
   * kda_chunk_prefill  on the 16k-token prefill (H=32, T=16384, d=128, bf16 q/k/v);
-  * kda_segment_package -> kda_package_scan -> kda_segment_replay on the same inputs split
-    into 8 segments of 2048 tokens;
+  * the segment path on the same inputs split into 8 segments of 2048 tokens:
+    kda_chunk_prepare (per-chunk records, once) -> kda_segment_package_prepared ->
+    kda_package_scan -> kda_segment_replay_prepared;
   * kda_decode_step    on 256 rows x 32 heads over a 4096-slot fp32 pool (8.6 GB).
 `value` is the headline metric: prefill tokens per second of kda_chunk_prefill on the 16k
 workload, from CUDA events around that call in each timed step; the other calls are reported
@@ -168,14 +169,15 @@ def run_gb300(args):
     def prefill():
         kda.chunk_prefill(x.q, x.k, x.v, x.g, x.beta, o=o, final_state=fin, workspace=ws_pf)
 
-    def package():
-        kda.segment_package(x.k, x.v, x.g, x.beta, offs, M=M, D=Dp, workspace=ws_seg)
+    def package():  # the records serve both walks of the segment path
+        kda.chunk_prepare(x.q, x.k, x.v, x.g, x.beta, offs, workspace=ws_seg)
+        kda.segment_package_prepared(ws_seg, offs, T, H, D, D, M=M, D=Dp)
 
     def scan():
         kda.package_scan(M, Dp, seq_seg, P, seg_init=seg_init, final_state=fin2, workspace=ws)
 
     def replay():
-        kda.segment_replay(x.q, x.k, x.v, x.g, x.beta, offs, seg_init, o=o2, workspace=ws_seg)
+        kda.segment_replay_prepared(ws_seg, offs, seg_init, T, H, D, D, o=o2)
 
     def decode():
         kda.decode_step(dec.q, dec.k, dec.v, dec.g, dec.beta, dec.slot_ids, dec.pool, o=od)

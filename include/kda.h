@@ -199,6 +199,47 @@ KDA_API kda_status kda_segment_replay(kda_dtype dt, int n_segs, int total_tokens
                               uint32_t* status, kda_stream_t stream);
 
 /*
+ * kda_chunk_prepare: the state-independent half of the chunked calls, on its own. Writes into
+ * `workspace` the per-(64-token chunk, head) records of n_ranges token ranges
+ * [offsets[i], offsets[i+1]) (offsets may be NULL for one range of total_tokens tokens). The
+ * records depend only on q, k, v, g, beta, the ranges and scale, so one preparation serves
+ * both walks of the segment path over the same segments: kda_segment_package_prepared, and
+ * (when q was given) kda_segment_replay_prepared. With q == NULL the records carry only what a
+ * package walk reads.
+ *   workspace  at least kda_chunk_workspace(dt, n_ranges, total_tokens, H, dk, dv) bytes,
+ *              256-byte aligned; the tensor-core shapes only (that query > 0), others return
+ *              KDA_ERR_UNSUPPORTED.
+ *   beta       16-byte aligned. status: optional device word (KDA_STATUS_DECAY_RANGE).
+ * The pages have no separate counterpart: their context-parallel members prepare a segment
+ * once and both publish its package and replay it ("same segment walk, same chunk step",
+ * pegainfer PR #970, fabric data-plane commit message).
+ */
+KDA_API kda_status kda_chunk_prepare(kda_dtype dt, int n_ranges, int total_tokens,
+                                     const int32_t* offsets, int H, int dk, int dv, int chunk,
+                                     float scale, const void* q, const void* k, const void* v,
+                                     const float* g, const float* beta, void* workspace,
+                                     size_t ws_bytes, uint32_t* status, kda_stream_t stream);
+
+/*
+ * kda_segment_package_prepared / kda_segment_replay_prepared: the state walks of
+ * kda_segment_package / kda_segment_replay over records that kda_chunk_prepare wrote into
+ * `workspace` for the same segments (same seg_offsets, total_tokens, H, dk, dv; the replay
+ * also needs records prepared with q and the replay's scale). The workspace is only read.
+ * Results equal those of the unprepared calls on the inputs that were prepared.
+ */
+KDA_API kda_status kda_segment_package_prepared(kda_dtype dt, int n_segs, int total_tokens,
+                                                const int32_t* seg_offsets, int H, int dk,
+                                                int dv, int chunk, float* M, float* D,
+                                                const void* workspace, size_t ws_bytes,
+                                                uint32_t* status, kda_stream_t stream);
+KDA_API kda_status kda_segment_replay_prepared(kda_dtype dt, int n_segs, int total_tokens,
+                                               const int32_t* seg_offsets, int H, int dk,
+                                               int dv, int chunk, const float* seg_init,
+                                               void* o, float* seg_final,
+                                               const void* workspace, size_t ws_bytes,
+                                               uint32_t* status, kda_stream_t stream);
+
+/*
  * kda_decode_step: one token per batch row over a slot-addressed fp32 state pool,
  * updated in place: for row b and head h, S = pool[slot_ids[b], h] becomes its successor
  * and o[b, h] = scale * S_new^T q.

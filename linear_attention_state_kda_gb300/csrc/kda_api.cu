@@ -190,6 +190,100 @@ kda_status kda_segment_replay(kda_dtype dt, int n_segs, int total_tokens,
   return st;
 }
 
+kda_status kda_chunk_prepare(kda_dtype dt, int n_ranges, int total_tokens,
+                             const int32_t* offsets, int H, int dk, int dv, int chunk,
+                             float scale, const void* q, const void* k, const void* v,
+                             const float* g, const float* beta, void* workspace,
+                             size_t ws_bytes, uint32_t* status, kda_stream_t stream) {
+  const char* fn = "kda_chunk_prepare";
+  kda_status st = check_shape(fn, dt, H, dk, dv, chunk);
+  if (st != KDA_OK) return st;
+  KDA_REQUIRE(n_ranges >= 0 && total_tokens >= 0, KDA_ERR_INVALID_ARG,
+              "kda_chunk_prepare: n_ranges and total_tokens must be >= 0");
+  KDA_REQUIRE(offsets || n_ranges <= 1, KDA_ERR_INVALID_ARG,
+              "kda_chunk_prepare: offsets are required when n_ranges > 1");
+  if (n_ranges == 0 || total_tokens == 0) return KDA_OK;
+  KDA_REQUIRE(chunk_workspace(dt, n_ranges, total_tokens, H, dk, dv) > 0, KDA_ERR_UNSUPPORTED,
+              "kda_chunk_prepare: records exist for the tensor-core shapes only (bf16, "
+              "dk = dv = 128, H a multiple of 4)");
+  KDA_REQUIRE(k && v && g && beta, KDA_ERR_INVALID_ARG,
+              "kda_chunk_prepare: k, v, g and beta must be non-null");
+  KDA_REQUIRE(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(g, 16) &&
+                  aligned(beta, 16) && aligned(offsets, 4) && aligned(status, 4),
+              KDA_ERR_INVALID_ARG,
+              "kda_chunk_prepare: q, k, v, g must be 16-byte aligned, beta too");
+  ChunkParams p{};
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+  p.offsets = offsets; p.n_ranges = n_ranges; p.total_tokens = total_tokens;
+  p.H = H; p.dk = dk; p.dv = dv; p.scale = scale; p.status = status;
+  p.package = q ? 0 : 1;  // without q, only the factors a package walk reads
+  const size_t need = chunk_workspace(dt, n_ranges, total_tokens, H, dk, dv);
+  KDA_REQUIRE(workspace && ws_bytes >= need && aligned(workspace, 256), KDA_ERR_WORKSPACE,
+              "kda_chunk_prepare: workspace missing, too small or not 256-byte aligned (need " +
+                  std::to_string(need) + " bytes)");
+  return launch_chunk_tc(p, dt, workspace, ws_bytes, (cudaStream_t)stream, kPhasePrep);
+}
+
+namespace {
+kda_status check_prepared(const char* fn, kda_dtype dt, int n_segs, int total_tokens,
+                          const int32_t* seg_offsets, int H, int dk, int dv, int chunk,
+                          const void* workspace, size_t ws_bytes) {
+  kda_status st = check_shape(fn, dt, H, dk, dv, chunk);
+  if (st != KDA_OK) return st;
+  KDA_REQUIRE(n_segs >= 0 && total_tokens >= 0, KDA_ERR_INVALID_ARG,
+              std::string(fn) + ": n_segs and total_tokens must be >= 0");
+  if (n_segs == 0 || total_tokens == 0) return KDA_OK;
+  KDA_REQUIRE(seg_offsets, KDA_ERR_INVALID_ARG, std::string(fn) + ": seg_offsets must be non-null");
+  const size_t need = chunk_workspace(dt, n_segs, total_tokens, H, dk, dv);
+  KDA_REQUIRE(need > 0, KDA_ERR_UNSUPPORTED,
+              std::string(fn) + ": prepared records exist for the tensor-core shapes only");
+  KDA_REQUIRE(workspace && ws_bytes >= need && aligned(workspace, 256), KDA_ERR_WORKSPACE,
+              std::string(fn) + ": workspace missing, too small or not 256-byte aligned");
+  return KDA_OK;
+}
+}  // namespace
+
+kda_status kda_segment_package_prepared(kda_dtype dt, int n_segs, int total_tokens,
+                                        const int32_t* seg_offsets, int H, int dk, int dv,
+                                        int chunk, float* M, float* D, const void* workspace,
+                                        size_t ws_bytes, uint32_t* status, kda_stream_t stream) {
+  const char* fn = "kda_segment_package_prepared";
+  kda_status st = check_prepared(fn, dt, n_segs, total_tokens, seg_offsets, H, dk, dv, chunk,
+                                 workspace, ws_bytes);
+  if (st != KDA_OK || n_segs == 0) return st;
+  KDA_REQUIRE(M && D && aligned(M, 16) && aligned(D, 16) && aligned(status, 4),
+              KDA_ERR_INVALID_ARG, "kda_segment_package_prepared: M and D must be non-null and "
+                                   "16-byte aligned");
+  if (total_tokens == 0) return KDA_OK;
+  ChunkParams p{};
+  p.offsets = seg_offsets; p.n_ranges = n_segs; p.total_tokens = total_tokens;
+  p.H = H; p.dk = dk; p.dv = dv; p.scale = 1.0f;
+  p.M = M; p.D = D; p.status = status; p.package = 1;
+  return launch_chunk_tc(p, dt, const_cast<void*>(workspace), ws_bytes, (cudaStream_t)stream,
+                         kPhaseState);
+}
+
+kda_status kda_segment_replay_prepared(kda_dtype dt, int n_segs, int total_tokens,
+                                       const int32_t* seg_offsets, int H, int dk, int dv,
+                                       int chunk, const float* seg_init, void* o,
+                                       float* seg_final, const void* workspace, size_t ws_bytes,
+                                       uint32_t* status, kda_stream_t stream) {
+  const char* fn = "kda_segment_replay_prepared";
+  kda_status st = check_prepared(fn, dt, n_segs, total_tokens, seg_offsets, H, dk, dv, chunk,
+                                 workspace, ws_bytes);
+  if (st != KDA_OK || n_segs == 0 || total_tokens == 0) return st;
+  KDA_REQUIRE(o && aligned(o, 16) && aligned(seg_init, 16) && aligned(seg_final, 16) &&
+                  aligned(status, 4),
+              KDA_ERR_INVALID_ARG, "kda_segment_replay_prepared: o must be non-null, pointers "
+                                   "16-byte aligned");
+  ChunkParams p{};
+  p.offsets = seg_offsets; p.n_ranges = n_segs; p.total_tokens = total_tokens;
+  p.H = H; p.dk = dk; p.dv = dv; p.scale = 1.0f;
+  p.init = seg_init; p.o = o; p.final_state = seg_final; p.status = status; p.package = 0;
+  return launch_chunk_tc(p, dt, const_cast<void*>(workspace), ws_bytes, (cudaStream_t)stream,
+                         kPhaseState);
+}
+
 kda_status kda_decode_step(kda_dtype dt, int batch, int H, int dk, int dv, float scale,
                            const void* q, const void* k, const void* v, const float* g,
                            const float* beta, const int32_t* slot_ids, float* state_pool,

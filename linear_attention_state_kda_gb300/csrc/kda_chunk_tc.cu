@@ -1229,7 +1229,7 @@ bool chunk_tc_supported(const ChunkParams& p, kda_dtype dt) {
 }
 
 kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, size_t ws_bytes,
-                           cudaStream_t s) {
+                           cudaStream_t s, int phases) {
   (void)dt;
   if (p.n_ranges == 0) return KDA_OK;
   const int64_t n_items = n_items_of(p.n_ranges, p.total_tokens, p.H);
@@ -1245,18 +1245,26 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   ws.dec = (float*)(base + (size_t)n_items * (kWqBytes + kKbtBytes + kU0Bytes + kO0Bytes));
   uint32_t* flags = (uint32_t*)(base + (size_t)n_items * kItemBytes);
 
+  const bool do_prep = (phases & kPhasePrep) != 0, do_state = (phases & kPhaseState) != 0;
   CUtensorMap mq, mk, mv, mg, mb, mwq, mkbt, mdec, swq, mo;
-  const void* qp = p.q ? p.q : p.k;
   const uint64_t rows128 = (uint64_t)n_items * 128;
-  if (!make_map3(&mq, qp, p.total_tokens, p.H, 64, false) ||
-      !make_map3(&mk, p.k, p.total_tokens, p.H, 64, false) ||
-      !make_map3(&mv, p.v, p.total_tokens, p.H, 64, false) ||
-      !make_map3(&mg, p.g, p.total_tokens, p.H, 32, true) ||
-      !make_map_beta(&mb, p.beta, p.total_tokens, p.H) ||
-      !make_map_ws(&mwq, ws.wq, rows128, 128, 128) || !make_map_ws(&mkbt, ws.kbt, rows128, 64, 128) ||
-      !make_map_dec(&mdec, ws.dec, (uint64_t)n_items) ||
-      !make_map_ws(&swq, ws.wq, rows128, 128, 64) ||
-      !make_map_out(&mo, p.o ? p.o : p.k, p.total_tokens, p.H))
+  bool maps_ok = true;
+  if (do_prep) {
+    const void* qp = p.q ? p.q : p.k;
+    maps_ok = make_map3(&mq, qp, p.total_tokens, p.H, 64, false) &&
+              make_map3(&mk, p.k, p.total_tokens, p.H, 64, false) &&
+              make_map3(&mv, p.v, p.total_tokens, p.H, 64, false) &&
+              make_map3(&mg, p.g, p.total_tokens, p.H, 32, true) &&
+              make_map_beta(&mb, p.beta, p.total_tokens, p.H) &&
+              make_map_ws(&swq, ws.wq, rows128, 128, 64);
+  }
+  if (maps_ok && do_state) {
+    maps_ok = make_map_ws(&mwq, ws.wq, rows128, 128, 128) &&
+              make_map_ws(&mkbt, ws.kbt, rows128, 64, 128) &&
+              make_map_dec(&mdec, ws.dec, (uint64_t)n_items) &&
+              make_map_out(&mo, p.o ? p.o : (const void*)ws.wq, p.total_tokens, p.H);
+  }
+  if (!maps_ok)
     return set_error(KDA_ERR_CUDA, "tensor-core chunk path: cuTensorMapEncodeTiled failed");
   cudaError_t e =
       cudaFuncSetAttribute(chunk_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM);
@@ -1274,7 +1282,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   const int sms = sm_count();
   // Few serial walks: run them next to the prep work in one cooperative launch (at most a
   // quarter of the SMs walk, the rest prepare records).
-  if (n_state * 4 <= sms && cooperative_ok()) {
+  if (do_prep && do_state && n_state * 4 <= sms && cooperative_ok()) {
     e = cudaMemsetAsync(flags, 0, (size_t)n_items * 4, s);
     if (e != cudaSuccess)
       return set_error(KDA_ERR_CUDA, std::string("tensor-core chunk path flags: ") +
@@ -1297,12 +1305,14 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
     }
     (void)cudaGetLastError();  // not co-resident here: two launches instead
   }
-  const int grid1 = (int)std::min<int64_t>(n_items, sms);
-  chunk_prep_kernel<<<grid1, kThreads, P_SMEM, s>>>(p, mq, mk, mv, mg, mb, swq, ws,
-                                                     (int)n_items);
-  count_launches(1);
-  kda_status st = check_launch("tensor-core chunk prep kernel");
-  if (st != KDA_OK) return st;
+  if (do_prep) {
+    const int grid1 = (int)std::min<int64_t>(n_items, sms);
+    chunk_prep_kernel<<<grid1, kThreads, P_SMEM, s>>>(p, mq, mk, mv, mg, mb, swq, ws,
+                                                       (int)n_items);
+    count_launches(1);
+    kda_status st = check_launch("tensor-core chunk prep kernel");
+    if (st != KDA_OK || !do_state) return st;
+  }
   dim3 grid2(tiles, p.H, p.n_ranges);
   chunk_state_kernel<<<grid2, kStateThreads, S_SMEM, s>>>(p, mwq, mkbt, mdec, mo, ws);
   count_launches(1);

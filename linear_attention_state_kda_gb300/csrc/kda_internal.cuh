@@ -66,8 +66,10 @@ kda_status launch_chunk_simt(const ChunkParams& p, kda_dtype dt, cudaStream_t s)
 bool chunk_tc_shape_ok(kda_dtype dt, int n_ranges, int total_tokens, int H, int dk, int dv);
 size_t chunk_tc_workspace_bytes(int n_ranges, int total_tokens, int H);
 bool chunk_tc_supported(const ChunkParams& p, kda_dtype dt);
+// phases: kPhasePrep writes the records, kPhaseState walks them; both = one chunked call.
+constexpr int kPhasePrep = 1, kPhaseState = 2;
 kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, size_t ws_bytes,
-                           cudaStream_t s);
+                           cudaStream_t s, int phases = kPhasePrep | kPhaseState);
 
 // Decode step.
 kda_status launch_decode(kda_dtype dt, int batch, int H, int dk, int dv, float scale,

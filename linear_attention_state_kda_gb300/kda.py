@@ -59,6 +59,12 @@ def lib():
     L.kda_segment_replay.restype = I
     L.kda_segment_replay.argtypes = [I, I, I, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, Z, P,
                                      P]
+    L.kda_chunk_prepare.restype = I
+    L.kda_chunk_prepare.argtypes = [I, I, I, P, I, I, I, I, F, P, P, P, P, P, P, Z, P, P]
+    L.kda_segment_package_prepared.restype = I
+    L.kda_segment_package_prepared.argtypes = [I, I, I, P, I, I, I, I, P, P, P, Z, P, P]
+    L.kda_segment_replay_prepared.restype = I
+    L.kda_segment_replay_prepared.argtypes = [I, I, I, P, I, I, I, I, P, P, P, P, Z, P, P]
     L.kda_decode_step.restype = I
     L.kda_decode_step.argtypes = [I, I, I, I, I, F, P, P, P, P, P, P, P, I64, P, P, P]
     _lib = L
@@ -222,6 +228,57 @@ def segment_replay(q, k, v, g, beta, seg_offsets, seg_init, scale=1.0, o=None,
                                     float(scale), _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                                     _ptr(beta), _ptr(seg_init), _ptr(o), _ptr(seg_final),
                                     _ptr(ws), ws_bytes, _ptr(status), _stream(stream)))
+    return o, seg_final
+
+
+def chunk_prepare(q, k, v, g, beta, offsets=None, scale=1.0, workspace=None, status=None,
+                  chunk=64, stream=None):
+    """kda_chunk_prepare: per-chunk records of the ranges in `offsets` (q may be None when
+    only packages will be built). Returns the workspace tensor holding them."""
+    _contig(q, k, v, g, beta, offsets)
+    T, H, dk = k.shape
+    dv = v.shape[2]
+    n = 1 if offsets is None else offsets.numel() - 1
+    ws, ws_bytes = _chunk_ws(workspace, k.dtype, n, T, H, dk, dv, k.device)
+    _check(lib().kda_chunk_prepare(_dt(k), n, T, _ptr(offsets), H, dk, dv, chunk, float(scale),
+                                   _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(ws),
+                                   ws_bytes, _ptr(status), _stream(stream)))
+    return ws
+
+
+def segment_package_prepared(workspace, seg_offsets, T, H, dk, dv, M=None, D=None,
+                             dtype=torch.bfloat16, status=None, chunk=64, stream=None):
+    """kda_segment_package_prepared over records from chunk_prepare. Returns (M, D)."""
+    _contig(seg_offsets, M, D)
+    P = seg_offsets.numel() - 1
+    dev = workspace.device
+    if M is None:
+        M = torch.empty(P, H, dk, dk, dtype=torch.float32, device=dev)
+    if D is None:
+        D = torch.empty(P, H, dk, dv, dtype=torch.float32, device=dev)
+    dt = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    _check(lib().kda_segment_package_prepared(dt, P, T, _ptr(seg_offsets), H, dk, dv, chunk,
+                                              _ptr(M), _ptr(D), _ptr(workspace),
+                                              workspace.numel(), _ptr(status), _stream(stream)))
+    return M, D
+
+
+def segment_replay_prepared(workspace, seg_offsets, seg_init, T, H, dk, dv, o=None,
+                            seg_final=None, want_final=False, dtype=torch.bfloat16, status=None,
+                            chunk=64, stream=None):
+    """kda_segment_replay_prepared over records prepared with q. Returns (o, seg_final)."""
+    _contig(seg_offsets, seg_init, o, seg_final)
+    P = seg_offsets.numel() - 1
+    dev = workspace.device
+    if o is None:
+        o = torch.empty(T, H, dv, dtype=dtype, device=dev)
+    if seg_final is None and want_final:
+        seg_final = torch.empty(P, H, dk, dv, dtype=torch.float32, device=dev)
+    dt = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    _check(lib().kda_segment_replay_prepared(dt, P, T, _ptr(seg_offsets), H, dk, dv, chunk,
+                                             _ptr(seg_init), _ptr(o), _ptr(seg_final),
+                                             _ptr(workspace), workspace.numel(), _ptr(status),
+                                             _stream(stream)))
     return o, seg_final
 
 

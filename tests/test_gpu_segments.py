@@ -128,3 +128,24 @@ def test_varlen_long_leveled_sampled_head():
     assert rel_o(f64(o1[:, heads]), ro) < to
     assert rel_s(f64(f1[:, heads]), rf) < ts
     assert rel_o(f64(r["o"][:, heads]), ro) < to
+
+
+def test_prepared_records_serve_package_and_replay():
+    """One kda_chunk_prepare feeds both walks: identical to the unprepared calls."""
+    x = inputs.make_workload("segments_8x2048", device=DEV)
+    segs = inputs.workload_segments("segments_8x2048")
+    r = _segment_path(x, segs, want_seg_final=True)
+    T, H, dk = x.k.shape
+    dv = x.v.shape[2]
+    ws = kda.chunk_prepare(x.q, x.k, x.v, x.g, x.beta, r["offs"])
+    M, D = kda.segment_package_prepared(ws, r["offs"], T, H, dk, dv)
+    o, seg_final = kda.segment_replay_prepared(ws, r["offs"], r["seg_init"], T, H, dk, dv,
+                                               want_final=True)
+    torch.cuda.synchronize()
+    assert torch.equal(M, r["M"]) and torch.equal(D, r["D"])
+    assert torch.equal(o, r["o"]) and torch.equal(seg_final, r["seg_final"])
+    # records prepared without q still serve the package walk
+    ws2 = kda.chunk_prepare(None, x.k, x.v, x.g, x.beta, r["offs"])
+    M2, D2 = kda.segment_package_prepared(ws2, r["offs"], T, H, dk, dv)
+    torch.cuda.synchronize()
+    assert torch.equal(M2, r["M"]) and torch.equal(D2, r["D"])
