@@ -11,11 +11,11 @@
 //   * down-sweep: at stride d, (a[i-d], a[i]) <- (a[i], a[i-d] o a[i]);
 //   * leaf j then holds the exclusive prefix (M_<j, D_<j), and the segment's entry state is
 //     M_<j S_init + D_<j.
-// Every combine is a dk x dk times dk x (dk + dv) product. For dk = dv = 128 the combines and
-// the entry-state applications run on tcgen05 tensor cores with a 3xTF32 split (namespace tc
-// below). The CUDA-core version (dk = 64) has a CTA compute a 32-row block of one combine's
-// result: it reads only its own rows of the left operand, so that storage can take the
-// result in place.
+// Every combine is a dk x dk times dk x (dk + dv) product. For dk = dv = 128 the whole tree of
+// a (sequence, head) runs in one launch, one cluster of 4 CTAs per tree, every combine and
+// entry-state application on tcgen05 tensor cores with a 3xTF32 split (namespace tc below).
+// The CUDA-core version (dk = 64) has a CTA compute a 32-row block of one combine's result: it
+// reads only its own rows of the left operand, so that storage can take the result in place.
 #include "kda_internal.cuh"
 #include "ptx.cuh"
 
@@ -208,19 +208,143 @@ __device__ __forceinline__ float hi(float x) {
   return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
 
-// One 64-column tile (tile < 2: M columns, else D columns) of A o B. bm may be null (state
-// application: D tiles only). Whole-CTA function (256 threads).
-__device__ void combine_tile(const float* A, const float* bm, const float* bd, float* om,
-                             float* od, int tile, uint32_t* status) {
+// ------------------------------------------------------------ whole tree in one launch
+// One cluster of 4 CTAs per (sequence, head) runs fill, up-sweep, root, down-sweep and the
+// entry-state applications; CTA r owns column tile r of every combine (tiles 0, 1: M columns,
+// 2, 3: D columns). Every combine reads the whole left operand, so a level writes its results
+// to the tmp nodes, and after a cluster barrier each CTA moves its own tiles into place.
+// TMEM (64 columns) and the operand barrier live for the whole kernel.
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+struct TileCtx {
+  uint32_t tbase;
+  uint64_t* bar;
+  uint32_t phase;
+  bool ok;
+};
+
+// out tile = A o B (bm null: state application, out.D = A.M S + A.D with S = bd; bd null as
+// well: out.D = A.D). TMEM and the barrier come with the context (allocated once per CTA).
+__device__ void tile_combine(TileCtx& cx, const float* A, const float* bm, const float* bd,
+                             float* om, float* od, int tile, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-  __shared__ uint64_t bar;
-  __shared__ uint32_t tslot;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool mtile = tile < DK / NT;
   const int col0 = (mtile ? tile : tile - DK / NT) * NT;
-  const float* B = mtile ? bm : bd;  // [128 (k)][128 (n)] row-major
   float* out = mtile ? om : od;
+  const float* B = mtile ? bm : bd;
+  if (B) {
+    for (int e = tid; e < 128 * 32; e += blockDim.x) {  // A.M -> hi / lo, K-major [r][k]
+      const int r = e >> 5, k4 = (e & 31) * 4;
+      const float4 a = *reinterpret_cast<const float4*>(A + r * DK + k4);
+      const float4 hh = make_float4(hi(a.x), hi(a.y), hi(a.z), hi(a.w));
+      const uint32_t off = sw128_off32(r, k4, A_KB);
+      *reinterpret_cast<float4*>(sm + AH + off) = hh;
+      *reinterpret_cast<float4*>(sm + AL + off) =
+          make_float4(a.x - hh.x, a.y - hh.y, a.z - hh.z, a.w - hh.w);
+    }
+    for (int e = tid; e < 128 * (NT / 4); e += blockDim.x) {  // B tile, transposed
+      const int k = e / (NT / 4), n4 = (e % (NT / 4)) * 4;
+      const float4 b = *reinterpret_cast<const float4*>(B + k * DK + col0 + n4);
+      const float bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint32_t off = sw128_off32(n4 + u, k, B_KB);
+        const float h = hi(bv[u]);
+        *reinterpret_cast<float*>(sm + BH + off) = h;
+        *reinterpret_cast<float*>(sm + BL + off) = bv[u] - h;
+      }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+      const uint32_t sb = smem_u32(sm);
+      const uint32_t idesc = idesc_make(kFmtTF32, 128, NT, false, false);
+#pragma unroll 1
+      for (int s = 0; s < 16; ++s) {
+        const uint32_t ka = (s >> 2) * A_KB + (s & 3) * 32, kb = (s >> 2) * B_KB + (s & 3) * 32;
+        const uint64_t ah = sdesc_sw128(sb + AH + ka, 16, 1024);
+        const uint64_t al = sdesc_sw128(sb + AL + ka, 16, 1024);
+        const uint64_t bh = sdesc_sw128(sb + BH + kb, 16, 1024);
+        const uint64_t bl = sdesc_sw128(sb + BL + kb, 16, 1024);
+        mma_tf32(cx.tbase, ah, bh, idesc, s > 0 ? 1u : 0u);
+        mma_tf32(cx.tbase, ah, bl, idesc, 1);
+        mma_tf32(cx.tbase, al, bh, idesc, 1);
+      }
+      mma_commit(cx.bar);
+    }
+    const bool ok = mbar_wait(cx.bar, cx.phase);
+    cx.phase ^= 1u;
+    if (!ok) {
+      cx.ok = false;
+      if (tid == 0 && status) atomicOr(status, KDA_STATUS_TIMEOUT);
+    }
+    tc_fence_after();
+  }
+  {  // warp w: rows 32 (w % 4).., columns 32 (w / 4)..; D tiles add A.D
+    const int r = (warp & 3) * 32 + lane, cb = (warp >> 2) * 32;
+    float v[32];
+    if (B) {
+      tmem_ld32(cx.tbase + ((uint32_t)((warp & 3) * 32) << 16) + cb, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+    }
+    const float* ad = A + DK * DK + r * DK + col0 + cb;
+    float* dst = out + r * DK + col0 + cb;
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      float4 x = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      if (!mtile) {
+        const float4 a = *reinterpret_cast<const float4*>(ad + j);
+        x.x += a.x; x.y += a.y; x.z += a.z; x.w += a.w;
+      }
+      *reinterpret_cast<float4*>(dst + j) = x;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();  // the operand buffers and TMEM are reused by the next call
+  tc_fence_after();
+}
+
+// Copy column tile `tile` (0, 1: M columns; 2, 3: D columns) of a package: src_m / src_d are
+// the source's M and D pieces (both null: the identity package (I, 0)), dst the destination
+// package ([M | D] contiguous).
+__device__ void tile_copy(const float* src_m, const float* src_d, float* dst, int tile) {
+  const bool mtile = tile < DK / NT;
+  const int col0 = (mtile ? tile : tile - DK / NT) * NT;
+  float* d = dst + (mtile ? 0 : DK * DK);
+  const float* sp = mtile ? src_m : src_d;
+  for (int e = threadIdx.x; e < DK * (NT / 4); e += blockDim.x) {
+    const int r = e / (NT / 4), c4 = col0 + (e % (NT / 4)) * 4;
+    float4 x;
+    if (sp) {
+      x = *reinterpret_cast<const float4*>(sp + r * DK + c4);
+    } else {
+      x = make_float4(mtile && r == c4 ? 1.f : 0.f, mtile && r == c4 + 1 ? 1.f : 0.f,
+                      mtile && r == c4 + 2 ? 1.f : 0.f, mtile && r == c4 + 3 ? 1.f : 0.f);
+    }
+    *reinterpret_cast<float4*>(d + r * DK + c4) = x;
+  }
+}
+__device__ __forceinline__ void tile_move(const float* src, float* dst, int tile) {
+  tile_copy(src, src + DK * DK, dst, tile);
+}
+
+__global__ void __cluster_dims__(4, 1, 1) __launch_bounds__(256, 1)
+scan_tree_tc(Tree t, const int32_t* seq_off, const float* M, const float* D, const float* init,
+             float* seg_init, float* final_state, uint32_t* status) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tslot;
+  const int tile = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) {
     tmem_alloc(&tslot, NT);
     tmem_relinquish();
@@ -229,135 +353,78 @@ __device__ void combine_tile(const float* A, const float* bm, const float* bd, f
     mbar_init(&bar, 1);
     fence_mbar_init();
   }
-  for (int e = tid; e < 128 * 32; e += blockDim.x) {  // A.M -> hi / lo, K-major [r][k]
-    const int r = e >> 5, k4 = (e & 31) * 4;
-    const float4 a = *reinterpret_cast<const float4*>(A + r * DK + k4);
-    const float4 h = make_float4(hi(a.x), hi(a.y), hi(a.z), hi(a.w));
-    const uint32_t off = sw128_off32(r, k4, A_KB);
-    *reinterpret_cast<float4*>(sm + AH + off) = h;
-    *reinterpret_cast<float4*>(sm + AL + off) =
-        make_float4(a.x - h.x, a.y - h.y, a.z - h.z, a.w - h.w);
-  }
-  for (int e = tid; e < 128 * (NT / 4); e += blockDim.x) {  // B tile, transposed
-    const int k = e / (NT / 4), n4 = (e % (NT / 4)) * 4;
-    const float4 b = *reinterpret_cast<const float4*>(B + k * DK + col0 + n4);
-    const float bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint32_t off = sw128_off32(n4 + u, k, B_KB);
-      const float h = hi(bv[u]);
-      *reinterpret_cast<float*>(sm + BH + off) = h;
-      *reinterpret_cast<float*>(sm + BL + off) = bv[u] - h;
-    }
-  }
-  fence_proxy_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tbase = tslot;
-  if (tid == 0) {
-    const uint32_t sb = smem_u32(sm);
-    const uint32_t idesc = idesc_make(kFmtTF32, 128, NT, false, false);
-#pragma unroll 1
-    for (int s = 0; s < 16; ++s) {
-      const uint32_t ka = (s >> 2) * A_KB + (s & 3) * 32, kb = (s >> 2) * B_KB + (s & 3) * 32;
-      const uint64_t ah = sdesc_sw128(sb + AH + ka, 16, 1024);
-      const uint64_t al = sdesc_sw128(sb + AL + ka, 16, 1024);
-      const uint64_t bh = sdesc_sw128(sb + BH + kb, 16, 1024);
-      const uint64_t bl = sdesc_sw128(sb + BL + kb, 16, 1024);
-      mma_tf32(tbase, ah, bh, idesc, s > 0 ? 1u : 0u);
-      mma_tf32(tbase, ah, bl, idesc, 1);
-      mma_tf32(tbase, al, bh, idesc, 1);
-    }
-    mma_commit(&bar);
-  }
-  const bool ok = mbar_wait(&bar, 0);
-  if (!ok && tid == 0 && status) atomicOr(status, KDA_STATUS_TIMEOUT);
-  tc_fence_after();
-  {  // warp w: lanes 32 (w % 4).. (rows), columns 32 (w / 4)..; D tiles add A.D
-    const int r = (warp & 3) * 32 + lane, cb = (warp >> 2) * 32;
-    float v[32];
-    tmem_ld32(tbase + ((uint32_t)((warp & 3) * 32) << 16) + cb, v);
-    if (ok) {
-      const float* ad = A + DK * DK + r * DK + col0 + cb;
-      float* dst = out + r * DK + col0 + cb;
-#pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        float4 x = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-        if (!mtile) {
-          const float4 a = *reinterpret_cast<const float4*>(ad + j);
-          x.x += a.x; x.y += a.y; x.z += a.z; x.w += a.w;
-        }
-        *reinterpret_cast<float4*>(dst + j) = x;
-      }
-    }
-  }
-  if (!ok && tid == 0) {  // let the MMAs drain (bounded) before the TMEM is released
-    mbar_wait(&bar, 0, 100000000ull);
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tbase, NT);
-}
-
-// MODE 0: up-sweep at stride d: tmp[pair] = a[i] o a[i-d]
-// MODE 1: down-sweep at stride d: tmp[pair] = a[i-d] o a[i]
-// MODE 2: exit state: final[s] = root applied to init[s]
-// MODE 3: entry states: seg_init[first + j] = a[j] applied to init[s]
-template <int MODE>
-__global__ void __launch_bounds__(256, 1)
-scan_tc(Tree t, int d, const int32_t* seq_off, const float* init, float* outp,
-        uint32_t* status) {
-  const int tile = blockIdx.x, idx = blockIdx.y;
-  const int s = blockIdx.z / t.H, h = blockIdx.z % t.H;
+  TileCtx cx{tslot, &bar, 0u, true};
+  int first, cnt;
+  if (!t.seq_range(seq_off, s, first, cnt) && tile == 0 && h == 0 && tid == 0 && status)
+    atomicOr(status, KDA_STATUS_BAD_OFFSETS);
   const int64_t sd = (int64_t)DK * DK;
-  if (MODE <= 1) {
-    const int i = (2 * idx + 2) * d - 1;
-    const float* A = t.node(s, MODE == 0 ? i : i - d, h);
-    const float* B = t.node(s, MODE == 0 ? i - d : i, h);
-    float* o = t.tnode(s, idx, h);
-    combine_tile(A, B, B + sd, o, o + sd, tile, status);
-  } else if (MODE == 2) {
-    combine_tile(t.node(s, t.P2 - 1, h), nullptr, init + ((int64_t)s * t.H + h) * sd, nullptr,
-                 outp + ((int64_t)s * t.H + h) * sd, tile + DK / NT, status);
-  } else {
-    int first, cnt;
-    t.seq_range(seq_off, s, first, cnt);
-    if (idx >= cnt) return;  // whole CTA
-    combine_tile(t.node(s, idx, h), nullptr, init + ((int64_t)s * t.H + h) * sd, nullptr,
-                 outp + ((int64_t)(first + idx) * t.H + h) * sd, tile + DK / NT, status);
+  // fill: packages of the sequence, then (I, 0)
+  for (int i = 0; i < t.P2; ++i) {
+    float* dst = t.node(s, i, h);
+    if (i < cnt) {
+      const float* m = M + ((int64_t)(first + i) * t.H + h) * sd;
+      const float* d = D + ((int64_t)(first + i) * t.H + h) * sd;
+      tile_copy(m, d, dst, tile);  // the caller's M and D arrays
+    } else {
+      tile_copy(nullptr, nullptr, dst, tile);
+    }
   }
-}
-
-// The package moves between tree levels are plain copies: 16-byte accesses, kMoveParts CTAs
-// per package.
-constexpr int kMoveParts = 8;
-
-// a[i] <- tmp[pair] after an up-sweep level
-__global__ void scan_up_move(Tree t, int d) {
-  const int pair = blockIdx.x / kMoveParts, part = blockIdx.x % kMoveParts;
-  const int h = blockIdx.y, s = blockIdx.z;
-  const int i = (2 * pair + 2) * d - 1;
-  const int64_t per = pkg_floats(t.dk, t.dv) / 4 / kMoveParts;
-  float4* R = reinterpret_cast<float4*>(t.node(s, i, h)) + part * per;
-  const float4* X = reinterpret_cast<const float4*>(t.tnode(s, pair, h)) + part * per;
-  for (int64_t e = threadIdx.x; e < per; e += blockDim.x) R[e] = X[e];
-}
-
-// a[i-d] <- a[i], a[i] <- tmp[pair] after a down-sweep level
-__global__ void scan_down_move(Tree t, int d) {
-  const int pair = blockIdx.x / kMoveParts, part = blockIdx.x % kMoveParts;
-  const int h = blockIdx.y, s = blockIdx.z;
-  const int i = (2 * pair + 2) * d - 1;
-  const int64_t per = pkg_floats(t.dk, t.dv) / 4 / kMoveParts;
-  float4* L = reinterpret_cast<float4*>(t.node(s, i - d, h)) + part * per;
-  float4* R = reinterpret_cast<float4*>(t.node(s, i, h)) + part * per;
-  const float4* X = reinterpret_cast<const float4*>(t.tnode(s, pair, h)) + part * per;
-  for (int64_t e = threadIdx.x; e < per; e += blockDim.x) {
-    const float4 r = R[e];
-    L[e] = r;
-    R[e] = X[e];
+  cluster_sync_all();
+  // up-sweep: a[i] = a[i] o a[i - d]
+  for (int d = 1; d < t.P2; d <<= 1) {
+    for (int pair = 0; pair < t.P2 / (2 * d); ++pair) {
+      const int i = (2 * pair + 2) * d - 1;
+      const float* A = t.node(s, i, h);
+      const float* B = t.node(s, i - d, h);
+      float* o = t.tnode(s, pair, h);
+      tile_combine(cx, A, B, B + sd, o, o + sd, tile, status);
+    }
+    cluster_sync_all();
+    for (int pair = 0; pair < t.P2 / (2 * d); ++pair)
+      tile_move(t.tnode(s, pair, h), t.node(s, (2 * pair + 2) * d - 1, h), tile);
+    cluster_sync_all();
   }
+  // root: the exit state (D tiles), then (I, 0)
+  float* root = t.node(s, t.P2 - 1, h);
+  if (final_state && tile >= DK / NT) {
+    float* fo = final_state + ((int64_t)s * t.H + h) * sd;
+    tile_combine(cx, root, nullptr, init ? init + ((int64_t)s * t.H + h) * sd : nullptr, nullptr,
+                 fo, tile, status);
+  }
+  cluster_sync_all();
+  tile_copy(nullptr, nullptr, root, tile);
+  cluster_sync_all();
+  // down-sweep: (a[i - d], a[i]) <- (a[i], a[i - d] o a[i])
+  for (int d = t.P2 / 2; d >= 1; d >>= 1) {
+    for (int pair = 0; pair < t.P2 / (2 * d); ++pair) {
+      const int i = (2 * pair + 2) * d - 1;
+      const float* A = t.node(s, i - d, h);
+      const float* B = t.node(s, i, h);
+      float* o = t.tnode(s, pair, h);
+      tile_combine(cx, A, B, B + sd, o, o + sd, tile, status);
+    }
+    cluster_sync_all();
+    for (int pair = 0; pair < t.P2 / (2 * d); ++pair) {
+      const int i = (2 * pair + 2) * d - 1;
+      tile_move(t.node(s, i, h), t.node(s, i - d, h), tile);
+      tile_move(t.tnode(s, pair, h), t.node(s, i, h), tile);
+    }
+    cluster_sync_all();
+  }
+  // entry states: leaf j's prefix applied to the sequence's entry state; the two D tiles of
+  // each leaf are spread over the four CTAs
+  for (int j = tile >> 1; j < cnt; j += 2) {
+    const int dt = DK / NT + (tile & 1);
+    float* so = seg_init + ((int64_t)(first + j) * t.H + h) * sd;
+    tile_combine(cx, t.node(s, j, h), nullptr,
+                 init ? init + ((int64_t)s * t.H + h) * sd : nullptr, nullptr, so, dt, status);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tslot, NT);
 }
 
 }  // namespace tc
@@ -381,45 +448,11 @@ kda_status run_tc(int n_seqs, int n_segs, const int32_t* seq_off, int max_segs, 
   t.n_segs = n_segs;
   t.base = (float*)ws;
   t.tmp = t.base + (int64_t)n_seqs * t.P2 * H * pkg_floats(DK, DV);
-  const int rb = DK / kRows;
-  const unsigned zh = (unsigned)(n_seqs * H);
   const int smem = (int)tc::SMEM;
-  cudaFuncSetAttribute(tc::scan_tc<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  cudaFuncSetAttribute(tc::scan_tc<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  cudaFuncSetAttribute(tc::scan_tc<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  cudaFuncSetAttribute(tc::scan_tc<3>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-  int launches = 0;
-  scan_fill<<<dim3(t.P2, H, n_seqs), kThreads, 0, s>>>(t, M, D, seq_off, status);
-  ++launches;
-  for (int d = 1; d < t.P2; d <<= 1) {
-    tc::scan_tc<0><<<dim3(4, t.P2 / (2 * d), zh), 256, smem, s>>>(t, d, seq_off, init, nullptr,
-                                                                  status);
-    tc::scan_up_move<<<dim3(t.P2 / (2 * d) * tc::kMoveParts, H, n_seqs), kThreads, 0, s>>>(t,
-                                                                                         d);
-    launches += 2;
-  }
-  if (final_state && init) {
-    tc::scan_tc<2><<<dim3(2, 1, zh), 256, smem, s>>>(t, 0, seq_off, init, final_state, status);
-    ++launches;
-  }
-  // reset the root to (I, 0); without an entry state the exit state is the root's D
-  scan_root<DK, DV><<<dim3(1, H * rb, n_seqs), kThreads, 0, s>>>(
-      t, nullptr, init ? nullptr : final_state);
-  ++launches;
-  for (int d = t.P2 / 2; d >= 1; d >>= 1) {
-    tc::scan_tc<1><<<dim3(4, t.P2 / (2 * d), zh), 256, smem, s>>>(t, d, seq_off, init, nullptr,
-                                                                  status);
-    tc::scan_down_move<<<dim3(t.P2 / (2 * d) * tc::kMoveParts, H, n_seqs), kThreads, 0, s>>>(t,
-                                                                                           d);
-    launches += 2;
-  }
-  if (init)
-    tc::scan_tc<3><<<dim3(2, t.P2, zh), 256, smem, s>>>(t, 0, seq_off, init, seg_init, status);
-  else
-    scan_apply<DK, DV><<<dim3(t.P2, H * rb, n_seqs), kThreads, 0, s>>>(t, seq_off, nullptr,
-                                                                        seg_init);
-  ++launches;
-  count_launches(launches);
+  cudaFuncSetAttribute(tc::scan_tree_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  tc::scan_tree_tc<<<dim3(4, H, n_seqs), 256, smem, s>>>(t, seq_off, M, D, init, seg_init,
+                                                          final_state, status);
+  count_launches(1);
   return check_launch("kda_package_scan (tensor cores)");
 }
 
