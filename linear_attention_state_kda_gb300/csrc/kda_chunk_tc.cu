@@ -162,11 +162,20 @@ struct PrepMisc {
   uint32_t tmem_base;
   int abort;
   int nxt[4];  // item, t0, n, head of the item whose loads are in flight
-  float part[2][DK];
-  float erho[DK];
-  float beta[C];
+  // fused launch: items whose records are complete, handed from the loader thread to the
+  // publishing warp (ring of 4; pub_head counts the items handed over, pub_tail the flags
+  // published; item -1 ends the stream)
+  int pub_ring[4];
+  uint32_t pub_head, pub_tail;
+  // read with 16-byte vector loads
+  alignas(16) float part[2][DK];
+  alignas(16) float erho[DK];
+  alignas(16) float beta[C];
 };
 static_assert(sizeof(PrepMisc) <= 2048, "misc overflow");
+static_assert(offsetof(PrepMisc, part) % 16 == 0 && offsetof(PrepMisc, erho) % 16 == 0 &&
+                  offsetof(PrepMisc, beta) % 16 == 0,
+              "vector-loaded arrays must be 16-byte aligned");
 
 // The prep CTA's 256 threads synchronise on named barrier 1 (a fused launch runs them next to
 // a ninth, idle warp).
@@ -249,6 +258,17 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
   bool tma_out = false;  // loader: a load is in flight, completing phase parity tma_par
   uint32_t tma_par = 0;
   int prev_item = -1;    // loader: item whose record's store group is the latest but one
+  uint32_t pub_n = 0;    // loader: items handed to the publishing warp
+  // loader: hands an item (or -1, the end) to the publishing warp of a fused launch
+  auto hand_over = [&](int it) {
+    const uint64_t t0 = globaltimer_ns();
+    while (pub_n - ld_acquire_cta(&misc->pub_tail) >= 4u) {  // ring full: bounded wait
+      if (globaltimer_ns() - t0 > 1000000000ull) { misc->abort = 1; return; }
+      __nanosleep(32);
+    }
+    misc->pub_ring[pub_n & 3] = it;
+    st_release_cta(&misc->pub_head, ++pub_n);
+  };
   if (tid == kLoader) tma_out = advance(first);
   psync();
 
@@ -407,6 +427,16 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     if (tid == kLoader && !misc->abort) {
       tma_out = advance(item + stride);
       tma_par = par ^ 1u;
+      // Hand the previous item to the publishing warp: its record's store group was committed
+      // a phase ago (this item's group is not committed yet), and the generic stores of its
+      // record were ordered before this release by the barriers since. The publishing warp
+      // stores nothing else, so its gpu-scope release does not wait on this CTA's traffic.
+      if (flags && prev_item >= 0) {
+        bulk_wait0();
+        fence_proxy_async_global();
+        hand_over(prev_item);
+        prev_item = -1;
+      }
     }
     if (!mbar_wait(&misc->bar_a, par)) misc->abort = 1;
     tc_fence_after();
@@ -656,17 +686,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
         if (need_out) tma_store_2d(&twq_st, sm + ST_Q + kb * 8192, kb * 32, item * 128 + 64);
       }
       bulk_commit();
-      // the previous item's record is complete once its store group is: publish it (its
-      // generic stores, Kb'^T and the decays, were ordered before this thread's release by
-      // the barriers since)
-      if (flags) {
-        if (prev_item >= 0) {
-          bulk_wait1();
-          fence_proxy_async_global();
-          st_release_gpu(flags + prev_item, 1u);
-        }
-        prev_item = item;
-      }
+      if (flags) prev_item = item;  // published during the next item's A1 product
     }
     psync();
     if (misc->abort) break;
@@ -682,9 +702,10 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
   }
   if (tid == kLoader) {
     bulk_wait0();
-    if (flags && prev_item >= 0 && !misc->abort) {
+    if (flags) {  // the last item, then the end of the stream
       fence_proxy_async_global();
-      st_release_gpu(flags + prev_item, 1u);
+      if (prev_item >= 0 && !misc->abort) hand_over(prev_item);
+      hand_over(-1);
     }
   }
   psync();
@@ -1089,9 +1110,31 @@ chunk_fused_kernel(const __grid_constant__ ChunkParams p, const __grid_constant_
     state_run(p, twq, tkbt, tdec, tout, ws, b % tiles, (b / tiles) % p.H, b / (tiles * p.H),
               flags);
   } else {
-    if (threadIdx.x >= kThreads) return;  // the prep work uses 8 warps
-    prep_run(p, tmq, tmk, tmv, tmg, tmb, twq_st, ws, n_items, b - n_state,
-             (int)gridDim.x - n_state, flags);
+    // the prep work uses 8 warps; the ninth publishes the finished items' flags
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    PrepMisc* misc = reinterpret_cast<PrepMisc*>(sm + P_MISC);
+    if (threadIdx.x == 0) misc->pub_head = misc->pub_tail = 0;
+    __syncthreads();
+    if (threadIdx.x < kThreads) {
+      prep_run(p, tmq, tmk, tmv, tmg, tmb, twq_st, ws, n_items, b - n_state,
+               (int)gridDim.x - n_state, flags);
+    } else if (threadIdx.x == kThreads) {
+      for (uint32_t c = 0;; ++c) {
+        // bounded: the loader hands over an item per prep iteration, and ends the stream
+        const uint64_t t0 = globaltimer_ns();
+        bool got = true;
+        while (ld_acquire_cta(&misc->pub_head) <= c) {
+          if (globaltimer_ns() - t0 > 4000000000ull) { got = false; break; }
+          __nanosleep(32);
+        }
+        if (!got) break;
+        const int item = misc->pub_ring[c & 3];
+        if (item < 0) break;
+        st_release_gpu(flags + item, 1u);
+        st_release_cta(&misc->pub_tail, c + 1);
+      }
+    }
   }
 }
 
