@@ -129,8 +129,8 @@ constexpr uint32_t P_BE = P_KB + 32768;  // [K'^T ; V^T] [256][64 tok] fp32 (2 K
 constexpr uint32_t P_BE_KB = 32768;
 constexpr uint32_t P_TBT = P_BE + 65536;  // TB^T [64][64] fp32 (2 K-blocks of 8 KiB)
 constexpr uint32_t P_TBT_KB = 8192;
-// After the solve, the Kb buffer holds TB and P row-major ([t][t'], K-major over t'): the B
-// operands of U0^T = V^T TB^T and O0^T = V^T P^T.
+// After the solve, the Kb buffer holds TB and tril(A_qk) row-major ([t][t'], K-major over t'):
+// the B operands of U0^T = V^T TB^T and O0^T = U0^T A_qk^T.
 constexpr uint32_t P_TBN = P_KB;
 constexpr uint32_t P_PN = P_KB + 16384;
 constexpr uint32_t P_XTRA = P_TBT + 16384;
@@ -155,10 +155,10 @@ constexpr uint32_t TM_A1 = 128;  // 64: [Kh ; Qh] Kb^T -> [0 ; Aqk], the A opera
 constexpr uint32_t TM_E = 192;   // 64: [TB ; 0] + [0 ; Aqk] TB = [TB ; P], the A operand of E
 constexpr uint32_t TM_R = 256;   // 128: [TB ; P] K' = [W ; P K']
 constexpr uint32_t TM_U0T = 384;  // 64: V^T TB^T = U0^T (lanes = value columns)
-constexpr uint32_t TM_O0T = 448;  // 64: V^T P^T = (P V)^T
+constexpr uint32_t TM_O0T = 448;  // 64: U0^T A_qk^T = (A_qk TB V)^T = (P V)^T
 
 struct PrepMisc {
-  uint64_t bar_tma, bar_a, bar_p, bar_e, bar_drain;
+  uint64_t bar_tma, bar_a, bar_p, bar_u, bar_e, bar_drain;
   uint32_t tmem_base;
   int abort;
   int nxt[4];  // item, t0, n, head of the item whose loads are in flight
@@ -212,6 +212,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     mbar_init(&misc->bar_tma, 1);
     mbar_init(&misc->bar_a, 1);
     mbar_init(&misc->bar_p, 1);
+    mbar_init(&misc->bar_u, 1);
     mbar_init(&misc->bar_e, 1);
     mbar_init(&misc->bar_drain, 1);
     misc->abort = 0;
@@ -567,14 +568,24 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       for (int j = 0; j < 16; ++j) z[j] = 0.0f;
       tmem_st16(tbase + lane_base + TM_E + chh * 32, z);
       tmem_st16(tbase + lane_base + TM_E + chh * 32 + 16, z);
+      if (need_out) {  // tril(A_qk) rows (A1 lanes 64..127) -> row-major [t][t'] for O0^T
+        const int t = (qd - 2) * 32 + lane;
+        float v[32];
+        tmem_ld32(tbase + lane_base + TM_A1 + chh * 32, v);
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4*>(sm + P_PN + sw128_off32(t, chh * 32 + j, 8192)) =
+              make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      }
     }
     tmem_st_wait();
     fence_proxy_async_smem();
     psync();
-    // ================= E = [TB ; 0] + [0 ; Aqk] TB (and U0^T = V^T TB^T); then P row-major;
-    // then R = E K' (and O0^T = V^T P^T)
+    // ================= E = [TB ; 0] + [0 ; Aqk] TB = [TB ; P] and U0^T = V^T TB^T; then
+    // R = E K' = [W ; P K'] and O0^T = U0^T Aqk^T, each issued once its TMEM operand is complete
     if (tid == 0 && !misc->abort) {
       const uint32_t id64 = idesc_make(kFmtTF32, 128, 64, false, false);
+      const uint32_t id128 = idesc_make(kFmtTF32, 128, 128, false, false);
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const uint32_t kb = (s >> 2) * P_TBT_KB + (s & 3) * 32;
@@ -582,7 +593,6 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
                     id64, 1);
       }
       mma_commit(&misc->bar_p);
-      // U0^T after the commit: P's readout below overlaps it (bar_e covers it)
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
         const uint32_t kb = (s >> 2) * P_TBT_KB + (s & 3) * 32;
@@ -590,33 +600,29 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
                  sdesc_sw128(sbase + P_BE + (s >> 2) * P_BE_KB + 16384 + (s & 3) * 32, 16, 1024),
                  sdesc_sw128(sbase + P_TBN + kb, 16, 1024), id64, s > 0);
       }
-    }
-    if (!mbar_wait(&misc->bar_p, par)) misc->abort = 1;
-    tc_fence_after();
-    if (qd >= 2 && need_out) {  // P rows (E lanes 64..127) -> row-major [t][t'] for O0^T
-      const int t = (qd - 2) * 32 + lane;
-      float v[32];
-      tmem_ld32(tbase + lane_base + TM_E + chh * 32, v);
+      mma_commit(&misc->bar_u);
+      bool ok = mbar_wait(&misc->bar_p, par);
+      tc_fence_after();
+      if (ok) {
 #pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(sm + P_PN + sw128_off32(t, chh * 32 + j, 8192)) =
-            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-    }
-    fence_proxy_async_smem();
-    psync();
-    if (tid == 0 && !misc->abort) {
-      const uint32_t id64 = idesc_make(kFmtTF32, 128, 64, false, false);
-      const uint32_t id128 = idesc_make(kFmtTF32, 128, 128, false, false);
+        for (int s = 0; s < 8; ++s) {
+          const uint32_t kbe = (s >> 2) * P_BE_KB + (s & 3) * 32;
+          mma_tf32_ts(tbase + TM_R, tbase + TM_E + s * 8,
+                      sdesc_sw128(sbase + P_BE + kbe, 16, 1024), id128, s > 0);
+        }
+        if (need_out) {
+          ok = mbar_wait(&misc->bar_u, par);
+          tc_fence_after();
+          if (ok) {
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t kbe = (s >> 2) * P_BE_KB + (s & 3) * 32;
-        mma_tf32_ts(tbase + TM_R, tbase + TM_E + s * 8, sdesc_sw128(sbase + P_BE + kbe, 16, 1024),
-                    id128, s > 0);
-        if (need_out)
-          mma_tf32(tbase + TM_O0T, sdesc_sw128(sbase + P_BE + kbe + 16384, 16, 1024),
-                   sdesc_sw128(sbase + P_PN + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024), id64,
-                   s > 0);
+            for (int s = 0; s < 8; ++s)
+              mma_tf32_ts(tbase + TM_O0T, tbase + TM_U0T + s * 8,
+                          sdesc_sw128(sbase + P_PN + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024),
+                          id64, s > 0);
+          }
+        }
       }
+      if (!ok) misc->abort = 1;
       mma_commit(&misc->bar_e);
     }
     pbar();

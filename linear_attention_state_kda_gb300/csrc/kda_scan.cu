@@ -239,25 +239,41 @@ __device__ void tile_combine(TileCtx& cx, const float* A, const float* bm, const
   float* out = mtile ? om : od;
   const float* B = mtile ? bm : bd;
   if (B) {
-    for (int e = tid; e < 128 * 32; e += blockDim.x) {  // A.M -> hi / lo, K-major [r][k]
-      const int r = e >> 5, k4 = (e & 31) * 4;
-      const float4 a = *reinterpret_cast<const float4*>(A + r * DK + k4);
-      const float4 hh = make_float4(hi(a.x), hi(a.y), hi(a.z), hi(a.w));
-      const uint32_t off = sw128_off32(r, k4, A_KB);
+    // every load of the two operands is issued before the first shared-memory store, so that a
+    // combine waits for one round trip to L2 rather than one per loop step
+    float4 a[16], b[8];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {  // A.M, row-major: element e = tid + 256 u
+      const int e = tid + u * kThreads;
+      a[u] = *reinterpret_cast<const float4*>(A + (e >> 5) * DK + (e & 31) * 4);
+    }
+    // the B tile: element e = tid + 256 u is row k = (e & 127) of columns n4 .. n4 + 3,
+    // n4 = 4 (e >> 7), so that a warp's transposed stores below fill whole 128-byte rows
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int e = tid + u * kThreads;
+      b[u] = *reinterpret_cast<const float4*>(B + (e & 127) * DK + col0 + (e >> 7) * 4);
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {  // A.M -> hi / lo, K-major [r][k]
+      const int e = tid + u * kThreads;
+      const float4 hh = make_float4(hi(a[u].x), hi(a[u].y), hi(a[u].z), hi(a[u].w));
+      const uint32_t off = sw128_off32(e >> 5, (e & 31) * 4, A_KB);
       *reinterpret_cast<float4*>(sm + AH + off) = hh;
       *reinterpret_cast<float4*>(sm + AL + off) =
-          make_float4(a.x - hh.x, a.y - hh.y, a.z - hh.z, a.w - hh.w);
+          make_float4(a[u].x - hh.x, a[u].y - hh.y, a[u].z - hh.z, a[u].w - hh.w);
     }
-    for (int e = tid; e < 128 * (NT / 4); e += blockDim.x) {  // B tile, transposed
-      const int k = e / (NT / 4), n4 = (e % (NT / 4)) * 4;
-      const float4 b = *reinterpret_cast<const float4*>(B + k * DK + col0 + n4);
-      const float bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint32_t off = sw128_off32(n4 + u, k, B_KB);
-        const float h = hi(bv[u]);
+    for (int u = 0; u < 8; ++u) {  // B tile, transposed (row n, 32 consecutive k per warp)
+      const int e = tid + u * kThreads;
+      const int k = e & 127, n4 = (e >> 7) * 4;
+      const float bv[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t off = sw128_off32(n4 + q, k, B_KB);
+        const float h = hi(bv[q]);
         *reinterpret_cast<float*>(sm + BH + off) = h;
-        *reinterpret_cast<float*>(sm + BL + off) = bv[u] - h;
+        *reinterpret_cast<float*>(sm + BL + off) = bv[q] - h;
       }
     }
     fence_proxy_async_smem();
@@ -299,15 +315,18 @@ __device__ void tile_combine(TileCtx& cx, const float* A, const float* bm, const
     }
     const float* ad = A + DK * DK + r * DK + col0 + cb;
     float* dst = out + r * DK + col0 + cb;
+    if (!mtile) {  // all eight loads of A.D first
+      float4 a[8];
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      float4 x = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
-      if (!mtile) {
-        const float4 a = *reinterpret_cast<const float4*>(ad + j);
-        x.x += a.x; x.y += a.y; x.z += a.z; x.w += a.w;
+      for (int j = 0; j < 8; ++j) a[j] = reinterpret_cast<const float4*>(ad)[j];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        v[4 * j] += a[j].x; v[4 * j + 1] += a[j].y; v[4 * j + 2] += a[j].z; v[4 * j + 3] += a[j].w;
       }
-      *reinterpret_cast<float4*>(dst + j) = x;
     }
+#pragma unroll
+    for (int j = 0; j < 32; j += 4)
+      *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
   }
   tc_fence_before();
   __syncthreads();  // the operand buffers and TMEM are reused by the next call
@@ -322,16 +341,23 @@ __device__ void tile_copy(const float* src_m, const float* src_d, float* dst, in
   const int col0 = (mtile ? tile : tile - DK / NT) * NT;
   float* d = dst + (mtile ? 0 : DK * DK);
   const float* sp = mtile ? src_m : src_d;
-  for (int e = threadIdx.x; e < DK * (NT / 4); e += blockDim.x) {
+  // 8 float4 per thread (256 threads): all loads before the first store
+  float4 x[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int e = threadIdx.x + u * kThreads;
     const int r = e / (NT / 4), c4 = col0 + (e % (NT / 4)) * 4;
-    float4 x;
     if (sp) {
-      x = *reinterpret_cast<const float4*>(sp + r * DK + c4);
+      x[u] = *reinterpret_cast<const float4*>(sp + r * DK + c4);
     } else {
-      x = make_float4(mtile && r == c4 ? 1.f : 0.f, mtile && r == c4 + 1 ? 1.f : 0.f,
-                      mtile && r == c4 + 2 ? 1.f : 0.f, mtile && r == c4 + 3 ? 1.f : 0.f);
+      x[u] = make_float4(mtile && r == c4 ? 1.f : 0.f, mtile && r == c4 + 1 ? 1.f : 0.f,
+                         mtile && r == c4 + 2 ? 1.f : 0.f, mtile && r == c4 + 3 ? 1.f : 0.f);
     }
-    *reinterpret_cast<float4*>(d + r * DK + c4) = x;
+  }
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int e = threadIdx.x + u * kThreads;
+    *reinterpret_cast<float4*>(d + (e / (NT / 4)) * DK + col0 + (e % (NT / 4)) * 4) = x[u];
   }
 }
 __device__ __forceinline__ void tile_move(const float* src, float* dst, int tile) {
