@@ -125,12 +125,14 @@ constexpr uint32_t P_STG_G = 49152;     // 4 x [64 tok][32 ch] fp32, 128-byte sw
 constexpr uint32_t P_STG_B = 81920;     // [64 tok][4 heads] fp32
 constexpr uint32_t P_KB = 82944;        // Kb [64 tok][128 ch] fp32 (4 K-blocks of 8 KiB)
 constexpr uint32_t P_KB_KB = 8192;
-constexpr uint32_t P_BE = P_KB + 32768;  // [K'^T ; V^T] [256][64 tok] fp32 (2 K-blocks)
-constexpr uint32_t P_BE_KB = 32768;
-constexpr uint32_t P_TBT = P_BE + 65536;  // TB^T [64][64] fp32 (2 K-blocks of 8 KiB)
+constexpr uint32_t P_BE = P_KB + 32768;  // K'^T [128][64 tok] fp32 (2 K-blocks)
+constexpr uint32_t P_BE_KB = 16384;
+constexpr uint32_t P_TBT = P_BE + 32768;  // TB^T [64][64] fp32 (2 K-blocks of 8 KiB)
 constexpr uint32_t P_TBT_KB = 8192;
-// After the solve, the Kb buffer holds TB and tril(A_qk) row-major ([t][t'], K-major over t'):
-// the B operands of U0^T = V^T TB^T and O0^T = U0^T A_qk^T.
+// After the solve, the Kb buffer holds TB as bf16 hi and lo parts ([t][t'] rows of 128 B,
+// K-major over t'; TB = hi + lo to 2^-17) and tril(A_qk) row-major fp32: the B operands of
+// U0^T = V^T TB^T (a kind::f16 product whose A operand is the bf16 V staging itself, read
+// MN-major) and of O0^T = U0^T A_qk^T.
 constexpr uint32_t P_TBN = P_KB;
 constexpr uint32_t P_PN = P_KB + 16384;
 constexpr uint32_t P_XTRA = P_TBT + 16384;
@@ -158,7 +160,7 @@ constexpr uint32_t TM_U0T = 384;  // 64: V^T TB^T = U0^T (lanes = value columns)
 constexpr uint32_t TM_O0T = 448;  // 64: U0^T A_qk^T = (A_qk TB V)^T = (P V)^T
 
 struct PrepMisc {
-  uint64_t bar_tma, bar_a, bar_p, bar_u, bar_e, bar_drain;
+  uint64_t bar_tma, bar_v, bar_a, bar_p, bar_u, bar_e, bar_drain;
   uint32_t tmem_base;
   int abort;
   int nxt[4];  // item, t0, n, head of the item whose loads are in flight
@@ -202,7 +204,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
   const int chh = warp >> 2;  // half of the columns / channels
   const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
   const bool need_out = p.package == 0;
-  const uint32_t tx_bytes = (need_out ? 16384u : 0u) + 16384u + 16384u + 32768u + 1024u;
+  const uint32_t tx_bytes = (need_out ? 16384u : 0u) + 16384u + 32768u + 1024u;  // q, k, g, beta
 
   if (warp == 0) {
     tmem_alloc(&misc->tmem_base, 512);
@@ -210,6 +212,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
   }
   if (tid == 0) {
     mbar_init(&misc->bar_tma, 1);
+    mbar_init(&misc->bar_v, 1);
     mbar_init(&misc->bar_a, 1);
     mbar_init(&misc->bar_p, 1);
     mbar_init(&misc->bar_u, 1);
@@ -235,12 +238,17 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     }
     tma_load_3d(sm + P_STG_K, &tmk, &misc->bar_tma, 0, hh, t0);
     tma_load_3d(sm + P_STG_K + 8192, &tmk, &misc->bar_tma, 64, hh, t0);
-    tma_load_3d(sm + P_STG_V, &tmv, &misc->bar_tma, 0, hh, t0);
-    tma_load_3d(sm + P_STG_V + 8192, &tmv, &misc->bar_tma, 64, hh, t0);
 #pragma unroll
     for (int kb = 0; kb < 4; ++kb)
       tma_load_3d(sm + P_STG_G + kb * 8192, &tmg, &misc->bar_tma, kb * 32, hh, t0);
     tma_load_2d(sm + P_STG_B, &tmb, &misc->bar_tma, hh & ~3, t0);
+  };
+  // v has its own barrier: its staging is the A operand of the U0^T product, so the next
+  // item's v is loaded once that product is complete
+  auto issue_v = [&](int t0, int hh) {
+    mbar_arrive_expect_tx(&misc->bar_v, 16384u);
+    tma_load_3d(sm + P_STG_V, &tmv, &misc->bar_v, 0, hh, t0);
+    tma_load_3d(sm + P_STG_V + 8192, &tmv, &misc->bar_v, 64, hh, t0);
   };
   // thread 0: finds this CTA's next item holding a chunk, from `from` on, and issues its loads
   auto advance = [&](int from) {
@@ -258,6 +266,8 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
   constexpr int kLoader = 32;
   bool tma_out = false;  // loader: a load is in flight, completing phase parity tma_par
   uint32_t tma_par = 0;
+  bool v_issued = false;  // loader: a v load was issued, the last completing phase v_par
+  uint32_t v_par = 0;
   int prev_item = -1;    // loader: item whose record's store group is the latest but one
   uint32_t pub_n = 0;    // loader: items handed to the publishing warp
   // loader: hands an item (or -1, the end) to the publishing warp of a fused launch
@@ -270,7 +280,13 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     misc->pub_ring[pub_n & 3] = it;
     st_release_cta(&misc->pub_head, ++pub_n);
   };
-  if (tid == kLoader) tma_out = advance(first);
+  if (tid == kLoader) {
+    tma_out = advance(first);
+    if (tma_out) {
+      issue_v(misc->nxt[1], misc->nxt[3]);
+      v_issued = true;
+    }
+  }
   psync();
 
   uint32_t k_it = 0;
@@ -317,7 +333,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     if (tid == kLoader) bulk_wait_read0();  // the previous record has left the staging buffers
     pbar();
     // ================= operands (row role: token t; key rows in warps 0,1,4,5, query rows
-    // and values in warps 2,3,6,7; channel half chh)
+    // in warps 2,3,6,7; channel half chh)
     {
       const int t = (qd & 1) * 32 + lane;
       const bool valid = t < n;
@@ -386,11 +402,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
 #pragma unroll
           for (int u = 0; u < 16; u += 8) {
             const int c0 = chh * 64 + cb + u;
-            float vv[8], x[8];
-            load_bf8(P_STG_V, c0, vv);
-#pragma unroll
-            for (int e = 0; e < 8; ++e)
-              *f32at(sm, P_BE + sw128_off32(128 + c0 + e, t, P_BE_KB)) = valid ? vv[e] : 0.0f;
+            float x[8];
             if (need_out || cb >= 32) load_x(c0, x);
             if (need_out) {
               float qv[8];
@@ -410,6 +422,14 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
           tmem_st16(tbase + lane_base + TM_XA + chh * 64 + cb, qh);
         }
       }
+    }
+    if (qd >= 2 && !((qd & 1) * 32 + lane < n)) {
+      // token t past a partial chunk's end: its v row (box chh) reads as zero in the U0^T
+      // product whatever the staging holds (the next range's tokens)
+      if (!mbar_wait(&misc->bar_v, par)) misc->abort = 1;
+      uint4* row = reinterpret_cast<uint4*>(sm + P_STG_V + chh * 8192 + ((qd & 1) * 32 + lane) * 128);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) row[j] = make_uint4(0u, 0u, 0u, 0u);
     }
     tmem_st_wait();
     fence_proxy_async_smem();
@@ -558,10 +578,24 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
 #pragma unroll
       for (int j = 0; j < 32; ++j)
         *f32at(sm, P_TBT + sw128_off32(chh * 32 + j, r, P_TBT_KB)) = v[j];
+      // TB rows as bf16 hi and lo parts: 16-byte chunk m of the row holds columns 8 m .. 8 m + 7
 #pragma unroll
-      for (int j = 0; j < 32; j += 4)
-        *reinterpret_cast<float4*>(sm + P_TBN + sw128_off32(r, chh * 32 + j, 8192)) =
-            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+      for (int m = 0; m < 4; ++m) {
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a = v[8 * m + 2 * e], b = v[8 * m + 2 * e + 1];
+          const __nv_bfloat162 hi2 = __floats2bfloat162_rn(a, b);
+          const __nv_bfloat162 lo2 =
+              __floats2bfloat162_rn(a - __low2float(hi2), b - __high2float(hi2));
+          hw[e] = *reinterpret_cast<const uint32_t*>(&hi2);
+          lw[e] = *reinterpret_cast<const uint32_t*>(&lo2);
+        }
+        const uint32_t off =
+            (uint32_t)r * 128u + ((((uint32_t)(chh * 4 + m)) ^ ((uint32_t)r & 7u)) << 4);
+        *reinterpret_cast<uint4*>(sm + P_TBN + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(sm + P_TBN + 8192 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
     } else {
       float z[16];
 #pragma unroll
@@ -593,15 +627,20 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
                     id64, 1);
       }
       mma_commit(&misc->bar_p);
+      // U0^T = V^T (TB_hi + TB_lo)^T: A is the v staging read MN-major (value channel c of
+      // token t at row t; the two 64-channel boxes 8 KiB apart), 16 tokens per K-step
+      bool ok = mbar_wait(&misc->bar_v, par);
+      if (ok) {
+        const uint32_t idv = idesc_make(kFmtBF16, 128, 64, true, false);
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t kb = (s >> 2) * P_TBT_KB + (s & 3) * 32;
-        mma_tf32(tbase + TM_U0T,
-                 sdesc_sw128(sbase + P_BE + (s >> 2) * P_BE_KB + 16384 + (s & 3) * 32, 16, 1024),
-                 sdesc_sw128(sbase + P_TBN + kb, 16, 1024), id64, s > 0);
+        for (int s = 0; s < 4; ++s) {
+          const uint64_t a = sdesc_sw128(sbase + P_STG_V + s * 2048, 8192, 1024);
+          mma_f16(tbase + TM_U0T, a, sdesc_sw128(sbase + P_TBN + s * 32, 16, 1024), idv, s > 0);
+          mma_f16(tbase + TM_U0T, a, sdesc_sw128(sbase + P_TBN + 8192 + s * 32, 16, 1024), idv, 1);
+        }
       }
       mma_commit(&misc->bar_u);
-      bool ok = mbar_wait(&misc->bar_p, par);
+      ok = ok && mbar_wait(&misc->bar_p, par);
       tc_fence_after();
       if (ok) {
 #pragma unroll
@@ -629,6 +668,11 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     if (misc->abort) break;
     if (!mbar_wait(&misc->bar_e, par)) misc->abort = 1;
     tc_fence_after();
+    if (tid == kLoader && !misc->abort && misc->nxt[0] < n_items) {
+      issue_v(misc->nxt[1], misc->nxt[3]);  // the U0^T product has read this item's v
+      v_issued = true;
+      v_par = par ^ 1u;
+    }
     // ================= workspace record: rows staged in shared memory in the boxes'
     // 128-byte swizzle (16-byte chunk j of row r at ((j ^ (r & 7)) << 4)), then bulk stores
     {
@@ -705,6 +749,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       mbar_wait(&misc->bar_drain, 0, 100000000ull);
     }
     if (tid == kLoader && tma_out) mbar_wait(&misc->bar_tma, tma_par, 100000000ull);
+    if (tid == kLoader && v_issued) mbar_wait(&misc->bar_v, v_par, 100000000ull);
   }
   if (tid == kLoader) {
     bulk_wait0();
@@ -740,9 +785,12 @@ constexpr uint32_t S_STAGE = 98304;     // one chunk's [W ; Q''] (64 KiB) and Kb
 constexpr uint32_t S_WQ = 0;            // 4 K-blocks of [128][32] fp32
 constexpr uint32_t S_KBT = 65536;       // 2 K-blocks of [128][32] fp32
 constexpr uint32_t S_DEC = 2 * S_STAGE;  // 3 x [128] fp32: the chunk decays (ring of 3)
-constexpr uint32_t S_OST = S_DEC + 2048;  // 8 warps x [32 tokens][32 columns] bf16
-constexpr uint32_t S_MISC = S_OST + 8 * 2048;
+constexpr uint32_t S_MISC = S_DEC + 3 * 512;
+// Kept under the 196 KiB shared-memory carve-out (with the 1 KiB the system reserves per CTA),
+// so that the SM keeps 60 KiB of L1 for the compute warps' U0^T / O0^T loads; at the 228 KiB
+// carve-out the 28 KiB left for L1 stalled those loads for about a thousand cycles a chunk.
 constexpr uint32_t S_SMEM = S_MISC + 256 + 1024;
+static_assert(S_SMEM + 1024 <= 196 * 1024, "state kernel shared memory above the 196 KiB carve-out");
 constexpr uint32_t TS_S = 0;     // 128: S^T
 constexpr uint32_t TS_X = 128;   // 128: X^T
 constexpr uint32_t TS_Y = 256;   // 128: Y^T
@@ -770,8 +818,8 @@ __device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { retur
 // With `flags`, waits (acquire) for each item's record before reading it.
 __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMap& twq,
                                           const CUtensorMap& tkbt, const CUtensorMap& tdec,
-                                          const CUtensorMap& tout, const Ws& ws, const int tile,
-                                          const int h, const int ridx, const uint32_t* flags) {
+                                          const Ws& ws, const int tile, const int h,
+                                          const int ridx, const uint32_t* flags) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   StateMisc* misc = reinterpret_cast<StateMisc*>(sm + S_MISC);
@@ -995,37 +1043,6 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
           }
         }
       }
-      // outputs: through this warp's staging area and a bulk store while Y is on the tensor
-      // core; partial blocks of a range's last chunk with plain stores
-      if (!pkg && p.o) {
-        if (nvalid >= hf * 32 + 32) {
-          // this warp's 32 x 32 output block through its staging area and one bulk store
-          uint8_t* ost = sm + S_OST + warp * 2048;
-          if (lane == 0) bulk_wait_read0();  // the previous block has left the staging area
-          __syncwarp();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&ob16[i]);
-            *reinterpret_cast<__nv_bfloat16*>(ost + (2 * i) * 64 + lane * 2) = b.x;
-            *reinterpret_cast<__nv_bfloat16*>(ost + (2 * i + 1) * 64 + lane * 2) = b.y;
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_3d(&tout, ost, qd * 32, h, t0 + hf * 32);
-            bulk_commit();
-          }
-        } else {
-          __nv_bfloat16* o = (__nv_bfloat16*)p.o + ((int64_t)t0 * H + h) * DK + n;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const int t = hf * 32 + 2 * i;
-            const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&ob16[i]);
-            if (t < nvalid) o[(int64_t)t * H * DK] = b.x;
-            if (t + 1 < nvalid) o[(int64_t)(t + 1) * H * DK] = b.y;
-          }
-        }
-      }
       // ================= S^T = S^T Diag(e^gamma_C) + Y^T (channels 64 hf ..)
       if (!mbar_wait_relaxed(&misc->bar_y, par)) misc->abort = 1;
       tc_fence_after();
@@ -1053,13 +1070,24 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
         __syncwarp();
         if (lane == 0 && j + 1 < nch) mbar_arrive_relaxed(&misc->s_ready[hf]);
       }
+      // outputs, after the state update has released the next chunk's X product: token t of
+      // column n (32 lanes = 64 contiguous bytes of one token's row)
+      if (!pkg && p.o) {
+        __nv_bfloat16* o = (__nv_bfloat16*)p.o + ((int64_t)t0 * H + h) * DK + n;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int t = hf * 32 + 2 * i;
+          const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&ob16[i]);
+          if (t < nvalid) o[(int64_t)t * H * DK] = b.x;
+          if (t + 1 < nvalid) o[(int64_t)(t + 1) * H * DK] = b.y;
+        }
+      }
       // the next chunk's register operands (this chunk's are consumed), loaded while the next
       // chunk's X is on the tensor core (the issuer has brought them into L2)
       if (j + 1 < nch) load_regs(j + 1, u0, o0);
       if (misc->abort) break;
     }
   }
-  if (!issuer && lane == 0) bulk_wait0();  // this warp's output stores have completed
   cta_sync();
   if (!issuer && !misc->abort) {  // exit state rows c of column n (coalesced across lanes)
     const int64_t sh = (int64_t)ridx * H + h;
@@ -1085,9 +1113,8 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const __grid_constant__ ChunkParams p,
                    const __grid_constant__ CUtensorMap twq,
                    const __grid_constant__ CUtensorMap tkbt,
-                   const __grid_constant__ CUtensorMap tdec,
-                   const __grid_constant__ CUtensorMap tout, const Ws ws) {
-  state_run(p, twq, tkbt, tdec, tout, ws, blockIdx.x, blockIdx.y, blockIdx.z, nullptr);
+                   const __grid_constant__ CUtensorMap tdec, const Ws ws) {
+  state_run(p, twq, tkbt, tdec, ws, blockIdx.x, blockIdx.y, blockIdx.z, nullptr);
 }
 
 // ============================================================================ fused launch
@@ -1107,14 +1134,12 @@ chunk_fused_kernel(const __grid_constant__ ChunkParams p, const __grid_constant_
                    const __grid_constant__ CUtensorMap twq_st,
                    const __grid_constant__ CUtensorMap twq,
                    const __grid_constant__ CUtensorMap tkbt,
-                   const __grid_constant__ CUtensorMap tdec,
-                   const __grid_constant__ CUtensorMap tout, const Ws ws, const int n_items,
+                   const __grid_constant__ CUtensorMap tdec, const Ws ws, const int n_items,
                    const int n_state, uint32_t* flags) {
   const int b = blockIdx.x;
   if (b < n_state) {
     const int tiles = p.package ? 2 : 1;
-    state_run(p, twq, tkbt, tdec, tout, ws, b % tiles, (b / tiles) % p.H, b / (tiles * p.H),
-              flags);
+    state_run(p, twq, tkbt, tdec, ws, b % tiles, (b / tiles) % p.H, b / (tiles * p.H), flags);
   } else {
     // the prep work uses 8 warps; the ninth publishes the finished items' flags
     extern __shared__ uint8_t smem_raw[];
@@ -1214,20 +1239,6 @@ bool make_map_ws(CUtensorMap* m, const void* ptr, uint64_t rows, uint64_t cols, 
   return r == CUDA_SUCCESS;
 }
 
-// o [T, H, 128] bf16 as a 3-D tensor (128, H, T); box (32, 1, 32): one warp's output block.
-bool make_map_out(CUtensorMap* m, const void* ptr, int T, int H) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)DK, (cuuint64_t)H, (cuuint64_t)(T > 0 ? T : 1)};
-  cuuint64_t strides[2] = {(cuuint64_t)DK * 2, (cuuint64_t)H * DK * 2};
-  cuuint32_t box[3] = {32, 1, 32};
-  cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
-                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 // dec [items][128] fp32 as a 2-D tensor (128, items); box (128, 1): one item's decays.
 bool make_map_dec(CUtensorMap* m, const float* ptr, uint64_t items) {
   EncodeTiledFn enc = encode_fn();
@@ -1295,7 +1306,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   uint32_t* flags = (uint32_t*)(base + (size_t)n_items * kItemBytes);
 
   const bool do_prep = (phases & kPhasePrep) != 0, do_state = (phases & kPhaseState) != 0;
-  CUtensorMap mq, mk, mv, mg, mb, mwq, mkbt, mdec, swq, mo;
+  CUtensorMap mq, mk, mv, mg, mb, mwq, mkbt, mdec, swq;
   const uint64_t rows128 = (uint64_t)n_items * 128;
   bool maps_ok = true;
   if (do_prep) {
@@ -1310,8 +1321,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   if (maps_ok && do_state) {
     maps_ok = make_map_ws(&mwq, ws.wq, rows128, 128, 128) &&
               make_map_ws(&mkbt, ws.kbt, rows128, 64, 128) &&
-              make_map_dec(&mdec, ws.dec, (uint64_t)n_items) &&
-              make_map_out(&mo, p.o ? p.o : (const void*)ws.wq, p.total_tokens, p.H);
+              make_map_dec(&mdec, ws.dec, (uint64_t)n_items);
   }
   if (!maps_ok)
     return set_error(KDA_ERR_CUDA, "tensor-core chunk path: cuTensorMapEncodeTiled failed");
@@ -1347,7 +1357,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, chunk_fused_kernel, p, mq, mk, mv, mg, mb, swq, mwq, mkbt, mdec,
-                           mo, ws, (int)n_items, (int)n_state, flags);
+                           ws, (int)n_items, (int)n_state, flags);
     if (e == cudaSuccess) {
       count_launches(1);
       return check_launch("tensor-core chunk fused kernel");
@@ -1363,7 +1373,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
     if (st != KDA_OK || !do_state) return st;
   }
   dim3 grid2(tiles, p.H, p.n_ranges);
-  chunk_state_kernel<<<grid2, kStateThreads, S_SMEM, s>>>(p, mwq, mkbt, mdec, mo, ws);
+  chunk_state_kernel<<<grid2, kStateThreads, S_SMEM, s>>>(p, mwq, mkbt, mdec, ws);
   count_launches(1);
   return check_launch("tensor-core chunk state kernel");
 }
