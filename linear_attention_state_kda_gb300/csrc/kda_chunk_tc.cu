@@ -141,12 +141,14 @@ constexpr uint32_t SCR_A = P_KB;          // beta_r A_kk [64][68] (Kb is dead by
 constexpr uint32_t SCR_X = P_XTRA;        // (I + A_kk)^-1 [64][68]
 constexpr uint32_t SCR_P = P_XTRA + 64 * LA * 4;  // 8 warps x [16][8]
 constexpr uint32_t P_MISC = SCR_P + 8 * 128 * 4;
-// Workspace-record staging for the bulk-tensor stores, over Kb, [K'^T ; V^T] and TB^T (all
-// dead once the last products are complete): W and Q'' as 4 boxes of [64 rows][32] fp32 in the
-// 128-byte swizzle (U0^T and O0^T go straight from registers to their interleaved records).
-constexpr uint32_t ST_W = P_KB;
-constexpr uint32_t ST_Q = P_KB + 32768;
-static_assert(ST_Q + 32768 <= P_XTRA, "record staging overflow");
+// Workspace-record staging for the bulk-tensor stores (U0^T and O0^T go straight from
+// registers to their interleaved records): W and Q'' as 4 boxes of [64 rows][32] fp32 in the
+// 128-byte swizzle. Q'' over the Kb buffer and W over TB^T and the solve's X scratch, all dead
+// once the last products are complete. Only Q'' (stored first) has to have left before the
+// next item's operands are written; W's region is next written by that item's solve.
+constexpr uint32_t ST_Q = P_KB;
+constexpr uint32_t ST_W = P_TBT;
+static_assert(ST_W + 32768 <= SCR_P, "W staging overflow");
 constexpr uint32_t P_SMEM = P_MISC + 2048 + 1024;
 static_assert(64 * LA * 4 <= 32768, "A_kk scratch must fit in the Kb buffer");
 static_assert(P_KB % 1024 == 0 && P_BE % 1024 == 0 && P_TBT % 1024 == 0, "alignment");
@@ -330,7 +332,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
         *f32at(sm, gbase + (uint32_t)i * 128u + ((xg ^ (uint32_t)(i & 7)) << 4)) = gam - rho2;
       }
     }
-    if (tid == kLoader) bulk_wait_read0();  // the previous record has left the staging buffers
+    if (tid == kLoader) bulk_wait_read1();  // the previous record's Q'' has left its staging
     pbar();
     // ================= operands (row role: token t; key rows in warps 0,1,4,5, query rows
     // in warps 2,3,6,7; channel half chh)
@@ -340,9 +342,10 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       const uint32_t tsw = (uint32_t)(t & 7);
       const uint32_t grow = P_STG_G + (uint32_t)t * 128u;
       const uint32_t brow = (uint32_t)t * 128u;
-      // Kb (the B operand of A1) and Kb'^T (workspace) of token t: key-row threads cover the
-      // first 32 channels of their half, query-row threads the last 32, so both roles issue
-      // 96 exponentials per thread
+      // Kb (the B operand of A1), Kb'^T (workspace) and K'^T (B operand of R) of token t:
+      // key-row threads cover the first 32 channels of their half, query-row threads the last
+      // 32 (reusing the query's e^x), so both roles issue 96 exponentials and 32 transposed
+      // stores per thread
       float* kbt_out = ws.kbt + (size_t)item * DK * C + t;
       auto load_x = [&](int c0, float* x) {  // gamma - rho of channels c0 .. c0 + 7
         const uint32_t g0 = grow + (uint32_t)(c0 >> 5) * 8192u;
@@ -387,11 +390,13 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
             const float4 eb = *reinterpret_cast<const float4*>(misc->erho + c0 + 4);
             const float er[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              kh[u + e] = (valid ? kv[e] : 0.0f) * ex2_approx(x[e]);
-              *f32at(sm, P_BE + sw128_off32(c0 + e, t, P_BE_KB)) = kh[u + e] * er[e];  // K'^T
+            for (int e = 0; e < 8; ++e) kh[u + e] = (valid ? kv[e] : 0.0f) * ex2_approx(x[e]);
+            if (cb < 32) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e)  // K'^T
+                *f32at(sm, P_BE + sw128_off32(c0 + e, t, P_BE_KB)) = kh[u + e] * er[e];
+              kb_out(c0, x, kv);
             }
-            if (cb < 32) kb_out(c0, x, kv);
           }
           tmem_st16(tbase + lane_base + TM_XA + chh * 64 + cb, kh);
         }
@@ -402,13 +407,17 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
 #pragma unroll
           for (int u = 0; u < 16; u += 8) {
             const int c0 = chh * 64 + cb + u;
-            float x[8];
-            if (need_out || cb >= 32) load_x(c0, x);
+            float x[8], ex[8];
+            if (need_out || cb >= 32) {
+              load_x(c0, x);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) ex[e] = ex2_approx(x[e]);
+            }
             if (need_out) {
               float qv[8];
               load_bf8(P_STG_Q, c0, qv);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) qh[u + e] = valid ? qv[e] * ex2_approx(x[e]) : 0.0f;
+              for (int e = 0; e < 8; ++e) qh[u + e] = valid ? qv[e] * ex[e] : 0.0f;
             } else {
 #pragma unroll
               for (int e = 0; e < 8; ++e) qh[u + e] = 0.0f;
@@ -416,6 +425,13 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
             if (cb >= 32) {
               float kv[8];
               load_bf8(P_STG_K, c0, kv);
+              const float4 ea = *reinterpret_cast<const float4*>(misc->erho + c0);
+              const float4 eb = *reinterpret_cast<const float4*>(misc->erho + c0 + 4);
+              const float er[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
+#pragma unroll
+              for (int e = 0; e < 8; ++e)  // K'^T
+                *f32at(sm, P_BE + sw128_off32(c0 + e, t, P_BE_KB)) =
+                    (valid ? kv[e] : 0.0f) * ex[e] * er[e];
               kb_out(c0, x, kv);
             }
           }
@@ -448,6 +464,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     if (tid == kLoader && !misc->abort) {
       tma_out = advance(item + stride);
       tma_par = par ^ 1u;
+      bulk_wait_read0();  // the previous record's W has left its staging (the solve's scratch)
       // Hand the previous item to the publishing warp: its record's store group was committed
       // a phase ago (this item's group is not committed yet), and the generic stores of its
       // record were ordered before this release by the barriers since. The publishing warp
@@ -576,7 +593,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       tmem_st16(tbase + lane_base + TM_E + chh * 32, v);
       tmem_st16(tbase + lane_base + TM_E + chh * 32 + 16, v + 16);
 #pragma unroll
-      for (int j = 0; j < 32; ++j)
+      for (int j = 0; j < 16; ++j)  // TB^T, first 16 of the 32 columns (the rest: warps qd >= 2)
         *f32at(sm, P_TBT + sw128_off32(chh * 32 + j, r, P_TBT_KB)) = v[j];
       // TB rows as bf16 hi and lo parts: 16-byte chunk m of the row holds columns 8 m .. 8 m + 7
 #pragma unroll
@@ -602,6 +619,20 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       for (int j = 0; j < 16; ++j) z[j] = 0.0f;
       tmem_st16(tbase + lane_base + TM_E + chh * 32, z);
       tmem_st16(tbase + lane_base + TM_E + chh * 32 + 16, z);
+      {  // TB^T of row r = the thread's token, columns chh * 32 + 16 .. + 31
+        const int r = (qd - 2) * 32 + lane;
+        const float* xrow = f32at(sm, SCR_X) + r * LA + chh * 32 + 16;
+        const float* bt = misc->beta + chh * 32 + 16;
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+          const float4 t4 = *reinterpret_cast<const float4*>(xrow + j);
+          const int c = chh * 32 + 16 + j;
+          *f32at(sm, P_TBT + sw128_off32(c, r, P_TBT_KB)) = t4.x * bt[j];
+          *f32at(sm, P_TBT + sw128_off32(c + 1, r, P_TBT_KB)) = t4.y * bt[j + 1];
+          *f32at(sm, P_TBT + sw128_off32(c + 2, r, P_TBT_KB)) = t4.z * bt[j + 2];
+          *f32at(sm, P_TBT + sw128_off32(c + 3, r, P_TBT_KB)) = t4.w * bt[j + 3];
+        }
+      }
       if (need_out) {  // tril(A_qk) rows (A1 lanes 64..127) -> row-major [t][t'] for O0^T
         const int t = (qd - 2) * 32 + lane;
         float v[32];
@@ -730,11 +761,14 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     fence_proxy_async_smem();
     psync();
     if (tid == kLoader) {
+      if (need_out) {
 #pragma unroll
-      for (int kb = 0; kb < 4; ++kb) {
-        tma_store_2d(&twq_st, sm + ST_W + kb * 8192, kb * 32, item * 128);
-        if (need_out) tma_store_2d(&twq_st, sm + ST_Q + kb * 8192, kb * 32, item * 128 + 64);
+        for (int kb = 0; kb < 4; ++kb)
+          tma_store_2d(&twq_st, sm + ST_Q + kb * 8192, kb * 32, item * 128 + 64);
+        bulk_commit();
       }
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) tma_store_2d(&twq_st, sm + ST_W + kb * 8192, kb * 32, item * 128);
       bulk_commit();
       if (flags) prev_item = item;  // published during the next item's A1 product
     }
