@@ -40,7 +40,7 @@ DECODE_BYTES_PER_ROW_HEAD = 2 * STATE_BYTES + 3 * D * 2 + D * 4 + 4 + D * 2
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one prefill_16k launch, from the
 # ncu capture summarised in profiles/ (None until a capture of the current kernel exists).
-TRAFFIC_PREFILL_16K = 1994.8e6  # 4 x 498.7 MB on the 4096-token case (traffic scales with tokens)
+TRAFFIC_PREFILL_16K = 1851.4e6  # 4 x 462.8 MB on the 4096-token case (traffic scales with tokens)
 
 
 def _peaks():
@@ -198,6 +198,9 @@ def run_gb300(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        # hold the stream on the device while the host enqueues the timed steps, so that the
+        # events time device execution only (not the host's launch latency)
+        torch.cuda._sleep(int(4e7))
         step_ev[0].record(stream)
         for i in range(args.steps):
             for n, fn in parts:
@@ -374,10 +377,15 @@ def run_profile_case(args):
         sso = torch.tensor([0, 2], dtype=torch.int32, device=dev)
         M, Dp = kda.segment_package(x.k, x.v, x.g, x.beta, offs)
         si, _ = kda.package_scan(M, Dp, sso, 2)
+        # the scan at the bench's tree shape: 8 packages per head (8 segments of 512 tokens)
+        offs8 = torch.arange(0, 4097, 512, dtype=torch.int32, device=dev)
+        sso8 = torch.tensor([0, 8], dtype=torch.int32, device=dev)
+        M8, D8 = kda.segment_package(x.k, x.v, x.g, x.beta, offs8)
+        si8, _ = kda.package_scan(M8, D8, sso8, 8)
         fns = {
             "prefill": [lambda: kda.chunk_prefill(x.q, x.k, x.v, x.g, x.beta)],
             "package": [lambda: kda.segment_package(x.k, x.v, x.g, x.beta, offs, M=M, D=Dp)],
-            "scan": [lambda: kda.package_scan(M, Dp, sso, 2, seg_init=si)],
+            "scan": [lambda: kda.package_scan(M8, D8, sso8, 8, seg_init=si8)],
             "replay": [lambda: kda.segment_replay(x.q, x.k, x.v, x.g, x.beta, offs, si)],
         }[case]
     torch.cuda.synchronize()
