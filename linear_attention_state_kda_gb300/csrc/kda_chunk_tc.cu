@@ -143,12 +143,13 @@ constexpr uint32_t SCR_P = P_XTRA + 64 * LA * 4;  // 8 warps x [16][8]
 constexpr uint32_t P_MISC = SCR_P + 8 * 128 * 4;
 // Workspace-record staging for the bulk-tensor stores (U0^T and O0^T go straight from
 // registers to their interleaved records): W and Q'' as 4 boxes of [64 rows][32] fp32 in the
-// 128-byte swizzle. Q'' over the Kb buffer and W over TB^T and the solve's X scratch, all dead
-// once the last products are complete. Only Q'' (stored first) has to have left before the
-// next item's operands are written; W's region is next written by that item's solve.
-constexpr uint32_t ST_Q = P_KB;
+// 128-byte swizzle. Q'' over K'^T and W over TB^T and the solve's X scratch, all dead once R
+// is complete (the O0^T product may still be reading tril(A_qk) in the Kb buffer). Only Q''
+// (stored first) has to have left before the next item's operands are written; W's region is
+// next written by that item's solve.
+constexpr uint32_t ST_Q = P_BE;
 constexpr uint32_t ST_W = P_TBT;
-static_assert(ST_W + 32768 <= SCR_P, "W staging overflow");
+static_assert(ST_Q + 32768 <= P_TBT && ST_W + 32768 <= SCR_P, "record staging overflow");
 constexpr uint32_t P_SMEM = P_MISC + 2048 + 1024;
 static_assert(64 * LA * 4 <= 32768, "A_kk scratch must fit in the Kb buffer");
 static_assert(P_KB % 1024 == 0 && P_BE % 1024 == 0 && P_TBT % 1024 == 0, "alignment");
@@ -162,7 +163,7 @@ constexpr uint32_t TM_U0T = 384;  // 64: V^T TB^T = U0^T (lanes = value columns)
 constexpr uint32_t TM_O0T = 448;  // 64: U0^T A_qk^T = (A_qk TB V)^T = (P V)^T
 
 struct PrepMisc {
-  uint64_t bar_tma, bar_v, bar_a, bar_p, bar_u, bar_e, bar_drain;
+  uint64_t bar_tma, bar_v, bar_a, bar_p, bar_u, bar_r, bar_e, bar_drain;
   uint32_t tmem_base;
   int abort;
   int nxt[4];  // item, t0, n, head of the item whose loads are in flight
@@ -218,6 +219,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     mbar_init(&misc->bar_a, 1);
     mbar_init(&misc->bar_p, 1);
     mbar_init(&misc->bar_u, 1);
+    mbar_init(&misc->bar_r, 1);
     mbar_init(&misc->bar_e, 1);
     mbar_init(&misc->bar_drain, 1);
     misc->abort = 0;
@@ -680,16 +682,17 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
           mma_tf32_ts(tbase + TM_R, tbase + TM_E + s * 8,
                       sdesc_sw128(sbase + P_BE + kbe, 16, 1024), id128, s > 0);
         }
-        if (need_out) {
-          ok = mbar_wait(&misc->bar_u, par);
-          tc_fence_after();
-          if (ok) {
+      }
+      mma_commit(&misc->bar_r);  // R (and the products before it): the record can start
+      if (ok && need_out) {
+        ok = mbar_wait(&misc->bar_u, par);
+        tc_fence_after();
+        if (ok) {
 #pragma unroll
-            for (int s = 0; s < 8; ++s)
-              mma_tf32_ts(tbase + TM_O0T, tbase + TM_U0T + s * 8,
-                          sdesc_sw128(sbase + P_PN + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024),
-                          id64, s > 0);
-          }
+          for (int s = 0; s < 8; ++s)
+            mma_tf32_ts(tbase + TM_O0T, tbase + TM_U0T + s * 8,
+                        sdesc_sw128(sbase + P_PN + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024),
+                        id64, s > 0);
         }
       }
       if (!ok) misc->abort = 1;
@@ -697,7 +700,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     }
     pbar();
     if (misc->abort) break;
-    if (!mbar_wait(&misc->bar_e, par)) misc->abort = 1;
+    if (!mbar_wait(&misc->bar_r, par)) misc->abort = 1;
     tc_fence_after();
     if (tid == kLoader && !misc->abort && misc->nxt[0] < n_items) {
       issue_v(misc->nxt[1], misc->nxt[3]);  // the U0^T product has read this item's v
@@ -739,6 +742,9 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
         for (int j = 0; j < 8; ++j)
           dst[j * 128] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
       }
+      // O0^T, the last product
+      if (!mbar_wait(&misc->bar_e, par)) misc->abort = 1;
+      tc_fence_after();
       if (need_out) {
         float v[32];
         tmem_ld32(tbase + lane_base + TM_O0T + chh * 32, v);
@@ -913,7 +919,8 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
         }
         uint8_t* st = sm + (j & 1) * S_STAGE;
         uint64_t* bar = &misc->full[j & 1];
-        mbar_arrive_expect_tx(bar, S_STAGE + 512);
+        // package mode has no outputs: the boxes hold W's 64 rows only (not Q'')
+        mbar_arrive_expect_tx(bar, (pkg ? 32768u : 65536u) + 32768u + 512u);
 #pragma unroll
         for (int kb = 0; kb < 4; ++kb)
           tma_load_2d(st + S_WQ + kb * 16384, &twq, bar, kb * 32, item * 128);
@@ -934,6 +941,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
         if (ok) tma_last = j;
       }
       const uint32_t idesc = idesc_make(kFmtTF32, 128, 128, false, false);
+      const uint32_t idesc_x = pkg ? idesc_make(kFmtTF32, 128, 64, false, false) : idesc;
       for (int j = 0; j < nch && ok; ++j) {
         const uint32_t par = (uint32_t)j & 1u;
         const uint32_t st = (uint32_t)(j & 1) * S_STAGE;
@@ -950,7 +958,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
             for (int k = 0; k < 8; ++k) {
               const int ks = hh * 8 + k;  // K-step: channels 8 ks .. 8 ks + 7
               mma_tf32_ts(tbase + TS_X, tbase + TS_S + ks * 8,
-                          desc_add(d_wq, (ks >> 2) * 16384 + (ks & 3) * 32), idesc, ks > 0);
+                          desc_add(d_wq, (ks >> 2) * 16384 + (ks & 3) * 32), idesc_x, ks > 0);
             }
           }
         }
@@ -1353,7 +1361,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
               make_map_ws(&swq, ws.wq, rows128, 128, 64);
   }
   if (maps_ok && do_state) {
-    maps_ok = make_map_ws(&mwq, ws.wq, rows128, 128, 128) &&
+    maps_ok = make_map_ws(&mwq, ws.wq, rows128, 128, p.package ? 64 : 128) &&
               make_map_ws(&mkbt, ws.kbt, rows128, 64, 128) &&
               make_map_dec(&mdec, ws.dec, (uint64_t)n_items);
   }
