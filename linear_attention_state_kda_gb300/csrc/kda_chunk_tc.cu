@@ -363,11 +363,8 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
                                                  (((((uint32_t)c0 & 63u) >> 3) ^ tsw) << 4)),
                 y);
       };
-      auto kb_out = [&](int c0, const float* x, const float* kv) {
+      auto kb_out = [&](int c0, const float* x, const float* kv, const float* er) {
         float kb[8];
-        const float4 ea = *reinterpret_cast<const float4*>(misc->erho + c0);
-        const float4 eb = *reinterpret_cast<const float4*>(misc->erho + c0 + 4);
-        const float er[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           kb[e] = (valid ? kv[e] : 0.0f) * ex2_approx(-x[e]);
@@ -388,16 +385,16 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
             float x[8], kv[8];
             load_x(c0, x);
             load_bf8(P_STG_K, c0, kv);
-            const float4 ea = *reinterpret_cast<const float4*>(misc->erho + c0);
-            const float4 eb = *reinterpret_cast<const float4*>(misc->erho + c0 + 4);
-            const float er[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
 #pragma unroll
             for (int e = 0; e < 8; ++e) kh[u + e] = (valid ? kv[e] : 0.0f) * ex2_approx(x[e]);
             if (cb < 32) {
+              const float4 ea = *reinterpret_cast<const float4*>(misc->erho + c0);
+              const float4 eb = *reinterpret_cast<const float4*>(misc->erho + c0 + 4);
+              const float er[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
 #pragma unroll
               for (int e = 0; e < 8; ++e)  // K'^T
                 *f32at(sm, P_BE + sw128_off32(c0 + e, t, P_BE_KB)) = kh[u + e] * er[e];
-              kb_out(c0, x, kv);
+              kb_out(c0, x, kv, er);
             }
           }
           tmem_st16(tbase + lane_base + TM_XA + chh * 64 + cb, kh);
@@ -434,7 +431,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
               for (int e = 0; e < 8; ++e)  // K'^T
                 *f32at(sm, P_BE + sw128_off32(c0 + e, t, P_BE_KB)) =
                     (valid ? kv[e] : 0.0f) * ex[e] * er[e];
-              kb_out(c0, x, kv);
+              kb_out(c0, x, kv, er);
             }
           }
           tmem_st16(tbase + lane_base + TM_XA + chh * 64 + cb, qh);
@@ -535,48 +532,55 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
         }
       }
       pbar();
-      // off-diagonal blocks by distance d: X_IJ = -X_II sum_{L=J}^{I-1} A_IL X_LJ (J = I - d).
-      // Warp w < 2 (4 - d) owns block J = w / 2 and its 8-column half w % 2; both 16 x 16
-      // block products run as warp-level 3xTF32 MMAs (fp32-level accuracy), the partial
-      // product passing through a per-warp 16 x 8 tile of shared memory.
+      // Off-diagonal blocks as a 2 x 2 block inverse over 32 x 32 blocks, every 16 x 16 block
+      // product a warp-level 3xTF32 MMA (fp32-level accuracy) on a 16 x 8 column half:
+      //   T11 = [X00 0; X10 X11], X10 = -X11 A10 X00;  T22 = [X22 0; X32 X33], X32 = -X33 A32 X22
+      //   T21 = -T22 (A21 T11)  (A21 = rows 32..63, columns 0..31 of A)
+      // so the chain is four dependent products deep.
       const int gq = lane >> 2, tq = lane & 3;
-      float* Pw = Pp + warp * 128;  // [16][8]
-      for (int dist = 1; dist < 4; ++dist) {
-        if (warp < 2 * (4 - dist)) {
-          const int J = warp >> 1, I = J + dist, n0 = J * 16 + (warp & 1) * 8;
-          float d[4] = {0.f, 0.f, 0.f, 0.f};
-          for (int L = J; L < I; ++L) {
+      // d += A_IL (16 x 16 block of M, row stride LA) * B rows L*16.., columns n0 .. n0 + 7
+      auto blk = [&](float* d, const float* M, int I, int L, const float* B, int bstride, int n0) {
 #pragma unroll
-            for (int kk = 0; kk < 16; kk += 8) {
-              const float* ar = Akk + (I * 16 + gq) * LA + L * 16 + kk + tq;
-              const float a[4] = {ar[0], ar[8 * LA], ar[4], ar[8 * LA + 4]};
-              const float* br = X + (L * 16 + kk + tq) * LA + n0 + gq;
-              const float bv[2] = {br[0], br[4 * LA]};
-              mma16x8x8_3xtf32(d, a, bv);
-            }
-          }
-          Pw[gq * 8 + 2 * tq] = d[0];
-          Pw[gq * 8 + 2 * tq + 1] = d[1];
-          Pw[(gq + 8) * 8 + 2 * tq] = d[2];
-          Pw[(gq + 8) * 8 + 2 * tq + 1] = d[3];
-          __syncwarp();
-          float e[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-          for (int kk = 0; kk < 16; kk += 8) {
-            const float* ar = X + (I * 16 + gq) * LA + I * 16 + kk + tq;
-            const float a[4] = {ar[0], ar[8 * LA], ar[4], ar[8 * LA + 4]};
-            const float bv[2] = {Pw[(kk + tq) * 8 + gq], Pw[(kk + tq + 4) * 8 + gq]};
-            mma16x8x8_3xtf32(e, a, bv);
-          }
-          float* xr = X + (I * 16 + gq) * LA + n0 + 2 * tq;
-          xr[0] = -e[0];
-          xr[1] = -e[1];
-          xr[8 * LA] = -e[2];
-          xr[8 * LA + 1] = -e[3];
-          __syncwarp();
+        for (int kk = 0; kk < 16; kk += 8) {
+          const float* ar = M + (I * 16 + gq) * LA + L * 16 + kk + tq;
+          const float am[4] = {ar[0], ar[8 * LA], ar[4], ar[8 * LA + 4]};
+          const float* br = B + (kk + tq) * bstride + n0 + gq;
+          const float bv[2] = {br[0], br[4 * bstride]};
+          mma16x8x8_3xtf32(d, am, bv);
         }
-        pbar();
+      };
+      auto put = [&](float* dst, int stride, const float* d, float sgn) {  // 16 x 8 tile
+        dst[gq * stride + 2 * tq] = sgn * d[0];
+        dst[gq * stride + 2 * tq + 1] = sgn * d[1];
+        dst[(gq + 8) * stride + 2 * tq] = sgn * d[2];
+        dst[(gq + 8) * stride + 2 * tq + 1] = sgn * d[3];
+      };
+      float* Pw = Pp + warp * 128;  // this warp's [16][8] tile
+      if (warp < 4) {  // X10 (warps 0, 1) and X32 (warps 2, 3), column half warp % 2
+        const int J = (warp >> 1) * 2, I = J + 1, n0 = J * 16 + (warp & 1) * 8;
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        blk(d, Akk, I, J, X + J * 16 * LA, LA, n0);
+        put(Pw, 8, d, 1.0f);
+        __syncwarp();
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+        blk(e, X, I, I, Pw, 8, 0);
+        put(X + I * 16 * LA + n0, LA, e, -1.0f);
       }
+      pbar();
+      // warp w: block (I, J) = (2 + w / 4, (w / 2) % 2) of T21, column half w % 2
+      const int I2 = 2 + (warp >> 2), J2 = (warp >> 1) & 1, n2 = J2 * 16 + (warp & 1) * 8;
+      {  // Y_IJ = sum_{L=J}^{1} A_IL X_LJ  (A21 T11)
+        float d[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int L = J2; L < 2; ++L) blk(d, Akk, I2, L, X + L * 16 * LA, LA, n2);
+        put(Pw, 8, d, 1.0f);
+      }
+      pbar();
+      {  // X_IJ = -sum_{L=2}^{I} X_IL Y_LJ  (Y_LJ: the tile of warp ((L - 2) << 2) | (warp & 3))
+        float e[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int L = 2; L <= I2; ++L) blk(e, X, I2, L, Pp + (((L - 2) << 2) | (warp & 3)) * 128, 8, 0);
+        put(X + I2 * 16 * LA + n2, LA, e, -1.0f);
+      }
+      pbar();
     }
     // ================= TB = T Diag(beta): TMEM E lanes 0..63 (lanes 64..127 zero) and TB^T
     if (qd < 2) {
