@@ -40,7 +40,7 @@ DECODE_BYTES_PER_ROW_HEAD = 2 * STATE_BYTES + 3 * D * 2 + D * 4 + 4 + D * 2
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one prefill_16k launch, from the
 # ncu capture summarised in profiles/ (None until a capture of the current kernel exists).
-TRAFFIC_PREFILL_16K = 1851.4e6  # 4 x 462.8 MB on the 4096-token case (traffic scales with tokens)
+TRAFFIC_PREFILL_16K = 1852.0e6  # 4 x 463.0 MB on the 4096-token case (traffic scales with tokens)
 
 
 def _peaks():
