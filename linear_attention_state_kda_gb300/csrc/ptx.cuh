@@ -152,14 +152,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* s
                : "memory");
 }
 // 3-D tiled bulk-tensor store from shared memory (see tma_store_2d).
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* src, int c0, int c1,
-                                             int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
-          (uint64_t)m),
-      "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
-      : "memory");
-}
 // Contiguous bulk copy shared -> global (both 16-byte aligned, size a multiple of 16), tracked
 // by this thread's bulk groups.
 __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
@@ -185,9 +177,6 @@ __device__ __forceinline__ void bulk_wait0() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 // Waits until all but the most recently committed bulk-store group of this thread completed.
-__device__ __forceinline__ void bulk_wait1() {
-  asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");
-}
 
 // ---------------------------------------------------------------- cross-CTA flags
 // Orders this thread's generic-proxy accesses of global memory with its async-proxy ones.
