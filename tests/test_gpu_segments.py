@@ -149,3 +149,22 @@ def test_prepared_records_serve_package_and_replay():
     M2, D2 = kda.segment_package_prepared(ws2, r["offs"], T, H, dk, dv)
     torch.cuda.synchronize()
     assert torch.equal(M2, r["M"]) and torch.equal(D2, r["D"])
+
+
+def test_fused_prefill_matches_two_kernel_walk():
+    """The 16k single-sequence prefill runs as one cooperative launch (walks next to the prep
+    work, records handed over through per-record flags); the same walk over the same records
+    from two separate launches (prepare, then a one-segment replay from a zero state) must give
+    bit-identical outputs and final states, every time."""
+    x = inputs.make_workload("prefill_16k", device=DEV)
+    T, H, dk = x.k.shape
+    dv = x.v.shape[2]
+    offs = torch.tensor([0, T], dtype=torch.int32, device=DEV)
+    zero = torch.zeros(1, H, dk, dv, dtype=torch.float32, device=DEV)
+    ws = kda.chunk_prepare(x.q, x.k, x.v, x.g, x.beta, offs)
+    o_ref, f_ref = kda.segment_replay_prepared(ws, offs, zero, T, H, dk, dv, want_final=True)
+    for _ in range(3):
+        o, f = kda.chunk_prefill(x.q, x.k, x.v, x.g, x.beta)
+        torch.cuda.synchronize()
+        assert torch.equal(o, o_ref)
+        assert torch.equal(f, f_ref)
