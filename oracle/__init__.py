@@ -44,6 +44,9 @@ def _load():
         lib.kda_ref_decode.argtypes = [c_int, c_int, c_int, c_int, c_dbl, d, d, d, d, d, i64,
                                        d, c_i64, d, c_int]
         lib.kda_ref_decode.restype = c_int
+        lib.kda_ref_decode_window.argtypes = [c_int, c_int, c_int, c_int, c_int, c_dbl, d, d, d,
+                                              d, d, c_int, i64, i64, d, c_i64, d, c_int]
+        lib.kda_ref_decode_window.restype = c_int
         _lib = lib
     return _lib
 
@@ -150,3 +153,59 @@ def decode(q, k, v, g, beta, slot_ids, pool, scale=1.0, threads=0):
     if rc < 0:
         raise ValueError("kda_ref_decode: bad arguments")
     return o, rc
+
+
+def decode_window(q, k, v, g, beta, read_slots, write_slots, pool, scale=1.0,
+                  beta_is_logit=False, threads=0):
+    """Verify window with a state fork over pool [n_slots,H,dk,dv] (a float64 copy, updated
+    in place): row b reads slot read_slots[b], runs the W tokens of its window (token b*W + j,
+    arrays [B*W, H, *]) and stores the state after token j into slot write_slots[b, j].
+    Returns (o [B*W,H,dv], number of slot ids >= n_slots)."""
+    lib = _load()
+    q, k, v, g, beta = _f64(q), _f64(k), _f64(v), _f64(g), _f64(beta)
+    rs = _i64(read_slots)
+    ws = _i64(write_slots)
+    B = rs.shape[0]
+    W = ws.size // B if B else 0
+    assert ws.size == B * W
+    n_tok, H, dk = k.shape
+    assert n_tok == B * W
+    dv = v.shape[2]
+    assert pool.dtype == np.float64 and pool.flags["C_CONTIGUOUS"]
+    o = np.zeros((n_tok, H, dv))
+    rc = lib.kda_ref_decode_window(B, W, H, dk, dv, float(scale), _ptr(q), _ptr(k), _ptr(v),
+                                   _ptr(g), _ptr(beta), int(bool(beta_is_logit)),
+                                   _ptr(rs, ctypes.c_int64), _ptr(ws.reshape(-1), ctypes.c_int64),
+                                   _ptr(pool), pool.shape[0], _ptr(o), int(threads))
+    if rc < 0:
+        raise ValueError("kda_ref_decode_window: bad arguments")
+    return o, rc
+
+
+def slot_zero(pool, slot_ids):
+    """Sets pool[s] = 0 for every listed slot s (pool [n_slots, ...], updated in place).
+    Negative ids are skipped; ids >= n_slots are skipped and counted. Returns the count."""
+    n = pool.shape[0]
+    bad = 0
+    for s in np.asarray(slot_ids, dtype=np.int64).reshape(-1):
+        if s >= n:
+            bad += 1
+        elif s >= 0:
+            pool[s] = 0
+    return bad
+
+
+def slot_copy(src, src_ids, dst, dst_ids):
+    """Copies slot src[src_ids[i]] into dst[dst_ids[i]] for each i (dst updated in place);
+    None for an id list means 0..n-1. A pair with a negative id is skipped; a pair with an
+    id past its pool's end is skipped and counted. Returns the count."""
+    n = len(src_ids) if src_ids is not None else len(dst_ids)
+    si = np.arange(n) if src_ids is None else np.asarray(src_ids, dtype=np.int64).reshape(-1)
+    di = np.arange(n) if dst_ids is None else np.asarray(dst_ids, dtype=np.int64).reshape(-1)
+    bad = 0
+    for a, b in zip(si, di):
+        if a >= src.shape[0] or b >= dst.shape[0]:
+            bad += 1
+        elif a >= 0 and b >= 0:
+            dst[b] = src[a]
+    return bad

@@ -260,4 +260,60 @@ int kda_ref_decode(int B, int H, int dk, int dv, double scale, const double* q,
   return bad.load();
 }
 
+// A verify window of W tokens per batch row, with a state fork: for row b and head h the
+// state is read from slot read_slots[b] and, after each token j of the row's window, the
+// current state is stored into slot write_slots[b*W + j] (a per-column snapshot, so that a
+// caller that accepts only the first n tokens resumes from the snapshot of column n - 1).
+// This is the read/write state-index split of the ATOM Kimi-K3 pipeline-parallel pull request
+// ("spec_state_indices_in" read slots, verify windows, "resumes from column
+// num_accepted - 1"); the recurrence per token is exactly the one above.
+//   q, k, g: [B*W, H, dk]; v: [B*W, H, dv]; beta: [B*W, H] (token b*W + j is column j of row
+//   b); read_slots: [B]; write_slots: [B*W]; pool: [n_slots, H, dk, dv]; o: [B*W, H, dv].
+//   beta_is_logit != 0: beta holds logits and the write strength is 1 / (1 + exp(-beta)).
+// A row whose read slot is negative (padding) or >= n_slots is skipped: its outputs are zero
+// and nothing is stored. A negative write slot stores nothing for that column; one >= n_slots
+// is skipped and counted. Returns the number of out-of-range slot ids seen (each counted
+// once, on head 0), or -1 on bad arguments.
+int kda_ref_decode_window(int B, int W, int H, int dk, int dv, double scale, const double* q,
+                          const double* k, const double* v, const double* g,
+                          const double* beta, int beta_is_logit, const int64_t* read_slots,
+                          const int64_t* write_slots, double* pool, int64_t n_slots,
+                          double* o, int n_threads) {
+  if (B < 0 || W < 0 || H <= 0 || dk <= 0 || dv <= 0 || !read_slots || !write_slots || !pool ||
+      !o)
+    return -1;
+  // write strengths of every (token, head), from the logits where asked
+  const int64_t n_tok = (int64_t)B * W;
+  std::vector<double> bw((size_t)(n_tok * H));
+  for (int64_t i = 0; i < n_tok * H; ++i)
+    bw[i] = beta_is_logit ? 1.0 / (1.0 + std::exp(-beta[i])) : beta[i];
+  std::atomic<int> bad(0);
+  const int64_t sd = (int64_t)dk * dv;
+  parallel_items((int64_t)B * H, n_threads, [&](int64_t it) {
+    const int h = (int)(it % H);
+    const int b = (int)(it / H);
+    const int64_t r = read_slots[b];
+    if (r < 0 || r >= n_slots) {
+      if (r >= n_slots && h == 0) bad.fetch_add(1);
+      for (int j = 0; j < W; ++j)
+        for (int c = 0; c < dv; ++c) o[(((int64_t)b * W + j) * H + h) * dv + c] = 0.0;
+      return;
+    }
+    std::vector<double> S(pool + (r * H + h) * sd, pool + (r * H + h) * sd + sd);
+    auto vcol = [&](int t, int c) { return v[((int64_t)t * H + h) * dv + c]; };
+    for (int j = 0; j < W; ++j) {
+      const int t = b * W + j;
+      recur_block(t, t + 1, h, H, dk, 0, dv, scale, q, k, g, bw.data(), vcol, S.data(), o,
+                  H * dv, h * dv);
+      const int64_t w = write_slots[t];
+      if (w >= n_slots) {
+        if (h == 0) bad.fetch_add(1);
+      } else if (w >= 0) {
+        std::memcpy(pool + (w * H + h) * sd, S.data(), sd * sizeof(double));
+      }
+    }
+  });
+  return bad.load();
+}
+
 }  // extern "C"

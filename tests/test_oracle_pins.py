@@ -289,3 +289,152 @@ def test_varlen_packing(oracle_mod):
         np.testing.assert_array_equal(o[a:b], oi)
         np.testing.assert_array_equal(fin[s], fi[0])
     assert np.array_equal(fin[1], S0[1])  # empty sequence keeps its state
+
+
+# Verify windows with a state fork (read slot, one write slot per window column) and write
+# strengths given as logits. Pinned by exact rational arithmetic, by the closed forms that
+# the logit extremes reduce to, by the library sigmoid, and by the pinned sequential pass.
+def test_window_snapshots_exact_rational(oracle_mod):
+    """Each column's snapshot is the exact state after that many tokens."""
+    rng = np.random.default_rng(21)
+    W, dk, dv = 4, 3, 2
+    fr = lambda x: Fraction(int(x), 8)
+    q = [[fr(rng.integers(-8, 9)) for _ in range(dk)] for _ in range(W)]
+    k = [[fr(rng.integers(-8, 9)) for _ in range(dk)] for _ in range(W)]
+    v = [[fr(rng.integers(-8, 9)) for _ in range(dv)] for _ in range(W)]
+    a = [[Fraction(int(rng.integers(1, 9)), 8) for _ in range(dk)] for _ in range(W)]
+    beta = [Fraction(int(rng.integers(0, 9)), 8) for _ in range(W)]
+    S0 = [[fr(rng.integers(-8, 9)) for _ in range(dv)] for _ in range(dk)]
+    f = lambda m: np.array([[float(x) for x in r] for r in m])
+    pool = np.zeros((7, 1, dk, dv))
+    pool[5, 0] = f(S0)
+    write = np.array([[1, 6, 2, 0]])
+    o, bad = oracle_mod.decode_window(f(q)[:, None], f(k)[:, None], f(v)[:, None],
+                                      np.log(f(a))[:, None],
+                                      np.array([[float(b)] for b in beta]), [5], write, pool)
+    assert bad == 0
+    for j in range(W):
+        outs, S = _exact_matrix_form(q[:j + 1], k[:j + 1], v[:j + 1], a[:j + 1], beta[:j + 1],
+                                     S0)
+        np.testing.assert_allclose(pool[write[0, j], 0], f(S), rtol=1e-12, atol=1e-12)
+        np.testing.assert_allclose(o[j, 0], f(outs)[-1], rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(pool[5, 0], f(S0))  # the read slot is not a write slot
+
+
+def test_window_logit_extremes_closed_forms(oracle_mod):
+    """Logit -800 gives beta = 0 exactly (decay only: S_j = Diag(exp(sum g)) S_0); logit +800
+    gives beta = 1 exactly (unit keys read back what was written: S_j^T k_j = v_j); logit 0
+    gives beta = 1/2 exactly."""
+    rng = np.random.default_rng(22)
+    B, W, H, dk, dv = 2, 3, 2, 4, 5
+    q, k, v, g, _ = _rand_inputs(rng, B * W, H, dk, dv)
+    pool0 = rng.standard_normal((8, H, dk, dv))
+    read = np.array([3, 7])
+    write = np.array([[0, 1, 2], [4, 5, 6]])
+    # beta = 0: decay only
+    pool = pool0.copy()
+    o, _ = oracle_mod.decode_window(q, k, v, g, np.full((B * W, H), -800.0), read, write, pool,
+                                    scale=0.6, beta_is_logit=True)
+    for b in range(B):
+        gam = np.cumsum(g[b * W:(b + 1) * W], axis=0)
+        for j in range(W):
+            for h in range(H):
+                Sj = np.exp(gam[j, h])[:, None] * pool0[read[b], h]
+                np.testing.assert_allclose(pool[write[b, j], h], Sj, rtol=1e-12, atol=1e-14)
+                np.testing.assert_allclose(o[b * W + j, h], 0.6 * Sj.T @ q[b * W + j, h],
+                                           rtol=1e-12, atol=1e-13)
+    # beta = 1: the write invariant, reading with the key just written
+    pool = pool0.copy()
+    o, _ = oracle_mod.decode_window(k.copy(), k, v, g, np.full((B * W, H), 800.0), read, write,
+                                    pool, beta_is_logit=True)
+    np.testing.assert_allclose(o, v, rtol=0, atol=1e-12)
+    # beta = 1/2 from logit 0, bit for bit
+    p1, p2 = pool0.copy(), pool0.copy()
+    o1, _ = oracle_mod.decode_window(q, k, v, g, np.zeros((B * W, H)), read, write, p1,
+                                     beta_is_logit=True)
+    o2, _ = oracle_mod.decode_window(q, k, v, g, np.full((B * W, H), 0.5), read, write, p2)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(p1, p2)
+
+
+def test_window_logit_matches_library_sigmoid(oracle_mod):
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(23)
+    B, W, H, dk, dv = 3, 2, 2, 3, 4
+    q, k, v, g, _ = _rand_inputs(rng, B * W, H, dk, dv)
+    logit = rng.standard_normal((B * W, H)) * 4.0
+    pool0 = rng.standard_normal((9, H, dk, dv))
+    read, write = np.array([0, 1, 2]), np.array([[3, 4], [5, 6], [7, 8]])
+    p1, p2 = pool0.copy(), pool0.copy()
+    o1, _ = oracle_mod.decode_window(q, k, v, g, logit, read, write, p1, beta_is_logit=True)
+    o2, _ = oracle_mod.decode_window(q, k, v, g, special.expit(logit), read, write, p2)
+    np.testing.assert_allclose(o1, o2, rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(p1, p2, rtol=1e-13, atol=1e-14)
+
+
+def test_window_fork_rollback_and_slots(oracle_mod):
+    """Snapshots equal the sequential pass over the window's prefix; the read slot and every
+    slot not written stay bit-identical; negative write slots store nothing; padding rows
+    output zeros; out-of-range ids are counted; resuming from the snapshot of column n - 1
+    reproduces the rest of the window (rollback after accepting n tokens)."""
+    rng = np.random.default_rng(24)
+    B, W, H, dk, dv, n_slots = 4, 5, 2, 3, 4, 40
+    q, k, v, g, beta = _rand_inputs(rng, B * W, H, dk, dv)
+    pool0 = rng.standard_normal((n_slots, H, dk, dv))
+    read = np.array([2, -1, 11, 50])
+    write = np.array([[20, 21, -1, 22, 2],      # the last column stores into the read slot
+                      [30, 31, 32, 33, 34],      # padding row: nothing stored
+                      [23, 24, 25, 26, 99],      # one out-of-range write
+                      [35, 36, 37, 38, 39]])     # out-of-range read: row skipped
+    pool = pool0.copy()
+    o, bad = oracle_mod.decode_window(q, k, v, g, beta, read, write, pool, scale=0.9)
+    assert bad == 2
+    for b in (1, 3):
+        assert np.abs(o[b * W:(b + 1) * W]).max() == 0.0
+    stored = set()
+    for b in (0, 2):
+        sl = slice(b * W, (b + 1) * W)
+        ob, _ = oracle_mod.forward(q[sl], k[sl], v[sl], g[sl], beta[sl],
+                                   init_state=pool0[read[b]][None], scale=0.9)
+        np.testing.assert_array_equal(o[sl], ob)
+        for j in range(W):
+            s = write[b, j]
+            if 0 <= s < n_slots:
+                _, fj = oracle_mod.forward(q[b * W:b * W + j + 1], k[b * W:b * W + j + 1],
+                                           v[b * W:b * W + j + 1], g[b * W:b * W + j + 1],
+                                           beta[b * W:b * W + j + 1],
+                                           init_state=pool0[read[b]][None], scale=0.9)
+                np.testing.assert_array_equal(pool[s], fj[0])
+                stored.add(int(s))
+    for s in range(n_slots):
+        if s not in stored:
+            np.testing.assert_array_equal(pool[s], pool0[s])
+    # rollback: row 2 accepted n = 2 tokens; resume from column 1's snapshot (slot 24)
+    n = 2
+    sl = slice(2 * W + n, 3 * W)
+    p2 = pool.copy()
+    o2, _ = oracle_mod.decode_window(q[sl], k[sl], v[sl], g[sl], beta[sl], [24],
+                                     [[1, 3, 4]], p2, scale=0.9)
+    np.testing.assert_array_equal(o2, o[sl])
+    np.testing.assert_array_equal(p2[1], pool[25])
+    np.testing.assert_array_equal(p2[3], pool[26])
+
+
+def test_slot_zero_and_copy(oracle_mod):
+    rng = np.random.default_rng(25)
+    pool0 = rng.standard_normal((10, 2, 3, 4))
+    pool = pool0.copy()
+    assert oracle_mod.slot_zero(pool, [3, -1, 7, 12]) == 1
+    for s in range(10):
+        if s in (3, 7):
+            assert not pool[s].any()
+        else:
+            np.testing.assert_array_equal(pool[s], pool0[s])
+    image = np.zeros((3, 2, 3, 4))
+    assert oracle_mod.slot_copy(pool0, [4, 9, 0], image, None) == 0   # checkpoint image
+    np.testing.assert_array_equal(image, pool0[[4, 9, 0]])
+    pool = pool0.copy()
+    assert oracle_mod.slot_copy(image, None, pool, [1, -1, 15]) == 1  # restore, one skipped
+    np.testing.assert_array_equal(pool[1], pool0[4])
+    np.testing.assert_array_equal(pool[[0] + list(range(2, 10))],
+                                  pool0[[0] + list(range(2, 10))])
