@@ -251,6 +251,68 @@ def run_gb300(args):
                 "traffic": TRAFFIC_PREFILL_16K, "kernel": "prefill_16k (chunk_fused_kernel)",
                 "peak_source": peaks["source"]}
 
+    # The slot-table extensions of the decode path, timed on their own after the step (each
+    # over its own CUDA events, the same number of iterations): a 4-token verify window per
+    # row with forked read slots and logit write strengths, a checkpoint image of the decode
+    # rows' 256 slots (and its restore), and zeroing 256 slots.
+    win = inputs.make_workload("window_256x4", device=dev)
+    Bw, Ww = win.write_slots.shape
+    ow = torch.empty_like(win.v)
+    image = torch.empty(B, H, D, D, device=dev)
+    named = torch.zeros(win.pool.shape[0], dtype=torch.bool, device=dev)
+    named[win.read_slots.long()] = True
+    named[win.write_slots.long().reshape(-1)] = True
+    free_slots = torch.nonzero(~named).reshape(-1)[:B].to(torch.int32).contiguous()
+
+    def window():
+        kda.decode_window(win.q, win.k, win.v, win.g, win.beta_logit, win.read_slots,
+                          win.write_slots, win.pool, beta_is_logit=True, o=ow)
+
+    def checkpoint():
+        kda.slot_copy(dec.pool, dec.slot_ids, image, None)
+
+    def restore():
+        kda.slot_copy(image, None, dec.pool, dec.slot_ids)
+
+    def zero():
+        kda.slot_zero(win.pool, free_slots)
+
+    ext_parts = [("window_256x4", window), ("slot_checkpoint_256", checkpoint),
+                 ("slot_restore_256", restore), ("slot_zero_256", zero)]
+    for _ in range(args.warmup):
+        for _, fn in ext_parts:
+            fn()
+    torch.cuda.synchronize()
+    ext_ev = {n: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(args.steps)] for n, _ in ext_parts}
+    torch.cuda._sleep(int(4e7))
+    for i in range(args.steps):
+        for n, fn in ext_parts:
+            ext_ev[n][i][0].record(stream)
+            fn()
+            ext_ev[n][i][1].record(stream)
+    torch.cuda.synchronize()
+    ext_ms = {n: sum(a.elapsed_time(b) for a, b in ext_ev[n]) / args.steps for n, _ in ext_parts}
+    red = max_over_ranks([ext_ms[n] for n, _ in ext_parts])
+    for i, (n, _) in enumerate(ext_parts):
+        ext_ms[n] = red[i]
+    slot_bytes = H * STATE_BYTES
+    ext_bytes = {
+        "window_256x4": (Bw * H * (STATE_BYTES + Ww * STATE_BYTES)
+                         + Bw * Ww * H * (3 * D * 2 + D * 4 + 4 + D * 2) + Bw * (Ww + 1) * 4),
+        "slot_checkpoint_256": 2 * B * slot_bytes + B * 4,
+        "slot_restore_256": 2 * B * slot_bytes + B * 4,
+        "slot_zero_256": B * slot_bytes + B * 4,
+    }
+    extensions = {}
+    for n, _ in ext_parts:
+        gbs = ext_bytes[n] / (ext_ms[n] * 1e-3) / 1e9
+        extensions[n] = {"ms": round(ext_ms[n], 4), "algorithmic_bytes": ext_bytes[n],
+                         "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)}
+    extensions["window_256x4"]["tokens_per_s"] = round(Bw * Ww / (ext_ms["window_256x4"] * 1e-3),
+                                                       1)
+    del win
+
     # end to end through the public API with host buffers: every step copies its inputs in from
     # pinned host memory, runs kda_chunk_prefill and copies o and the final state back out.
     # Steps are pipelined over three streams (copy-in, compute, copy-out) with two buffer sets,
@@ -326,6 +388,7 @@ def run_gb300(args):
         "components": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
                            for kk, vv in v.items()} for k, v in comps.items()},
         "roofline": roofline,
+        "extensions": extensions,
         "e2e": {"value": round(weak_scaling_value(T, world, e2e_ms), 1), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "what": "kda_chunk_prefill with pinned host inputs copied in and o/final state "
@@ -391,7 +454,8 @@ def run_reference(args):
 
 def run_profile_case(args):
     """A small case of one call (inputs still larger than L2, a few GB on the device at most)
-    for ncu captures: `--profile-case prefill|package|replay|scan|decode`, `--launches N`."""
+    for ncu captures: `--profile-case prefill|package|replay|scan|decode|window|slots`,
+    `--launches N`."""
     import torch
     from linear_attention_state_kda_gb300 import inputs, kda
     dev = torch.device("cuda", 0)
@@ -400,6 +464,14 @@ def run_profile_case(args):
     if case == "decode":
         d = inputs.make_decode(256, 32, D, D, 1024, seed=1004, device=dev)
         fns = [lambda: kda.decode_step(d.q, d.k, d.v, d.g, d.beta, d.slot_ids, d.pool)]
+    elif case == "window":
+        w = inputs.make_window(128, 4, 32, D, D, 640, seed=1005, device=dev)
+        fns = [lambda: kda.decode_window(w.q, w.k, w.v, w.g, w.beta_logit, w.read_slots,
+                                         w.write_slots, w.pool, beta_is_logit=True)]
+    elif case == "slots":
+        d = inputs.make_decode(256, 32, D, D, 1024, seed=1004, device=dev)
+        image = torch.empty(256, 32, D, D, device=dev)
+        fns = [lambda: kda.slot_copy(d.pool, d.slot_ids, image, None)]
     else:
         x = inputs.make_prefill([4096], 32, D, D, "bf16", seed=1001, device=dev)
         offs = torch.tensor([0, 2048, 4096], dtype=torch.int32, device=dev)
@@ -428,7 +500,8 @@ def run_profile_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile-case", default=None,
-                    choices=["prefill", "package", "scan", "replay", "decode"])
+                    choices=["prefill", "package", "scan", "replay", "decode", "window",
+                             "slots"])
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)

@@ -256,6 +256,69 @@ KDA_API kda_status kda_decode_step(kda_dtype dt, int batch, int H, int dk, int d
                            const float* beta, const int32_t* slot_ids, float* state_pool,
                            int64_t n_slots, void* o, uint32_t* status, kda_stream_t stream);
 
+/* Bits of the `flags` argument of kda_decode_window. */
+#define KDA_DECODE_BETA_LOGIT 1u /* beta holds logits; the write strength is 1/(1+exp(-beta)) */
+
+/*
+ * kda_decode_window: a verify window of `window` tokens per batch row with a state fork.
+ * Row b reads its state from slot read_slots[b] (the read-side index: a forked sequence is
+ * read from its source slot, nothing is copied onto the write slot first), runs the window's
+ * tokens in order (token j of row b is row b*window + j of the token arrays) and, after token
+ * j, stores the current state into slot write_slots[b*window + j]: one snapshot per window
+ * column, so that a caller that accepts the first n tokens continues from the slot of column
+ * n - 1 (and one that accepts all simply keeps the last). o[b*window + j] = scale * S_j^T q.
+ *   q, k, g [batch*window, H, dk]; v, o [batch*window, H, dv]; beta [batch*window, H] (the
+ *   write strength, or its logit when flags has KDA_DECODE_BETA_LOGIT).
+ *   read_slots  device int32 [batch]. Negative: a padding row (skipped, its window's o rows
+ *               written as zeros, nothing stored). >= n_slots: skipped the same way, and
+ *               KDA_STATUS_BAD_SLOT is set in *status.
+ *   write_slots device int32 [batch, window]. Negative: that column stores nothing.
+ *               >= n_slots: that store is skipped and KDA_STATUS_BAD_SLOT is set. A write
+ *               slot may equal the row's own read slot (the whole window reads the state
+ *               before the first store). The slots named by different rows must be disjoint
+ *               (a slot read by one row and written by another races).
+ *   state_pool  [n_slots, H, dk, dv] fp32 (16-byte aligned).
+ *   window      1 .. 16 (0 is a no-op). window = 1 with write_slots = read_slots is
+ *               kda_decode_step with the option of logit write strengths.
+ * Source: ATOM PR #2709 ("feat(kimi-k3): PP8 prefill for P/D serving - KDA state under PP"),
+ * the commits on reading a forked state through a read-side index and on resuming a verify
+ * window from its last accepted column, and the sigmoid-gated delta-rule update they name.
+ */
+KDA_API kda_status kda_decode_window(kda_dtype dt, int batch, int window, int H, int dk, int dv,
+                                     float scale, const void* q, const void* k, const void* v,
+                                     const float* g, const float* beta, unsigned flags,
+                                     const int32_t* read_slots, const int32_t* write_slots,
+                                     float* state_pool, int64_t n_slots, void* o,
+                                     uint32_t* status, kda_stream_t stream);
+
+/*
+ * kda_slot_zero: sets every listed slot of a state pool [n_slots, slot_elems] fp32 to zero.
+ *   slot_ids device int32 [n], or NULL for slots 0 .. n-1. Negative ids are skipped; ids
+ *            >= n_slots are skipped and set KDA_STATUS_BAD_SLOT.
+ *   slot_elems elements per slot (H * dk * dv for a KDA pool), a multiple of 4; the pool
+ *            16-byte aligned.
+ * Source: kern PR #44 (Runtime::zero_slot: the state slot a new sequence is given starts at
+ * zero).
+ */
+KDA_API kda_status kda_slot_zero(int n, const int32_t* slot_ids, float* state_pool,
+                                 int64_t n_slots, int64_t slot_elems, uint32_t* status,
+                                 kda_stream_t stream);
+
+/*
+ * kda_slot_copy: for i in [0, n) copies slot src[src_ids[i]] into slot dst[dst_ids[i]], where
+ * src is [n_src, slot_elems] and dst [n_dst, slot_elems] fp32 (the same pool or two; NULL id
+ * arrays mean 0 .. n-1). Taking a checkpoint image of some slots is a copy into a compact
+ * buffer (dst_ids NULL); restoring it is the copy back (src_ids NULL). A pair with an id past
+ * its pool's end is skipped and sets KDA_STATUS_BAD_SLOT; otherwise a pair with a negative id
+ * is skipped. No slot may be both a source and a destination of one call.
+ *   slot_elems a multiple of 4; both pools 16-byte aligned.
+ * Source: ATOM PR #2709, PAGE-backed KDA state checkpoints (an image is a copy of a
+ * sequence's state, made in stream order).
+ */
+KDA_API kda_status kda_slot_copy(int n, const float* src, const int32_t* src_ids, int64_t n_src,
+                                 float* dst, const int32_t* dst_ids, int64_t n_dst,
+                                 int64_t slot_elems, uint32_t* status, kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

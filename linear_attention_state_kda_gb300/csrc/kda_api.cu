@@ -306,4 +306,66 @@ kda_status kda_decode_step(kda_dtype dt, int batch, int H, int dk, int dv, float
                        n_slots, o, status, (cudaStream_t)stream);
 }
 
+kda_status kda_decode_window(kda_dtype dt, int batch, int window, int H, int dk, int dv,
+                             float scale, const void* q, const void* k, const void* v,
+                             const float* g, const float* beta, unsigned flags,
+                             const int32_t* read_slots, const int32_t* write_slots,
+                             float* state_pool, int64_t n_slots, void* o, uint32_t* status,
+                             kda_stream_t stream) {
+  const char* fn = "kda_decode_window";
+  kda_status st = check_shape(fn, dt, H, dk, dv, kChunk);
+  if (st != KDA_OK) return st;
+  KDA_REQUIRE(batch >= 0, KDA_ERR_INVALID_ARG, "kda_decode_window: batch must be >= 0");
+  KDA_REQUIRE(window >= 0 && window <= kMaxWindow, KDA_ERR_UNSUPPORTED,
+              "kda_decode_window: window must be in 0 .. 16");
+  KDA_REQUIRE(n_slots > 0, KDA_ERR_INVALID_ARG, "kda_decode_window: n_slots must be > 0");
+  KDA_REQUIRE((flags & ~KDA_DECODE_BETA_LOGIT) == 0, KDA_ERR_INVALID_ARG,
+              "kda_decode_window: unknown flag bits");
+  if (batch == 0 || window == 0) return KDA_OK;
+  KDA_REQUIRE(q && k && v && g && beta && read_slots && write_slots && state_pool && o,
+              KDA_ERR_INVALID_ARG, "kda_decode_window: pointers must be non-null");
+  KDA_REQUIRE((int64_t)batch * H <= 0x7fffffffLL && (int64_t)batch * window * H <= 0x7fffffffLL,
+              KDA_ERR_INVALID_ARG, "kda_decode_window: batch * window * H too large");
+  KDA_REQUIRE(aligned(state_pool, 16) && aligned(q, 4) && aligned(k, 4) && aligned(v, 4) &&
+                  aligned(o, 4) && aligned(g, 4) && aligned(beta, 4) && aligned(read_slots, 4) &&
+                  aligned(write_slots, 4) && aligned(status, 4),
+              KDA_ERR_INVALID_ARG, "kda_decode_window: misaligned pointer");
+  return launch_decode_window(dt, batch, window, H, dk, dv, scale, q, k, v, g, beta, flags,
+                              read_slots, write_slots, state_pool, n_slots, o, status,
+                              (cudaStream_t)stream);
+}
+
+kda_status kda_slot_zero(int n, const int32_t* slot_ids, float* state_pool, int64_t n_slots,
+                         int64_t slot_elems, uint32_t* status, kda_stream_t stream) {
+  KDA_REQUIRE(n >= 0 && n_slots > 0 && slot_elems >= 0, KDA_ERR_INVALID_ARG,
+              "kda_slot_zero: n >= 0, n_slots > 0 and slot_elems >= 0 required");
+  KDA_REQUIRE(slot_elems % 4 == 0, KDA_ERR_INVALID_ARG,
+              "kda_slot_zero: slot_elems must be a multiple of 4");
+  if (n == 0 || slot_elems == 0) return KDA_OK;
+  KDA_REQUIRE(state_pool && aligned(state_pool, 16) && aligned(slot_ids, 4) &&
+                  aligned(status, 4),
+              KDA_ERR_INVALID_ARG, "kda_slot_zero: pool must be non-null and 16-byte aligned");
+  KDA_REQUIRE(slot_ids || n <= n_slots, KDA_ERR_INVALID_ARG,
+              "kda_slot_zero: without slot ids, n must not exceed n_slots");
+  return launch_slots(true, n, nullptr, nullptr, 0, state_pool, slot_ids, n_slots, slot_elems,
+                      status, (cudaStream_t)stream);
+}
+
+kda_status kda_slot_copy(int n, const float* src, const int32_t* src_ids, int64_t n_src,
+                         float* dst, const int32_t* dst_ids, int64_t n_dst, int64_t slot_elems,
+                         uint32_t* status, kda_stream_t stream) {
+  KDA_REQUIRE(n >= 0 && n_src > 0 && n_dst > 0 && slot_elems >= 0, KDA_ERR_INVALID_ARG,
+              "kda_slot_copy: n >= 0, n_src > 0, n_dst > 0 and slot_elems >= 0 required");
+  KDA_REQUIRE(slot_elems % 4 == 0, KDA_ERR_INVALID_ARG,
+              "kda_slot_copy: slot_elems must be a multiple of 4");
+  if (n == 0 || slot_elems == 0) return KDA_OK;
+  KDA_REQUIRE(src && dst && aligned(src, 16) && aligned(dst, 16) && aligned(src_ids, 4) &&
+                  aligned(dst_ids, 4) && aligned(status, 4),
+              KDA_ERR_INVALID_ARG, "kda_slot_copy: pools must be non-null and 16-byte aligned");
+  KDA_REQUIRE((src_ids || n <= n_src) && (dst_ids || n <= n_dst), KDA_ERR_INVALID_ARG,
+              "kda_slot_copy: without ids, n must not exceed that pool's slot count");
+  return launch_slots(false, n, src, src_ids, n_src, dst, dst_ids, n_dst, slot_elems, status,
+                      (cudaStream_t)stream);
+}
+
 }  // extern "C"

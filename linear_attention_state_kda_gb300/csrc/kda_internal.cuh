@@ -77,6 +77,20 @@ kda_status launch_decode(kda_dtype dt, int batch, int H, int dk, int dv, float s
                          const float* beta, const int32_t* slot_ids, float* pool,
                          int64_t n_slots, void* o, uint32_t* status, cudaStream_t s);
 
+// Verify window with a state fork (read slot, one write slot per window column).
+constexpr int kMaxWindow = 16;
+kda_status launch_decode_window(kda_dtype dt, int batch, int window, int H, int dk, int dv,
+                                float scale, const void* q, const void* k, const void* v,
+                                const float* g, const float* beta, unsigned flags,
+                                const int32_t* read_slots, const int32_t* write_slots,
+                                float* pool, int64_t n_slots, void* o, uint32_t* status,
+                                cudaStream_t s);
+
+// Whole-slot zero (zero = true; src unused) or copy src[src_ids[i]] -> dst[dst_ids[i]].
+kda_status launch_slots(bool zero, int n, const float* src, const int32_t* src_ids, int64_t n_src,
+                        float* dst, const int32_t* dst_ids, int64_t n_dst, int64_t slot_elems,
+                        uint32_t* status, cudaStream_t s);
+
 // Package scan.
 size_t scan_workspace_bytes(int n_seqs, int max_segs, int H, int dk, int dv);
 kda_status launch_scan(int n_seqs, int n_segs, const int32_t* seq_seg_offsets, int max_segs,

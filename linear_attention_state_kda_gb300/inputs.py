@@ -69,10 +69,23 @@ class DecodeInputs:
     slot_ids: torch.Tensor   # [B] int32
 
 
+@dataclass
+class WindowInputs:
+    q: torch.Tensor            # [B*W, H, dk] (token j of row b is row b*W + j)
+    k: torch.Tensor            # [B*W, H, dk]
+    v: torch.Tensor            # [B*W, H, dv]
+    g: torch.Tensor            # [B*W, H, dk] fp32
+    beta: torch.Tensor         # [B*W, H] fp32 in (0, 1)
+    beta_logit: torch.Tensor   # [B*W, H] fp32, the N(0, 1) draw that beta is the sigmoid of
+    pool: torch.Tensor         # [n_slots, H, dk, dv] fp32
+    read_slots: torch.Tensor   # [B] int32
+    write_slots: torch.Tensor  # [B, W] int32, disjoint from each other and from read_slots
+
+
 _DT = {"bf16": torch.bfloat16, "f32": torch.float32}
 
 
-def _draw_qkvgb(gen, n, H, dk, dv, device, decay_scale, beta_scale=1.0):
+def _draw_qkvgb(gen, n, H, dk, dv, device, decay_scale, beta_scale=1.0, want_logit=False):
     q = torch.randn(n, H, dk, generator=gen, device=device)
     k = torch.randn(n, H, dk, generator=gen, device=device)
     k = k / k.norm(dim=-1, keepdim=True)
@@ -80,9 +93,12 @@ def _draw_qkvgb(gen, n, H, dk, dv, device, decay_scale, beta_scale=1.0):
     g = -F.softplus(torch.randn(n, H, dk, generator=gen, device=device))
     if decay_scale != 1.0:
         g = g * decay_scale
-    beta = torch.sigmoid(torch.randn(n, H, generator=gen, device=device))
+    logit = torch.randn(n, H, generator=gen, device=device)
+    beta = torch.sigmoid(logit)
     if beta_scale != 1.0:
         beta = beta * beta_scale
+    if want_logit:
+        return q, k, v, g, beta, logit
     return q, k, v, g, beta
 
 
@@ -116,6 +132,26 @@ def make_decode(B, H, dk, dv, n_slots, dtype="bf16", seed=0, device="cpu", pool_
     return DecodeInputs(q=q.to(dt).contiguous(), k=k.to(dt).contiguous(),
                         v=v.to(dt).contiguous(), g=g.contiguous(), beta=beta.contiguous(),
                         pool=pool.contiguous(), slot_ids=slots.contiguous())
+
+
+def make_window(B, W, H, dk, dv, n_slots, dtype="bf16", seed=0, device="cpu", pool_std=0.02,
+                decay_scale=1.0) -> WindowInputs:
+    """Verify windows: B rows of W tokens each, a pool of n_slots states, and B read slots
+    plus B x W write slots sampled without replacement (so every slot is named once)."""
+    if B * (W + 1) > n_slots:
+        raise ValueError("the pool is too small for distinct read and write slots")
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    q, k, v, g, beta, logit = _draw_qkvgb(gen, B * W, H, dk, dv, device, decay_scale,
+                                          want_logit=True)
+    pool = torch.randn(n_slots, H, dk, dv, generator=gen, device=device) * pool_std
+    perm = torch.randperm(n_slots, generator=gen, device=device)[:B * (W + 1)].to(torch.int32)
+    dt = _DT[dtype]
+    return WindowInputs(q=q.to(dt).contiguous(), k=k.to(dt).contiguous(),
+                        v=v.to(dt).contiguous(), g=g.contiguous(), beta=beta.contiguous(),
+                        beta_logit=logit.contiguous(), pool=pool.contiguous(),
+                        read_slots=perm[:B].contiguous(),
+                        write_slots=perm[B:].reshape(B, W).contiguous())
 
 
 def leveled_split(length, n_segs, q=LEVEL_Q, align=64):
@@ -195,6 +231,10 @@ WORKLOADS = {
     # decode: 256 sequences x H32 x d128 over a 4096-slot fp32 pool (~8.6 GB).
     "decode_256": dict(kind="decode", B=256, H=32, dk=128, dv=128, n_slots=4096, dtype="bf16",
                        seed=1004, pool_std=0.02),
+    # verify windows: 256 rows of 4 tokens (3 drafts + 1 bonus) x H32 x d128 over a 4096-slot
+    # pool, each row reading one slot and storing a snapshot per token into 4 others.
+    "window_256x4": dict(kind="window", B=256, W=4, H=32, dk=128, dv=128, n_slots=4096,
+                         dtype="bf16", seed=1005, pool_std=0.02),
 }
 
 
@@ -211,6 +251,9 @@ def workload_segments(name):
 def make_workload(name, device="cpu", decay_scale=1.0, beta_scale=1.0, **over):
     w = dict(WORKLOADS[name])
     w.update(over)
+    if w["kind"] == "window":
+        return make_window(w["B"], w["W"], w["H"], w["dk"], w["dv"], w["n_slots"], w["dtype"],
+                           w["seed"], device, w.get("pool_std", 0.02), decay_scale)
     if w["kind"] == "decode":
         return make_decode(w["B"], w["H"], w["dk"], w["dv"], w["n_slots"], w["dtype"],
                            w["seed"], device, w.get("pool_std", 0.02), decay_scale)

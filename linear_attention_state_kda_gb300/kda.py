@@ -15,6 +15,8 @@ LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA = range(5)
 KDA_F32, KDA_BF16 = 0, 1
+DECODE_BETA_LOGIT = 1
+MAX_WINDOW = 16
 STATUS_BAD_SLOT, STATUS_DECAY_RANGE, STATUS_BAD_OFFSETS = 1, 2, 4
 
 _lib = None
@@ -67,6 +69,13 @@ def lib():
     L.kda_segment_replay_prepared.argtypes = [I, I, I, P, I, I, I, I, P, P, P, P, Z, P, P]
     L.kda_decode_step.restype = I
     L.kda_decode_step.argtypes = [I, I, I, I, I, F, P, P, P, P, P, P, P, I64, P, P, P]
+    L.kda_decode_window.restype = I
+    L.kda_decode_window.argtypes = [I, I, I, I, I, I, F, P, P, P, P, P, ctypes.c_uint, P, P, P,
+                                    I64, P, P, P]
+    L.kda_slot_zero.restype = I
+    L.kda_slot_zero.argtypes = [I, P, P, I64, I64, P, P]
+    L.kda_slot_copy.restype = I
+    L.kda_slot_copy.argtypes = [I, P, P, I64, P, P, I64, I64, P, P]
     _lib = L
     return L
 
@@ -111,6 +120,12 @@ def _contig(*ts):
     for t in ts:
         if t is not None and not t.is_contiguous():
             raise ValueError("tensors must be contiguous")
+
+
+def _int32(*ts):
+    for t in ts:
+        if t is not None and t.dtype != torch.int32:
+            raise TypeError("slot ids must be int32 tensors")
 
 
 def chunk_workspace(dtype, n_ranges, total_tokens, H, dk, dv):
@@ -295,3 +310,58 @@ def decode_step(q, k, v, g, beta, slot_ids, state_pool, scale=1.0, o=None, statu
                                  int(state_pool.shape[0]), _ptr(o), _ptr(status),
                                  _stream(stream)))
     return o
+
+
+def decode_window(q, k, v, g, beta, read_slots, write_slots, state_pool, scale=1.0,
+                  beta_is_logit=False, o=None, status=None, stream=None):
+    """kda_decode_window: rows of `window` tokens (write_slots is [batch, window]; q, k, g are
+    [batch*window, H, dk] or [batch, window, H, dk], likewise v and beta). Row b reads slot
+    read_slots[b] and stores its state after token j into slot write_slots[b, j]. Returns o,
+    shaped like v."""
+    _contig(q, k, v, g, beta, read_slots, write_slots, state_pool, o)
+    _int32(read_slots, write_slots)
+    B = read_slots.numel()
+    W = write_slots.numel() // B if B else 0
+    if write_slots.numel() != B * W:
+        raise ValueError("write_slots must hold batch x window ids")
+    H, dk = k.shape[-2], k.shape[-1]
+    dv = v.shape[-1]
+    if k.numel() != B * W * H * dk:
+        raise ValueError("k must hold batch x window tokens")
+    if o is None:
+        o = torch.empty(v.shape, dtype=q.dtype, device=q.device)
+    _check(lib().kda_decode_window(_dt(q), B, W, H, dk, dv, float(scale), _ptr(q), _ptr(k),
+                                   _ptr(v), _ptr(g), _ptr(beta),
+                                   DECODE_BETA_LOGIT if beta_is_logit else 0, _ptr(read_slots),
+                                   _ptr(write_slots), _ptr(state_pool),
+                                   int(state_pool.shape[0]), _ptr(o), _ptr(status),
+                                   _stream(stream)))
+    return o
+
+
+def slot_zero(state_pool, slot_ids=None, n=None, status=None, stream=None):
+    """kda_slot_zero: zero the listed slots of state_pool (all of slots 0..n-1 when slot_ids
+    is None)."""
+    _contig(state_pool, slot_ids)
+    _int32(slot_ids)
+    if n is None:
+        n = slot_ids.numel() if slot_ids is not None else state_pool.shape[0]
+    _check(lib().kda_slot_zero(int(n), _ptr(slot_ids), _ptr(state_pool),
+                               int(state_pool.shape[0]), int(state_pool[0].numel()),
+                               _ptr(status), _stream(stream)))
+    return state_pool
+
+
+def slot_copy(src, src_ids, dst, dst_ids, n=None, status=None, stream=None):
+    """kda_slot_copy: dst[dst_ids[i]] = src[src_ids[i]] (None ids mean 0..n-1)."""
+    _contig(src, src_ids, dst, dst_ids)
+    _int32(src_ids, dst_ids)
+    if src[0].numel() != dst[0].numel():
+        raise ValueError("src and dst slots differ in size")
+    if n is None:
+        n = src_ids.numel() if src_ids is not None else dst_ids.numel()
+    _check(lib().kda_slot_copy(int(n), _ptr(src), _ptr(src_ids), int(src.shape[0]), _ptr(dst),
+                               _ptr(dst_ids), int(dst.shape[0]), int(src[0].numel()),
+                               _ptr(status), _stream(stream)))
+    return dst
+

@@ -264,9 +264,10 @@ int kda_ref_decode(int B, int H, int dk, int dv, double scale, const double* q,
 // state is read from slot read_slots[b] and, after each token j of the row's window, the
 // current state is stored into slot write_slots[b*W + j] (a per-column snapshot, so that a
 // caller that accepts only the first n tokens resumes from the snapshot of column n - 1).
-// This is the read/write state-index split of the ATOM Kimi-K3 pipeline-parallel pull request
-// ("spec_state_indices_in" read slots, verify windows, "resumes from column
-// num_accepted - 1"); the recurrence per token is exactly the one above.
+// This is the read/write state-index split of ATOM PR #2709 ("feat(kimi-k3): PP8 prefill for
+// P/D serving - KDA state under PP"): a forked state is read through a read-side slot index,
+// and a verify window keeps one state column per position, the next step starting from the
+// last accepted one. The recurrence per token is exactly the one above.
 //   q, k, g: [B*W, H, dk]; v: [B*W, H, dv]; beta: [B*W, H] (token b*W + j is column j of row
 //   b); read_slots: [B]; write_slots: [B*W]; pool: [n_slots, H, dk, dv]; o: [B*W, H, dv].
 //   beta_is_logit != 0: beta holds logits and the write strength is 1 / (1 + exp(-beta)).

@@ -130,3 +130,34 @@ def test_decode_checks(L):
                              None) == kda.KDA_ERR_UNSUPPORTED
     assert L.kda_decode_step(1, 0, 2, 128, 128, 1.0, p, p, p, p, p, p, p, 10, p, None,
                              None) == kda.KDA_OK
+
+
+def test_window_checks(L):
+    from linear_attention_state_kda_gb300 import kda
+    p = 4096
+    win = lambda batch=4, window=4, dk=128, flags=0, n_slots=10, pool=p, ws=p: \
+        L.kda_decode_window(1, batch, window, 2, dk, dk, 1.0, p, p, p, p, p, flags, p, ws, pool,
+                            n_slots, p, None, None)
+    assert win(window=kda.MAX_WINDOW + 1) == kda.KDA_ERR_UNSUPPORTED
+    assert "window" in kda.last_error()
+    assert win(dk=96) == kda.KDA_ERR_UNSUPPORTED
+    assert win(flags=2) == kda.KDA_ERR_INVALID_ARG
+    assert win(n_slots=0) == kda.KDA_ERR_INVALID_ARG
+    assert win(pool=p + 8) == kda.KDA_ERR_INVALID_ARG       # the pool must be 16-byte aligned
+    assert win(ws=None) == kda.KDA_ERR_INVALID_ARG
+    assert win(batch=-1) == kda.KDA_ERR_INVALID_ARG
+    assert win(batch=0) == kda.KDA_OK                      # nothing to do launches nothing
+    assert win(window=0) == kda.KDA_OK
+
+
+def test_slot_checks(L):
+    from linear_attention_state_kda_gb300 import kda
+    p = 4096
+    assert L.kda_slot_zero(4, p, p, 10, 6, None, None) == kda.KDA_ERR_INVALID_ARG  # 6 % 4
+    assert L.kda_slot_zero(4, p, p + 4, 10, 8, None, None) == kda.KDA_ERR_INVALID_ARG
+    assert L.kda_slot_zero(11, None, p, 10, 8, None, None) == kda.KDA_ERR_INVALID_ARG
+    assert L.kda_slot_zero(0, p, p, 10, 8, None, None) == kda.KDA_OK
+    assert L.kda_slot_copy(4, p, p, 10, None, p, 10, 8, None, None) == kda.KDA_ERR_INVALID_ARG
+    assert L.kda_slot_copy(5, p, None, 4, p, p, 10, 8, None, None) == kda.KDA_ERR_INVALID_ARG
+    assert L.kda_slot_copy(4, p, p, 0, p, p, 10, 8, None, None) == kda.KDA_ERR_INVALID_ARG
+    assert L.kda_slot_copy(0, p, p, 10, p, p, 10, 8, None, None) == kda.KDA_OK
