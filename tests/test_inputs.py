@@ -22,6 +22,18 @@ def test_decode_slots_unique():
     assert len(set(s)) == len(s) and min(s) >= 0 and max(s) < 500
 
 
+def test_window_slots_disjoint_and_logits():
+    w = inputs.make_window(16, 4, 2, 16, 16, 100, seed=3)
+    r, ws = w.read_slots.tolist(), w.write_slots.reshape(-1).tolist()
+    assert w.write_slots.shape == (16, 4) and w.q.shape == (64, 2, 16)
+    assert len(set(r + ws)) == len(r) + len(ws)
+    assert min(r + ws) >= 0 and max(r + ws) < 100
+    assert torch.equal(w.beta, torch.sigmoid(w.beta_logit))
+    # the q, k, v, g, beta draws come first, in the same order as the other workloads
+    p = inputs.make_prefill([64], 2, 16, 16, "bf16", seed=3)
+    assert torch.equal(w.q, p.q) and torch.equal(w.g, p.g) and torch.equal(w.beta, p.beta)
+
+
 def test_leveled_split_rule():
     for length, n in [(131072, 16), (65536, 16), (32768, 8), (8192, 4)]:
         segs = inputs.gang_split(length)
