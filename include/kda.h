@@ -248,6 +248,7 @@ KDA_API kda_status kda_segment_replay_prepared(kda_dtype dt, int n_segs, int tot
  *              its o row is written as zeros. An id >= n_slots is skipped the same way and
  *              sets KDA_STATUS_BAD_SLOT in *status. Two rows naming the same slot race.
  *   state_pool [n_slots, H, dk, dv] fp32, read and written in place (16-byte aligned).
+ *   batch * H at most 2^30.
  * Source: ATOM PR #2709 (slot-indexed KDA state for decode; read/write state indices) and
  * kern PR #44 (recurrent-state slots per sequence).
  */
@@ -279,7 +280,8 @@ KDA_API kda_status kda_decode_step(kda_dtype dt, int batch, int H, int dk, int d
  *               (a slot read by one row and written by another races).
  *   state_pool  [n_slots, H, dk, dv] fp32 (16-byte aligned).
  *   window      1 .. 16 (0 is a no-op). window = 1 with write_slots = read_slots is
- *               kda_decode_step with the option of logit write strengths.
+ *               kda_decode_step with the option of logit write strengths. batch * window * H
+ *               at most 2^30.
  * Source: ATOM PR #2709 ("feat(kimi-k3): PP8 prefill for P/D serving - KDA state under PP"),
  * the commits on reading a forked state through a read-side index and on resuming a verify
  * window from its last accepted column, and the sigmoid-gated delta-rule update they name.

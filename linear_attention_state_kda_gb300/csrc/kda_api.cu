@@ -296,8 +296,8 @@ kda_status kda_decode_step(kda_dtype dt, int batch, int H, int dk, int dv, float
   if (batch == 0) return KDA_OK;
   KDA_REQUIRE(q && k && v && g && beta && slot_ids && state_pool && o, KDA_ERR_INVALID_ARG,
               "kda_decode_step: pointers must be non-null");
-  KDA_REQUIRE((int64_t)batch * H <= 0x7fffffffLL, KDA_ERR_INVALID_ARG,
-              "kda_decode_step: batch * H too large");
+  KDA_REQUIRE((int64_t)batch * H <= (1LL << 30), KDA_ERR_INVALID_ARG,
+              "kda_decode_step: batch * H must not exceed 2^30");
   KDA_REQUIRE(aligned(state_pool, 16) && aligned(q, 4) && aligned(k, 4) && aligned(v, 4) &&
                   aligned(o, 4) && aligned(g, 4) && aligned(beta, 4) && aligned(slot_ids, 4) &&
                   aligned(status, 4),
@@ -324,8 +324,8 @@ kda_status kda_decode_window(kda_dtype dt, int batch, int window, int H, int dk,
   if (batch == 0 || window == 0) return KDA_OK;
   KDA_REQUIRE(q && k && v && g && beta && read_slots && write_slots && state_pool && o,
               KDA_ERR_INVALID_ARG, "kda_decode_window: pointers must be non-null");
-  KDA_REQUIRE((int64_t)batch * H <= 0x7fffffffLL && (int64_t)batch * window * H <= 0x7fffffffLL,
-              KDA_ERR_INVALID_ARG, "kda_decode_window: batch * window * H too large");
+  KDA_REQUIRE((int64_t)batch * window * H <= (1LL << 30), KDA_ERR_INVALID_ARG,
+              "kda_decode_window: batch * window * H must not exceed 2^30");
   KDA_REQUIRE(aligned(state_pool, 16) && aligned(q, 4) && aligned(k, 4) && aligned(v, 4) &&
                   aligned(o, 4) && aligned(g, 4) && aligned(beta, 4) && aligned(read_slots, 4) &&
                   aligned(write_slots, 4) && aligned(status, 4),

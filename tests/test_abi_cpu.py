@@ -130,6 +130,8 @@ def test_decode_checks(L):
                              None) == kda.KDA_ERR_UNSUPPORTED
     assert L.kda_decode_step(1, 0, 2, 128, 128, 1.0, p, p, p, p, p, p, p, 10, p, None,
                              None) == kda.KDA_OK
+    assert L.kda_decode_step(1, 1 << 30, 2, 128, 128, 1.0, p, p, p, p, p, p, p, 10, p, None,
+                             None) == kda.KDA_ERR_INVALID_ARG   # batch * H > 2^30
 
 
 def test_window_checks(L):
@@ -146,6 +148,7 @@ def test_window_checks(L):
     assert win(pool=p + 8) == kda.KDA_ERR_INVALID_ARG       # the pool must be 16-byte aligned
     assert win(ws=None) == kda.KDA_ERR_INVALID_ARG
     assert win(batch=-1) == kda.KDA_ERR_INVALID_ARG
+    assert win(batch=(1 << 27) + 1) == kda.KDA_ERR_INVALID_ARG  # batch * window * H > 2^30
     assert win(batch=0) == kda.KDA_OK                      # nothing to do launches nothing
     assert win(window=0) == kda.KDA_OK
 
