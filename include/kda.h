@@ -6,10 +6,11 @@
  *     S_t = (I - beta_t k_t k_t^T) Diag(a_t) S_{t-1} + beta_t k_t v_t^T,   a_t = exp(g_t)
  *     o_t = scale * S_t^T q_t
  * g_t in R^{dk} is a per-key-channel log-decay (g <= 0), beta_t a scalar write strength.
- * This is the "KDA" linear-attention state that pegainfer PR #970 ("feat(k3): cross-process
+ * This is the KDA linear-attention state that pegainfer PR #970 ("feat(k3): cross-process
  * CP whale gang - fleet-wide long-prompt prefill") prefills with FlashKDA per context-parallel
- * segment, and whose per-segment "(M,D) packages" it exchanges and combines with a
- * "Blelloch prefix-scan fallback" (whale-rendezvous and fabric data-plane commit messages).
+ * segment; each segment publishes its (M,D) package, and the packages are combined by an
+ * exchange or, at lower traffic, a Blelloch prefix scan (whale-rendezvous and fabric
+ * data-plane commit messages).
  * kern PR #44 keeps one KDA state block per packed sequence (varlen, cu_seqlens) and
  * ATOM PR #2709 ("feat(kimi-k3): PP8 prefill for P/D serving - KDA state under PP")
  * updates slot-addressed KDA state one decode token at a time.
@@ -110,7 +111,8 @@ KDA_API size_t kda_chunk_workspace(kda_dtype dt, int n_ranges, int total_tokens,
  *               NULL when that query returns 0 (KDA_ERR_WORKSPACE otherwise).
  *   status      optional device word (KDA_STATUS_DECAY_RANGE).
  * Source: the chunked FlashKDA prefill of kern PR #44 (varlen build with cu_seqlens and
- * per-sequence state blocks) and pegainfer PR #970 ("same segment walk, same chunk step").
+ * per-sequence state blocks) and pegainfer PR #970 (fabric data-plane commit message: the
+ * segment replay runs the same per-chunk step as the prefill).
  */
 KDA_API kda_status kda_chunk_prefill(kda_dtype dt, int n_seqs, int total_tokens,
                              const int32_t* cu_seqlens, int H, int dk, int dv, int chunk,
@@ -126,7 +128,8 @@ KDA_API kda_status kda_chunk_prefill(kda_dtype dt, int n_seqs, int total_tokens,
  * M S_in + D. No outputs o are produced and q is not read.
  *   seg_offsets device int32 [n_segs + 1].
  *   workspace   as for kda_chunk_prefill, sized by kda_chunk_workspace(dt, n_segs, ...).
- * Source: pegainfer PR #970, "KDA (M,D) packages" of the CP publish surface.
+ * Source: pegainfer PR #970, fabric data-plane commit message (the (M,D) package each
+ * context-parallel member publishes for its segment).
  */
 KDA_API kda_status kda_segment_package(kda_dtype dt, int n_segs, int total_tokens,
                                const int32_t* seg_offsets, int H, int dk, int dv, int chunk,
@@ -151,7 +154,8 @@ KDA_API kda_status kda_segment_package(kda_dtype dt, int n_segs, int total_token
  *                     padded tree: n_seqs * (3/2) * P2 * H packages of (dk*dk + dk*dv) fp32,
  *                     P2 = max_segs_per_seq rounded up to a power of two.
  *   status            optional device word (KDA_STATUS_BAD_OFFSETS).
- * Source: pegainfer PR #970, "the Blelloch prefix-scan fallback" for combining packages.
+ * Source: pegainfer PR #970, whale-rendezvous commit message (a Blelloch prefix scan over the
+ * packages as the lower-traffic way to combine them).
  */
 KDA_API size_t kda_package_scan_workspace(int n_seqs, int max_segs_per_seq, int H, int dk, int dv);
 KDA_API kda_status kda_package_scan(int n_seqs, int n_segs, const int32_t* seq_seg_offsets,
@@ -211,8 +215,8 @@ KDA_API kda_status kda_segment_replay(kda_dtype dt, int n_segs, int total_tokens
  *              KDA_ERR_UNSUPPORTED.
  *   beta       16-byte aligned. status: optional device word (KDA_STATUS_DECAY_RANGE).
  * The pages have no separate counterpart: their context-parallel members prepare a segment
- * once and both publish its package and replay it ("same segment walk, same chunk step",
- * pegainfer PR #970, fabric data-plane commit message).
+ * once and both publish its package and replay it with the same per-chunk step (pegainfer
+ * PR #970, fabric data-plane commit message).
  */
 KDA_API kda_status kda_chunk_prepare(kda_dtype dt, int n_ranges, int total_tokens,
                                      const int32_t* offsets, int H, int dk, int dv, int chunk,

@@ -2,9 +2,10 @@
 //
 // A package (M, D) maps a segment's entry state to its exit state, S_out = M S_in + D, and
 // two consecutive packages combine as (M2, D2) o (M1, D1) = (M2 M1, M2 D1 + D2) ("apply 1,
-// then 2"). pegainfer PR #970 exchanges these "KDA (M,D) packages" between context-parallel
-// ranks and names a "Blelloch prefix-scan fallback" for combining them; this file runs that
-// work-efficient scan on one GPU, per (sequence, head):
+// then 2"). pegainfer PR #970 (whale-rendezvous and fabric data-plane commit messages)
+// exchanges these KDA (M,D) packages between context-parallel ranks and names a Blelloch
+// prefix scan as the lower-traffic way to combine them; this file runs that work-efficient
+// scan on one GPU, per (sequence, head):
 //   * the sequence's packages are copied into a power-of-two tree, padded with (I, 0);
 //   * up-sweep: at stride d, node i (i+1 multiple of 2d) becomes a[i] o a[i-d];
 //   * the root (the whole sequence's package) gives the exit state, then becomes (I, 0);

@@ -9,8 +9,8 @@
 //   S_t = (I - beta_t k_t k_t^T) Diag(a_t) S_{t-1} + beta_t k_t v_t^T,  a_t = exp(g_t),
 //   o_t = scale * S_t^T q_t.
 // The recurrence is the one the pegainfer pull request #970 ("feat(k3): cross-process CP
-// whale gang - fleet-wide long-prompt prefill") prefills with FlashKDA and publishes as
-// "KDA (M,D) packages" per context-parallel segment (commit message of the fabric data-plane
+// whale gang - fleet-wide long-prompt prefill") prefills with FlashKDA and publishes as one
+// KDA (M,D) package per context-parallel segment (commit message of the fabric data-plane
 // change); the pages name the operator but do not write the formula, so the formula above is
 // the plainest statement of the gated delta rule with per-key-channel decay, decay applied
 // before the erase, and the output read from the updated state.
