@@ -47,6 +47,9 @@ def _load():
         lib.kda_ref_decode_window.argtypes = [c_int, c_int, c_int, c_int, c_int, c_dbl, d, d, d,
                                               d, d, c_int, i64, i64, d, c_i64, d, c_int]
         lib.kda_ref_decode_window.restype = c_int
+        lib.kda_ref_short_conv.argtypes = [c_int, i64, c_int, c_int, d, d, c_int, i64, i64, d,
+                                           c_i64, d, c_int]
+        lib.kda_ref_short_conv.restype = c_int
         _lib = lib
     return _lib
 
@@ -209,3 +212,30 @@ def slot_copy(src, src_ids, dst, dst_ids):
         elif a >= 0 and b >= 0:
             dst[b] = src[a]
     return bad
+
+
+def short_conv(x, w, cu_seqlens=None, silu=False, read_slots=None, write_slots=None,
+               pool=None, threads=0):
+    """Short causal depthwise convolution over packed sequences (x [T, C], w [C, W]) with a
+    per-sequence history of W - 1 inputs in pool [n_slots, W-1, C] (a float64 copy, updated
+    in place when write_slots is given). Returns (out [T, C], number of slot ids >= n_slots)."""
+    lib = _load()
+    x, w = _f64(x), _f64(w)
+    T, C = x.shape
+    W = w.shape[1]
+    cu = _i64([0, T] if cu_seqlens is None else cu_seqlens)
+    n = len(cu) - 1
+    rs = None if read_slots is None else _i64(read_slots)
+    ws = None if write_slots is None else _i64(write_slots)
+    if pool is not None:
+        assert pool.dtype == np.float64 and pool.flags["C_CONTIGUOUS"]
+    n_slots = 0 if pool is None else pool.shape[0]
+    out = np.zeros((T, C))
+    rc = lib.kda_ref_short_conv(n, _ptr(cu, ctypes.c_int64), C, W, _ptr(x), _ptr(w),
+                                int(bool(silu)), _ptr(rs, ctypes.c_int64),
+                                _ptr(ws, ctypes.c_int64), _ptr(pool), n_slots, _ptr(out),
+                                int(threads))
+    if rc < 0:
+        raise ValueError("kda_ref_short_conv: bad arguments")
+    return out, rc
+

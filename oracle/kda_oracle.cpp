@@ -317,4 +317,56 @@ int kda_ref_decode_window(int B, int W, int H, int dk, int dv, double scale, con
   return bad.load();
 }
 
+// Short causal depthwise convolution over packed varlen rows, with a per-sequence window of
+// the last (W - 1) inputs kept in a slot pool: the KDA short-conv gather and window update of
+// kern PR #44 (per-sequence varlen kernels of the stage split), read through a read-side slot
+// index as in ATOM PR #2709 (the spec conv update takes a read index). The pages do not give
+// the width W or an activation; both are parameters here.
+// For sequence s and channel c, with history h (W - 1 inputs, oldest first) taken from slot
+// read_slots[s] (zeros when the id is negative or read_slots is NULL):
+//   y_t = sum_{i=0}^{W-1} w[c, i] * z[t - (W - 1) + i],  z = [h ; x_s]  (w[c, W-1] multiplies
+//   the current input), out_t = silu ? y_t / (1 + exp(-y_t)) : y_t,
+// and afterwards the last W - 1 entries of z are stored into slot write_slots[s] (not stored
+// when the id is negative or write_slots is NULL).
+//   cu_seqlens: [n_seqs+1]; x, out: [T, C]; w: [C, W]; pool: [n_slots, W-1, C].
+// Ids >= n_slots are skipped (read: zero history; write: nothing stored) and counted.
+// Returns the count, or -1 on bad arguments.
+int kda_ref_short_conv(int n_seqs, const int64_t* cu_seqlens, int C, int W, const double* x,
+                       const double* w, int silu, const int64_t* read_slots,
+                       const int64_t* write_slots, double* pool, int64_t n_slots, double* out,
+                       int n_threads) {
+  if (n_seqs < 0 || C <= 0 || W <= 0 || !cu_seqlens || !x || !w || !out) return -1;
+  if ((read_slots || write_slots) && !pool) return -1;
+  std::atomic<int> bad(0);
+  const int nblk = (C + kColBlock - 1) / kColBlock;
+  const int hw = W - 1;
+  parallel_items((int64_t)n_seqs * nblk, n_threads, [&](int64_t it) {
+    const int blk = (int)(it % nblk);
+    const int s = (int)(it / nblk);
+    const int c0 = blk * kColBlock, c1 = std::min(C, c0 + kColBlock);
+    const int64_t r = read_slots ? read_slots[s] : -1;
+    const int64_t wr = write_slots ? write_slots[s] : -1;
+    if (blk == 0) bad.fetch_add((r >= n_slots ? 1 : 0) + (wr >= n_slots ? 1 : 0));
+    const int64_t t0 = cu_seqlens[s], t1 = cu_seqlens[s + 1];
+    for (int c = c0; c < c1; ++c) {
+      // z = [h ; x_s] for this channel
+      std::vector<double> z((size_t)(hw + (t1 - t0)), 0.0);
+      if (r >= 0 && r < n_slots)
+        for (int j = 0; j < hw; ++j) z[j] = pool[(r * hw + j) * C + c];
+      for (int64_t t = t0; t < t1; ++t) z[hw + (t - t0)] = x[t * C + c];
+      for (int64_t t = t0; t < t1; ++t) {
+        const int64_t u = hw + (t - t0);  // position of x_t in z
+        double y = 0.0;
+        for (int i = 0; i < W; ++i) y += w[(int64_t)c * W + i] * z[u - hw + i];
+        out[t * C + c] = silu ? y / (1.0 + std::exp(-y)) : y;
+      }
+      if (wr >= 0 && wr < n_slots) {
+        const size_t n = z.size();
+        for (int j = 0; j < hw; ++j) pool[(wr * hw + j) * C + c] = z[n - hw + j];
+      }
+    }
+  });
+  return bad.load();
+}
+
 }  // extern "C"

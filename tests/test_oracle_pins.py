@@ -438,3 +438,87 @@ def test_slot_zero_and_copy(oracle_mod):
     np.testing.assert_array_equal(pool[1], pool0[4])
     np.testing.assert_array_equal(pool[[0] + list(range(2, 10))],
                                   pool0[[0] + list(range(2, 10))])
+
+
+# Short causal depthwise convolution with a per-sequence history (the KDA short-conv gather
+# and window update). Pinned by numpy's and scipy's convolution / FIR filter routines, the
+# library sigmoid, and split/packing invariants.
+def test_short_conv_matches_library_convolution(oracle_mod):
+    rng = np.random.default_rng(31)
+    T, C = 23, 5
+    for W in (1, 2, 3, 4):
+        x = rng.standard_normal((T, C))
+        w = rng.standard_normal((C, W))
+        h0 = rng.standard_normal((1, W - 1, C))
+        pool = h0.copy()
+        out, bad = oracle_mod.short_conv(x, w, read_slots=[0], pool=pool)
+        assert bad == 0
+        for c in range(C):
+            z = np.concatenate([h0[0, :, c], x[:, c]])
+            ref = np.convolve(z, w[c, ::-1])[W - 1:W - 1 + T]   # correlation = reversed kernel
+            np.testing.assert_allclose(out[:, c], ref, rtol=1e-13, atol=1e-13)
+        out0, _ = oracle_mod.short_conv(x, w)                   # no history: zeros
+        for c in range(C):
+            np.testing.assert_allclose(out0[:, c], np.convolve(x[:, c], w[c, ::-1])[:T],
+                                       rtol=1e-13, atol=1e-13)
+    signal = pytest.importorskip("scipy.signal")
+    for c in range(C):
+        np.testing.assert_allclose(out0[:, c], signal.lfilter(w[c, ::-1], [1.0], x[:, c]),
+                                   rtol=1e-12, atol=1e-12)
+
+
+def test_short_conv_silu_matches_library_sigmoid(oracle_mod):
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(32)
+    x = rng.standard_normal((17, 6)) * 3
+    w = rng.standard_normal((6, 4))
+    y, _ = oracle_mod.short_conv(x, w)
+    s, _ = oracle_mod.short_conv(x, w, silu=True)
+    np.testing.assert_allclose(s, y * special.expit(y), rtol=1e-13, atol=1e-14)
+
+
+def test_short_conv_split_packing_and_slots(oracle_mod):
+    """Running a sequence in two calls, the history carried through a slot, equals one call at
+    every split point (including splits shorter than the window); packed sequences equal
+    separate runs; slot plumbing (fork, padding, out-of-range) behaves as specified."""
+    rng = np.random.default_rng(33)
+    T, C, W = 9, 4, 4
+    x = rng.standard_normal((T, C))
+    w = rng.standard_normal((C, W))
+    h0 = rng.standard_normal((3, W - 1, C))
+    full_pool = h0.copy()
+    full, _ = oracle_mod.short_conv(x, w, silu=True, read_slots=[0], write_slots=[1],
+                                    pool=full_pool)
+    np.testing.assert_array_equal(full_pool[0], h0[0])          # the read slot is untouched
+    np.testing.assert_array_equal(full_pool[1], x[T - (W - 1):])  # window = last W-1 inputs
+    for t in range(T + 1):
+        pool = h0.copy()
+        a, _ = oracle_mod.short_conv(x[:t], w, silu=True, read_slots=[0], write_slots=[2],
+                                     pool=pool)
+        b, _ = oracle_mod.short_conv(x[t:], w, silu=True, read_slots=[2], write_slots=[2],
+                                     pool=pool)
+        np.testing.assert_array_equal(np.concatenate([a, b]), full)
+        np.testing.assert_array_equal(pool[2], full_pool[1])
+    # packed sequences, one of them empty, one short
+    lens = [5, 0, 2, 7]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    xs = rng.standard_normal((cu[-1], C))
+    pool0 = rng.standard_normal((12, W - 1, C))
+    pool = pool0.copy()
+    read, write = [3, 4, 5, -1], [6, 7, 8, 20]
+    out, bad = oracle_mod.short_conv(xs, w, cu_seqlens=cu, read_slots=read, write_slots=write,
+                                     pool=pool)
+    assert bad == 1                                             # write slot 20 >= 12
+    for s in range(4):
+        p1 = pool0.copy()
+        o1, _ = oracle_mod.short_conv(xs[cu[s]:cu[s + 1]], w, read_slots=[read[s]],
+                                      write_slots=[write[s]] if write[s] < 12 else None,
+                                      pool=p1)
+        np.testing.assert_array_equal(out[cu[s]:cu[s + 1]], o1)
+        if write[s] < 12:
+            np.testing.assert_array_equal(pool[write[s]], p1[write[s]])
+    np.testing.assert_array_equal(pool[7], pool0[4])            # empty sequence: history kept
+    np.testing.assert_array_equal(pool[8][:1], pool0[5][2:])    # short: old tail, then inputs
+    np.testing.assert_array_equal(pool[8][1:], xs[cu[2]:cu[3]])
+    for sl in (0, 1, 2, 3, 4, 5, 9, 10, 11):
+        np.testing.assert_array_equal(pool[sl], pool0[sl])
