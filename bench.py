@@ -251,10 +251,10 @@ def run_gb300(args):
                 "traffic": TRAFFIC_PREFILL_16K, "kernel": "prefill_16k (chunk_fused_kernel)",
                 "peak_source": peaks["source"]}
 
-    # The slot-table extensions of the decode path, timed on their own after the step (each
-    # over its own CUDA events, the same number of iterations): a 4-token verify window per
-    # row with forked read slots and logit write strengths, a checkpoint image of the decode
-    # rows' 256 slots (and its restore), and zeroing 256 slots.
+    # The extensions, timed on their own after the step (each over its own CUDA events, the
+    # same number of iterations): a 4-token verify window per row with forked read slots and
+    # logit write strengths, a checkpoint image of the decode rows' 256 slots (and its
+    # restore), zeroing 256 slots, and the short conv over the 16k prefill's q, k, v channels.
     win = inputs.make_workload("window_256x4", device=dev)
     Bw, Ww = win.write_slots.shape
     ow = torch.empty_like(win.v)
@@ -277,8 +277,16 @@ def run_gb300(args):
     def zero():
         kda.slot_zero(win.pool, free_slots)
 
+    cv = inputs.make_workload("conv_16k", device=dev)
+    cv_out = torch.empty_like(cv.x)
+
+    def conv():
+        kda.short_conv(cv.x, cv.weight, cv.cu_seqlens, silu=True, read_slots=cv.read_slots,
+                       write_slots=cv.write_slots, conv_state=cv.state, out=cv_out)
+
     ext_parts = [("window_256x4", window), ("slot_checkpoint_256", checkpoint),
-                 ("slot_restore_256", restore), ("slot_zero_256", zero)]
+                 ("slot_restore_256", restore), ("slot_zero_256", zero),
+                 ("short_conv_16k", conv)]
     for _ in range(args.warmup):
         for _, fn in ext_parts:
             fn()
@@ -303,6 +311,9 @@ def run_gb300(args):
         "slot_checkpoint_256": 2 * B * slot_bytes + B * 4,
         "slot_restore_256": 2 * B * slot_bytes + B * 4,
         "slot_zero_256": B * slot_bytes + B * 4,
+        # x read once, out written once (bf16), weights, the two history windows
+        "short_conv_16k": (2 * cv.x.numel() * cv.x.element_size() + cv.weight.numel() * 4
+                           + 2 * cv.state[0].numel() * cv.state.element_size()),
     }
     extensions = {}
     for n, _ in ext_parts:
@@ -311,7 +322,9 @@ def run_gb300(args):
                          "gbs": round(gbs, 1), "hbm_frac": round(gbs / hbm, 4)}
     extensions["window_256x4"]["tokens_per_s"] = round(Bw * Ww / (ext_ms["window_256x4"] * 1e-3),
                                                        1)
-    del win
+    extensions["short_conv_16k"]["tokens_per_s"] = round(
+        cv.x.shape[0] / (ext_ms["short_conv_16k"] * 1e-3), 1)
+    del win, cv, cv_out
 
     # end to end through the public API with host buffers: every step copies its inputs in from
     # pinned host memory, runs kda_chunk_prefill and copies o and the final state back out.
@@ -454,7 +467,7 @@ def run_reference(args):
 
 def run_profile_case(args):
     """A small case of one call (inputs still larger than L2, a few GB on the device at most)
-    for ncu captures: `--profile-case prefill|package|replay|scan|decode|window|slots`,
+    for ncu captures: `--profile-case prefill|package|replay|scan|decode|window|slots|conv`,
     `--launches N`."""
     import torch
     from linear_attention_state_kda_gb300 import inputs, kda
@@ -468,6 +481,11 @@ def run_profile_case(args):
         w = inputs.make_window(128, 4, 32, D, D, 640, seed=1005, device=dev)
         fns = [lambda: kda.decode_window(w.q, w.k, w.v, w.g, w.beta_logit, w.read_slots,
                                          w.write_slots, w.pool, beta_is_logit=True)]
+    elif case == "conv":
+        cv = inputs.make_workload("conv_16k", device=dev)
+        fns = [lambda: kda.short_conv(cv.x, cv.weight, cv.cu_seqlens, silu=True,
+                                      read_slots=cv.read_slots, write_slots=cv.write_slots,
+                                      conv_state=cv.state)]
     elif case == "slots":
         d = inputs.make_decode(256, 32, D, D, 1024, seed=1004, device=dev)
         image = torch.empty(256, 32, D, D, device=dev)
@@ -501,7 +519,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile-case", default=None,
                     choices=["prefill", "package", "scan", "replay", "decode", "window",
-                             "slots"])
+                             "slots", "conv"])
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)

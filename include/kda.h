@@ -325,6 +325,40 @@ KDA_API kda_status kda_slot_copy(int n, const float* src, const int32_t* src_ids
                                  float* dst, const int32_t* dst_ids, int64_t n_dst,
                                  int64_t slot_elems, uint32_t* status, kda_stream_t stream);
 
+/* Bits of the `flags` argument of kda_short_conv. */
+#define KDA_CONV_SILU 1u /* out = y / (1 + exp(-y)) instead of y */
+
+/*
+ * kda_short_conv: short causal depthwise convolution over packed sequences, each with a
+ * history window of the width - 1 inputs before it kept in a slot pool (the KDA short-conv
+ * gather and window update). For sequence s and channel c, with h the window read from slot
+ * read_slots[s] (oldest first; zeros for a negative id or read_slots == NULL) and
+ * z = [h ; x rows of s]:
+ *     y_t = sum_{i=0}^{width-1} weight[c, i] * z[t - (width - 1) + i]
+ *     out_t = y_t, or y_t / (1 + exp(-y_t)) with KDA_CONV_SILU,
+ * and the last width - 1 entries of z are stored into slot write_slots[s] (nothing for a
+ * negative id or write_slots == NULL). An empty sequence passes its window through.
+ *   cu_seqlens   device int32 [n_seqs + 1], or NULL for one sequence of total_tokens.
+ *   x, out       [total_tokens, channels] (dtype dt), 16-byte aligned; out must not alias x.
+ *   weight       [channels, width] fp32 (weight[c, width-1] weighs the current input).
+ *   conv_state   [n_slots, width - 1, channels] (dtype dt), 16-byte aligned; may be NULL
+ *                when both slot tables are NULL or width = 1.
+ *   read_slots, write_slots  device int32 [n_seqs] or NULL. An id >= n_slots is treated as
+ *                negative and sets KDA_STATUS_BAD_SLOT. read slot = write slot updates the
+ *                window in place; slots named by different sequences must be disjoint.
+ *   channels     a positive multiple of 8; width 1 .. 4 (else KDA_ERR_UNSUPPORTED).
+ *   status       optional device word (KDA_STATUS_BAD_SLOT, KDA_STATUS_BAD_OFFSETS).
+ * Source: kern PR #44, squash message (the short-conv gather and window update among the
+ * per-sequence kernels generalised to varlen rows); ATOM PR #2709 (the speculative conv update
+ * reads its window through a read-side index). Width and activation are not on the pages.
+ */
+KDA_API kda_status kda_short_conv(kda_dtype dt, int n_seqs, int total_tokens,
+                                  const int32_t* cu_seqlens, int channels, int width,
+                                  const void* x, const float* weight, unsigned flags,
+                                  const int32_t* read_slots, const int32_t* write_slots,
+                                  void* conv_state, int64_t n_slots, void* out,
+                                  uint32_t* status, kda_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -368,4 +368,41 @@ kda_status kda_slot_copy(int n, const float* src, const int32_t* src_ids, int64_
                       (cudaStream_t)stream);
 }
 
+kda_status kda_short_conv(kda_dtype dt, int n_seqs, int total_tokens, const int32_t* cu_seqlens,
+                          int channels, int width, const void* x, const float* weight,
+                          unsigned flags, const int32_t* read_slots, const int32_t* write_slots,
+                          void* conv_state, int64_t n_slots, void* out, uint32_t* status,
+                          kda_stream_t stream) {
+  const char* fn = "kda_short_conv";
+  KDA_REQUIRE(dt == KDA_F32 || dt == KDA_BF16, KDA_ERR_UNSUPPORTED,
+              "kda_short_conv: dtype must be KDA_F32 or KDA_BF16");
+  KDA_REQUIRE(width >= 1 && width <= 4, KDA_ERR_UNSUPPORTED,
+              "kda_short_conv: width must be in 1 .. 4");
+  KDA_REQUIRE(channels > 0 && channels % 8 == 0, KDA_ERR_INVALID_ARG,
+              "kda_short_conv: channels must be a positive multiple of 8");
+  KDA_REQUIRE(n_seqs >= 0 && total_tokens >= 0, KDA_ERR_INVALID_ARG,
+              "kda_short_conv: n_seqs and total_tokens must be >= 0");
+  KDA_REQUIRE(cu_seqlens || n_seqs <= 1, KDA_ERR_INVALID_ARG,
+              "kda_short_conv: cu_seqlens is required for more than one sequence");
+  KDA_REQUIRE((flags & ~KDA_CONV_SILU) == 0, KDA_ERR_INVALID_ARG,
+              "kda_short_conv: unknown flag bits");
+  if (n_seqs == 0) return KDA_OK;
+  const bool slots = (read_slots || write_slots) && width > 1;
+  KDA_REQUIRE(!slots || (conv_state && n_slots > 0), KDA_ERR_INVALID_ARG,
+              "kda_short_conv: slot tables need conv_state and n_slots > 0");
+  KDA_REQUIRE(total_tokens == 0 || (x && weight && out), KDA_ERR_INVALID_ARG,
+              "kda_short_conv: x, weight and out must be non-null");
+  KDA_REQUIRE((int64_t)total_tokens / 64 + n_seqs <= 0x7fffffffLL, KDA_ERR_INVALID_ARG,
+              "kda_short_conv: too many tokens");
+  KDA_REQUIRE(aligned(x, 16) && aligned(out, 16) && aligned(conv_state, 16) &&
+                  aligned(weight, 4) && aligned(cu_seqlens, 4) && aligned(read_slots, 4) &&
+                  aligned(write_slots, 4) && aligned(status, 4),
+              KDA_ERR_INVALID_ARG, "kda_short_conv: misaligned pointer");
+  KDA_REQUIRE(!(x && x == out), KDA_ERR_INVALID_ARG, "kda_short_conv: out must not alias x");
+  (void)fn;
+  return launch_short_conv(dt, n_seqs, total_tokens, cu_seqlens, channels, width, x, weight,
+                           flags, slots ? read_slots : nullptr, slots ? write_slots : nullptr,
+                           conv_state, slots ? n_slots : 0, out, status, (cudaStream_t)stream);
+}
+
 }  // extern "C"

@@ -91,6 +91,12 @@ kda_status launch_slots(bool zero, int n, const float* src, const int32_t* src_i
                         float* dst, const int32_t* dst_ids, int64_t n_dst, int64_t slot_elems,
                         uint32_t* status, cudaStream_t s);
 
+// Short causal depthwise convolution with per-sequence history windows (width 1..4).
+kda_status launch_short_conv(kda_dtype dt, int n_seqs, int total, const int32_t* cu, int C,
+                             int width, const void* x, const float* w, unsigned flags,
+                             const int32_t* read_slots, const int32_t* write_slots, void* hist,
+                             int64_t n_slots, void* out, uint32_t* status, cudaStream_t s);
+
 // Package scan.
 size_t scan_workspace_bytes(int n_seqs, int max_segs, int H, int dk, int dv);
 kda_status launch_scan(int n_seqs, int n_segs, const int32_t* seq_seg_offsets, int max_segs,

@@ -82,6 +82,17 @@ class WindowInputs:
     write_slots: torch.Tensor  # [B, W] int32, disjoint from each other and from read_slots
 
 
+@dataclass
+class ConvInputs:
+    x: torch.Tensor            # [T, C] (packed sequences, token-major)
+    weight: torch.Tensor       # [C, W] fp32
+    cu_seqlens: torch.Tensor   # [N+1] int32
+    state: torch.Tensor        # [n_slots, W-1, C], dtype of x
+    read_slots: torch.Tensor   # [N] int32
+    write_slots: torch.Tensor  # [N] int32, disjoint from read_slots
+    lens: List[int] = field(default_factory=list)
+
+
 _DT = {"bf16": torch.bfloat16, "f32": torch.float32}
 
 
@@ -152,6 +163,27 @@ def make_window(B, W, H, dk, dv, n_slots, dtype="bf16", seed=0, device="cpu", po
                         beta_logit=logit.contiguous(), pool=pool.contiguous(),
                         read_slots=perm[:B].contiguous(),
                         write_slots=perm[B:].reshape(B, W).contiguous())
+
+
+def make_conv(lens, C, W, dtype="bf16", seed=0, device="cpu", n_slots=None) -> ConvInputs:
+    """Short-conv inputs: x ~ N(0, 1) [T, C], weight ~ N(0, 1/W) [C, W], history windows
+    ~ N(0, 1) in a pool of n_slots (default 2N) slots, and N read plus N write slots sampled
+    without replacement."""
+    lens = [int(v) for v in lens]
+    N, T = len(lens), sum(lens)
+    n_slots = 2 * N if n_slots is None else int(n_slots)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(int(seed))
+    x = torch.randn(T, C, generator=gen, device=device)
+    weight = torch.randn(C, W, generator=gen, device=device) / float(W) ** 0.5
+    state = torch.randn(n_slots, max(W - 1, 0), C, generator=gen, device=device)
+    perm = torch.randperm(n_slots, generator=gen, device=device)[:2 * N].to(torch.int32)
+    cu = torch.zeros(N + 1, dtype=torch.int32)
+    cu[1:] = torch.cumsum(torch.tensor(lens, dtype=torch.int64), 0).to(torch.int32)
+    dt = _DT[dtype]
+    return ConvInputs(x=x.to(dt).contiguous(), weight=weight.contiguous(), cu_seqlens=cu.to(device),
+                      state=state.to(dt).contiguous(), read_slots=perm[:N].contiguous(),
+                      write_slots=perm[N:].contiguous(), lens=lens)
 
 
 def leveled_split(length, n_segs, q=LEVEL_Q, align=64):
@@ -235,6 +267,9 @@ WORKLOADS = {
     # pool, each row reading one slot and storing a snapshot per token into 4 others.
     "window_256x4": dict(kind="window", B=256, W=4, H=32, dk=128, dv=128, n_slots=4096,
                          dtype="bf16", seed=1005, pool_std=0.02),
+    # short conv over the prefill's q, k and v channels (3 x 32 heads x 128 = 12288 channels)
+    # of one 16k-token sequence, width 4, SiLU, history read from one slot, stored to another.
+    "conv_16k": dict(kind="conv", lens=[16384], C=12288, W=4, dtype="bf16", seed=1006),
 }
 
 
@@ -251,6 +286,8 @@ def workload_segments(name):
 def make_workload(name, device="cpu", decay_scale=1.0, beta_scale=1.0, **over):
     w = dict(WORKLOADS[name])
     w.update(over)
+    if w["kind"] == "conv":
+        return make_conv(w["lens"], w["C"], w["W"], w["dtype"], w["seed"], device)
     if w["kind"] == "window":
         return make_window(w["B"], w["W"], w["H"], w["dk"], w["dv"], w["n_slots"], w["dtype"],
                            w["seed"], device, w.get("pool_std", 0.02), decay_scale)

@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libkda.so")
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_WORKSPACE, KDA_ERR_CUDA = range(5)
 KDA_F32, KDA_BF16 = 0, 1
 DECODE_BETA_LOGIT = 1
+CONV_SILU = 1
 MAX_WINDOW = 16
 STATUS_BAD_SLOT, STATUS_DECAY_RANGE, STATUS_BAD_OFFSETS = 1, 2, 4
 
@@ -76,6 +77,8 @@ def lib():
     L.kda_slot_zero.argtypes = [I, P, P, I64, I64, P, P]
     L.kda_slot_copy.restype = I
     L.kda_slot_copy.argtypes = [I, P, P, I64, P, P, I64, I64, P, P]
+    L.kda_short_conv.restype = I
+    L.kda_short_conv.argtypes = [I, I, I, P, I, I, P, P, ctypes.c_uint, P, P, P, I64, P, P, P]
     _lib = L
     return L
 
@@ -364,4 +367,25 @@ def slot_copy(src, src_ids, dst, dst_ids, n=None, status=None, stream=None):
                                _ptr(dst_ids), int(dst.shape[0]), int(src[0].numel()),
                                _ptr(status), _stream(stream)))
     return dst
+
+
+def short_conv(x, weight, cu_seqlens=None, silu=False, read_slots=None, write_slots=None,
+               conv_state=None, out=None, status=None, stream=None):
+    """kda_short_conv: causal depthwise convolution of x [T, C] with weight [C, W] over the
+    packed sequences of cu_seqlens, each starting from the W - 1 inputs in conv_state
+    [n_slots, W-1, C] at its read slot and leaving its last W - 1 inputs at its write slot.
+    Returns out [T, C]."""
+    _contig(x, weight, cu_seqlens, read_slots, write_slots, conv_state, out)
+    _int32(cu_seqlens, read_slots, write_slots)
+    T, C = x.shape
+    W = weight.shape[1]
+    n = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if out is None:
+        out = torch.empty_like(x)
+    n_slots = 0 if conv_state is None else int(conv_state.shape[0])
+    _check(lib().kda_short_conv(_dt(x), n, T, _ptr(cu_seqlens), C, W, _ptr(x), _ptr(weight),
+                                CONV_SILU if silu else 0, _ptr(read_slots), _ptr(write_slots),
+                                _ptr(conv_state), n_slots, _ptr(out), _ptr(status),
+                                _stream(stream)))
+    return out
 

@@ -164,3 +164,24 @@ def test_slot_checks(L):
     assert L.kda_slot_copy(5, p, None, 4, p, p, 10, 8, None, None) == kda.KDA_ERR_INVALID_ARG
     assert L.kda_slot_copy(4, p, p, 0, p, p, 10, 8, None, None) == kda.KDA_ERR_INVALID_ARG
     assert L.kda_slot_copy(0, p, p, 10, p, p, 10, 8, None, None) == kda.KDA_OK
+
+
+def test_short_conv_checks(L):
+    from linear_attention_state_kda_gb300 import kda
+    p = 4096
+    def conv(dt=1, n=1, T=64, cu=None, C=64, W=4, x=p, flags=0, rs=None, ws=None, st=None,
+             ns=0, out=p + 4096):
+        return L.kda_short_conv(dt, n, T, cu, C, W, x, p, flags, rs, ws, st, ns, out, None,
+                                None)
+
+    assert conv(W=5) == kda.KDA_ERR_UNSUPPORTED
+    assert conv(W=0) == kda.KDA_ERR_UNSUPPORTED
+    assert conv(dt=7) == kda.KDA_ERR_UNSUPPORTED
+    assert conv(C=12) == kda.KDA_ERR_INVALID_ARG               # not a multiple of 8
+    assert conv(n=2) == kda.KDA_ERR_INVALID_ARG                # two sequences need cu_seqlens
+    assert conv(flags=2) == kda.KDA_ERR_INVALID_ARG
+    assert conv(rs=p) == kda.KDA_ERR_INVALID_ARG               # slot tables need a state pool
+    assert conv(x=p + 8) == kda.KDA_ERR_INVALID_ARG            # misaligned
+    assert conv(out=p) == kda.KDA_ERR_INVALID_ARG              # out aliases x
+    assert conv(x=None) == kda.KDA_ERR_INVALID_ARG
+    assert conv(n=0) == kda.KDA_OK                             # nothing to do launches nothing

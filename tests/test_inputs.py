@@ -34,6 +34,16 @@ def test_window_slots_disjoint_and_logits():
     assert torch.equal(w.q, p.q) and torch.equal(w.g, p.g) and torch.equal(w.beta, p.beta)
 
 
+def test_conv_inputs():
+    c = inputs.make_conv([5, 0, 9], 16, 4, seed=2, n_slots=10)
+    assert c.x.shape == (14, 16) and c.weight.shape == (16, 4) and c.state.shape == (10, 3, 16)
+    assert c.cu_seqlens.tolist() == [0, 5, 5, 14]
+    ids = c.read_slots.tolist() + c.write_slots.tolist()
+    assert len(set(ids)) == 6 and min(ids) >= 0 and max(ids) < 10
+    d = inputs.make_conv([5, 0, 9], 16, 4, seed=2, n_slots=10)
+    assert torch.equal(c.x, d.x) and torch.equal(c.state, d.state)
+
+
 def test_leveled_split_rule():
     for length, n in [(131072, 16), (65536, 16), (32768, 8), (8192, 4)]:
         segs = inputs.gang_split(length)
