@@ -26,32 +26,35 @@ _lib = None
 def _load():
     global _lib
     if _lib is None:
-        path = _build.build()
-        lib = ctypes.CDLL(path)
-        d = ctypes.POINTER(ctypes.c_double)
-        i64 = ctypes.POINTER(ctypes.c_int64)
-        c_int, c_dbl, c_i64 = ctypes.c_int, ctypes.c_double, ctypes.c_int64
-        lib.kda_ref_forward.argtypes = [c_int, i64, c_int, c_int, c_int, c_dbl, d, d, d, d, d,
-                                        d, d, d, c_int]
-        lib.kda_ref_forward.restype = c_int
-        lib.kda_ref_package.argtypes = [c_int, i64, c_int, c_int, c_int, d, d, d, d, d, d,
-                                        c_int]
-        lib.kda_ref_package.restype = c_int
-        lib.kda_ref_compose.argtypes = [c_int, c_int, d, d, d, d, d, d]
-        lib.kda_ref_compose.restype = None
-        lib.kda_ref_scan.argtypes = [c_int, i64, c_int, c_int, c_int, d, d, d, d, d, c_int]
-        lib.kda_ref_scan.restype = c_int
-        lib.kda_ref_decode.argtypes = [c_int, c_int, c_int, c_int, c_dbl, d, d, d, d, d, i64,
-                                       d, c_i64, d, c_int]
-        lib.kda_ref_decode.restype = c_int
-        lib.kda_ref_decode_window.argtypes = [c_int, c_int, c_int, c_int, c_int, c_dbl, d, d, d,
-                                              d, d, c_int, i64, i64, d, c_i64, d, c_int]
-        lib.kda_ref_decode_window.restype = c_int
-        lib.kda_ref_short_conv.argtypes = [c_int, i64, c_int, c_int, d, d, c_int, i64, i64, d,
-                                           c_i64, d, c_int]
-        lib.kda_ref_short_conv.restype = c_int
-        _lib = lib
+        _lib = _bind(ctypes.CDLL(_build.build()))
     return _lib
+
+
+def _bind(lib):
+    """Declares the C signatures of the oracle's entry points on a loaded library."""
+    d = ctypes.POINTER(ctypes.c_double)
+    i64 = ctypes.POINTER(ctypes.c_int64)
+    c_int, c_dbl, c_i64 = ctypes.c_int, ctypes.c_double, ctypes.c_int64
+    lib.kda_ref_forward.argtypes = [c_int, i64, c_int, c_int, c_int, c_dbl, d, d, d, d, d,
+                                    d, d, d, c_int]
+    lib.kda_ref_forward.restype = c_int
+    lib.kda_ref_package.argtypes = [c_int, i64, c_int, c_int, c_int, d, d, d, d, d, d,
+                                    c_int]
+    lib.kda_ref_package.restype = c_int
+    lib.kda_ref_compose.argtypes = [c_int, c_int, d, d, d, d, d, d]
+    lib.kda_ref_compose.restype = None
+    lib.kda_ref_scan.argtypes = [c_int, i64, c_int, c_int, c_int, d, d, d, d, d, c_int]
+    lib.kda_ref_scan.restype = c_int
+    lib.kda_ref_decode.argtypes = [c_int, c_int, c_int, c_int, c_dbl, d, d, d, d, d, i64,
+                                   d, c_i64, d, c_int]
+    lib.kda_ref_decode.restype = c_int
+    lib.kda_ref_decode_window.argtypes = [c_int, c_int, c_int, c_int, c_int, c_dbl, d, d, d,
+                                          d, d, c_int, i64, i64, d, c_i64, d, c_int]
+    lib.kda_ref_decode_window.restype = c_int
+    lib.kda_ref_short_conv.argtypes = [c_int, i64, c_int, c_int, d, d, c_int, i64, i64, d,
+                                       c_i64, d, c_int]
+    lib.kda_ref_short_conv.restype = c_int
+    return lib
 
 
 def _f64(x):

@@ -13,17 +13,22 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libkda_oracle.so")
 
 
+def compile_source(src: str, out: str) -> str:
+    """Compiles one oracle source file into a shared library at `out` (the flags above)."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
+           "-fno-fast-math", "-ffp-contract=off", src, "-o", tmp]
+    subprocess.check_call(cmd)
+    os.replace(tmp, out)
+    return out
+
+
 def build(force: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     if (not force and os.path.exists(LIB)
             and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
-    cmd = ["g++", "-O2", "-std=c++17", "-fPIC", "-shared", "-pthread",
-           "-fno-fast-math", "-ffp-contract=off", SRC, "-o", tmp]
-    subprocess.check_call(cmd)
-    os.replace(tmp, LIB)
-    return LIB
+    return compile_source(SRC, LIB)
 
 
 if __name__ == "__main__":
