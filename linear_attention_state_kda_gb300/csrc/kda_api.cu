@@ -373,7 +373,6 @@ kda_status kda_short_conv(kda_dtype dt, int n_seqs, int total_tokens, const int3
                           unsigned flags, const int32_t* read_slots, const int32_t* write_slots,
                           void* conv_state, int64_t n_slots, void* out, uint32_t* status,
                           kda_stream_t stream) {
-  const char* fn = "kda_short_conv";
   KDA_REQUIRE(dt == KDA_F32 || dt == KDA_BF16, KDA_ERR_UNSUPPORTED,
               "kda_short_conv: dtype must be KDA_F32 or KDA_BF16");
   KDA_REQUIRE(width >= 1 && width <= 4, KDA_ERR_UNSUPPORTED,
@@ -399,7 +398,6 @@ kda_status kda_short_conv(kda_dtype dt, int n_seqs, int total_tokens, const int3
                   aligned(write_slots, 4) && aligned(status, 4),
               KDA_ERR_INVALID_ARG, "kda_short_conv: misaligned pointer");
   KDA_REQUIRE(!(x && x == out), KDA_ERR_INVALID_ARG, "kda_short_conv: out must not alias x");
-  (void)fn;
   return launch_short_conv(dt, n_seqs, total_tokens, cu_seqlens, channels, width, x, weight,
                            flags, slots ? read_slots : nullptr, slots ? write_slots : nullptr,
                            conv_state, slots ? n_slots : 0, out, status, (cudaStream_t)stream);
