@@ -5,7 +5,11 @@ One step = one pass of every hot-path call over synthetic inputs already residen
   * the segment path on the same inputs split into 8 segments of 2048 tokens:
     kda_chunk_prepare (per-chunk records, once) -> kda_segment_package_prepared ->
     kda_package_scan -> kda_segment_replay_prepared;
+  * kda_chunk_prefill and the same segment path on the long varlen workload (4 sequences of
+    131072, 65536, 32768 and 8192 tokens with entry states; 44 leveled segments);
   * kda_decode_step    on 256 rows x 32 heads over a 4096-slot fp32 pool (8.6 GB).
+After the timed steps, decode is also timed over 1000 back-to-back steps (the decode
+workload's own definition), and the slot-table extensions each on their own.
 `value` is the headline metric: prefill tokens per second of kda_chunk_prefill on the 16k
 workload, from CUDA events around that call in each timed step; the other calls are reported
 under "components" (tokens/s, achieved GB/s against the measured HBM peak). Every input is
@@ -39,8 +43,28 @@ DECODE_BYTES_PER_ROW_HEAD = 2 * STATE_BYTES + 3 * D * 2 + D * 4 + 4 + D * 2
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one prefill_16k launch, from the
-# ncu capture summarised in profiles/ (None until a capture of the current kernel exists).
+# ncu capture summarised in profiles/, and the SHA-256 prefix of the chunk kernels' source it
+# was taken on: once that source changes the figure no longer describes the kernel that runs,
+# and the roofline object reports traffic as null until a new capture replaces both.
 TRAFFIC_PREFILL_16K = 1852.0e6  # 4 x 463.0 MB on the 4096-token case (traffic scales with tokens)
+TRAFFIC_SOURCE_SHA = "unset"
+CHUNK_SOURCE = os.path.join(ROOT, "linear_attention_state_kda_gb300", "csrc", "kda_chunk_tc.cu")
+
+
+def _traffic_prefill():
+    import hashlib
+    with open(CHUNK_SOURCE, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    return (TRAFFIC_PREFILL_16K if sha == TRAFFIC_SOURCE_SHA else None), sha
+
+
+WORKLOAD = ("prefill_16k: H=32, T=16384, dk=dv=128, chunk 64, bf16 q/k/v, fp32 g/beta/state "
+            "(the headline); the step also runs segments_8x2048, varlen_long (4 sequences, "
+            "237,568 tokens, single pass and 44 leveled segments) and decode_256 (256 rows x "
+            "H32 over a 4096-slot pool)")
+CONFIG = {"workload": WORKLOAD,
+          "value_is": "tokens/s of kda_chunk_prefill on prefill_16k per GPU x n_gpus",
+          "l2": "inputs larger than L2; no flush"}
 
 
 def _peaks():
@@ -164,6 +188,27 @@ def run_gb300(args):
     ws_seg = torch.empty(kda.chunk_workspace(torch.bfloat16, P, T, H, D, D), dtype=torch.uint8,
                          device=dev)
     od = torch.empty_like(dec.v)
+    # the long varlen workload: 4 packed sequences with entry states, single pass and the
+    # leveled segment path (one workspace serves both, used one after the other)
+    xv = inputs.make_workload("varlen_long", device=dev)
+    Tv = xv.T
+    segs_v = inputs.workload_segments("varlen_long")
+    offs_v, sso_v = inputs.segment_offsets(xv.lens, segs_v)
+    offs_v, sso_v = offs_v.to(dev), sso_v.to(dev)
+    Nv, Pv = len(xv.lens), offs_v.numel() - 1
+    max_segs_v = max(len(sg) for sg in segs_v)
+    ov = torch.empty_like(xv.v)
+    finv = torch.empty(Nv, H, D, D, device=dev)
+    Mv = torch.empty(Pv, H, D, D, device=dev)
+    Dv = torch.empty(Pv, H, D, D, device=dev)
+    siv = torch.empty(Pv, H, D, D, device=dev)
+    finv2 = torch.empty(Nv, H, D, D, device=dev)
+    ov2 = torch.empty_like(xv.v)
+    ws_v = torch.empty(max(kda.chunk_workspace(torch.bfloat16, Nv, Tv, H, D, D),
+                           kda.chunk_workspace(torch.bfloat16, Pv, Tv, H, D, D)),
+                       dtype=torch.uint8, device=dev)
+    ws_vs = torch.empty(kda.package_scan_workspace(Nv, max_segs_v, H, D, D), dtype=torch.uint8,
+                        device=dev)
     stream = torch.cuda.current_stream()
 
     def prefill():
@@ -182,9 +227,25 @@ def run_gb300(args):
     def decode():
         kda.decode_step(dec.q, dec.k, dec.v, dec.g, dec.beta, dec.slot_ids, dec.pool, o=od)
 
-    # the segment path is package -> scan -> replay; each call is timed on its own too
+    def varlen():
+        kda.chunk_prefill(xv.q, xv.k, xv.v, xv.g, xv.beta, cu_seqlens=xv.cu_seqlens,
+                          init_state=xv.init_state, o=ov, final_state=finv, workspace=ws_v)
+
+    def varlen_package():
+        kda.chunk_prepare(xv.q, xv.k, xv.v, xv.g, xv.beta, offs_v, workspace=ws_v)
+        kda.segment_package_prepared(ws_v, offs_v, Tv, H, D, D, M=Mv, D=Dv)
+
+    def varlen_scan():
+        kda.package_scan(Mv, Dv, sso_v, max_segs_v, init_state=xv.init_state, seg_init=siv,
+                         final_state=finv2, workspace=ws_vs)
+
+    def varlen_replay():
+        kda.segment_replay_prepared(ws_v, offs_v, siv, Tv, H, D, D, o=ov2)
+
+    # the segment paths are package -> scan -> replay; each call is timed on its own too
     parts = [("prefill_16k", prefill), ("seg_package", package), ("seg_scan", scan),
-             ("seg_replay", replay), ("decode_256", decode)]
+             ("seg_replay", replay), ("varlen_long", varlen), ("vseg_package", varlen_package),
+             ("vseg_scan", varlen_scan), ("vseg_replay", varlen_replay), ("decode_256", decode)]
     for _ in range(args.warmup):
         for _, fn in parts:
             fn()
@@ -220,6 +281,22 @@ def run_gb300(args):
         comp_ms[n] = red[1 + i]
     comp_ms["segments_8x2048"] = (comp_ms["seg_package"] + comp_ms["seg_scan"] +
                                   comp_ms["seg_replay"])
+    comp_ms["varlen_long_segments"] = (comp_ms["vseg_package"] + comp_ms["vseg_scan"] +
+                                       comp_ms["vseg_replay"])
+
+    # decode as the workload states it: 1000 back-to-back steps over the same batch (the
+    # states keep evolving), one event pair around all of them
+    n_dec = 1000
+    d0, d1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches_dec0 = kda.launch_count()
+    torch.cuda._sleep(int(4e7))
+    d0.record(stream)
+    for _ in range(n_dec):
+        decode()
+    d1.record(stream)
+    torch.cuda.synchronize()
+    launches_dec = kda.launch_count() - launches_dec0
+    dec1000_ms = max_over_ranks([d0.elapsed_time(d1) / n_dec])[0]
 
     hbm = peaks["hbm_gbs"]
     pf_bytes = T * H * PREFILL_BYTES_PER_TOKEN_HEAD + H * STATE_BYTES
@@ -228,6 +305,15 @@ def run_gb300(args):
                  + P * H * 2 * STATE_BYTES + P * H * STATE_BYTES + H * STATE_BYTES  # scan
                  + T * H * PREFILL_BYTES_PER_TOKEN_HEAD + P * H * STATE_BYTES)     # replay
     dec_bytes = B * H * DECODE_BYTES_PER_ROW_HEAD + B * 4
+    # varlen_long: every token's inputs read and output written once, plus the entry states
+    # read and the exit states written; its segment path adds the package pass (k, v, g, beta
+    # read, packages written), the scan (packages and entry states read, segment entry states
+    # and exit states written) and the replay's segment entry states
+    v_pf_bytes = Tv * H * PREFILL_BYTES_PER_TOKEN_HEAD + 2 * Nv * H * STATE_BYTES
+    v_seg_bytes = (Tv * H * (2 * D * 2 + D * 4 + 4) + Pv * H * 2 * STATE_BYTES
+                   + Pv * H * 2 * STATE_BYTES + Nv * H * STATE_BYTES + Pv * H * STATE_BYTES
+                   + Nv * H * STATE_BYTES
+                   + Tv * H * PREFILL_BYTES_PER_TOKEN_HEAD + Pv * H * STATE_BYTES)
     comps = {
         "prefill_16k": dict(ms=comp_ms["prefill_16k"],
                             tokens_per_s=T / (comp_ms["prefill_16k"] * 1e-3),
@@ -239,17 +325,32 @@ def run_gb300(args):
                                 gbs=seg_bytes / (comp_ms["segments_8x2048"] * 1e-3) / 1e9,
                                 package_ms=comp_ms["seg_package"], scan_ms=comp_ms["seg_scan"],
                                 replay_ms=comp_ms["seg_replay"]),
+        "varlen_long": dict(ms=comp_ms["varlen_long"],
+                            tokens_per_s=Tv / (comp_ms["varlen_long"] * 1e-3),
+                            algorithmic_bytes=v_pf_bytes,
+                            gbs=v_pf_bytes / (comp_ms["varlen_long"] * 1e-3) / 1e9),
+        "varlen_long_segments": dict(
+            ms=comp_ms["varlen_long_segments"],
+            tokens_per_s=Tv / (comp_ms["varlen_long_segments"] * 1e-3),
+            algorithmic_bytes=v_seg_bytes,
+            gbs=v_seg_bytes / (comp_ms["varlen_long_segments"] * 1e-3) / 1e9,
+            package_ms=comp_ms["vseg_package"], scan_ms=comp_ms["vseg_scan"],
+            replay_ms=comp_ms["vseg_replay"], segments=Pv),
         "decode_256": dict(ms=comp_ms["decode_256"], algorithmic_bytes=dec_bytes,
                            gbs=dec_bytes / (comp_ms["decode_256"] * 1e-3) / 1e9),
+        "decode_256_x1000": dict(ms=dec1000_ms, steps=n_dec, launches=int(launches_dec),
+                                 algorithmic_bytes=dec_bytes,
+                                 gbs=dec_bytes / (dec1000_ms * 1e-3) / 1e9),
     }
     for c in comps.values():
         c["hbm_frac"] = c["gbs"] / hbm
     # dominant kernel: the longest single launch of the step, the prefill call (one fused
     # cooperative launch on this workload): algorithmic bytes of the call over its duration
+    traffic, chunk_sha = _traffic_prefill()
     roofline = {"bound": "hbm", "achieved": round(comps["prefill_16k"]["gbs"], 1), "peak": hbm,
                 "unit": "GB/s", "frac": round(comps["prefill_16k"]["gbs"] / hbm, 4),
-                "traffic": TRAFFIC_PREFILL_16K, "kernel": "prefill_16k (chunk_fused_kernel)",
-                "peak_source": peaks["source"]}
+                "traffic": traffic, "kernel": "prefill_16k (chunk_fused_kernel)",
+                "kernel_source_sha": chunk_sha, "peak_source": peaks["source"]}
 
     # The extensions, timed on their own after the step (each over its own CUDA events, the
     # same number of iterations): a 4-token verify window per row with forked read slots and
@@ -393,11 +494,7 @@ def run_gb300(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded; q,v~N(0,1), k L2-normalised, g=-softplus(N(0,1)), "
                 "beta=sigmoid(N(0,1)))",
-        "config": {"workload": "prefill_16k: H=32, T=16384, dk=dv=128, chunk 64, bf16 q/k/v, "
-                               "fp32 g/beta/state; step also runs segments_8x2048 and "
-                               "decode_256 (256 rows x H32 over a 4096-slot pool)",
-                   "value_is": "tokens/s of kda_chunk_prefill per GPU x n_gpus",
-                   "l2": "inputs larger than L2; no flush", "parallelism": f"replicas{world}"},
+        "config": dict(CONFIG, parallelism=f"replicas{world}"),
         "components": {k: {kk: (round(vv, 4) if isinstance(vv, float) else vv)
                            for kk, vv in v.items()} for k, v in comps.items()},
         "roofline": roofline,
@@ -462,7 +559,7 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": None, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "impl": "reference",
-        "config": {"workload": "prefill_16k (sampled heads)", "parallelism": "cpu"},
+        "config": dict(CONFIG, parallelism=f"replicas{world}"),
         "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
                          "cores": per[-1]["cores"], "sample": per[-1]["sample"]},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,

@@ -110,6 +110,10 @@ KDA_API size_t kda_chunk_workspace(kda_dtype dt, int n_ranges, int total_tokens,
  *               dk, dv) bytes, 256-byte aligned, contents need not be initialised; may be
  *               NULL when that query returns 0 (KDA_ERR_WORKSPACE otherwise).
  *   status      optional device word (KDA_STATUS_DECAY_RANGE).
+ * q, k, v, g, beta, o and the states must be 16-byte aligned (KDA_ERR_INVALID_ARG otherwise).
+ * A shape whose workspace query is positive runs on the tensor-core kernels and on nothing
+ * else: if the CUDA driver does not provide cuTensorMapEncodeTiled, the call returns
+ * KDA_ERR_UNSUPPORTED. The same holds for every chunked call below.
  * Source: the chunked FlashKDA prefill of kern PR #44 (varlen build with cu_seqlens and
  * per-sequence state blocks) and pegainfer PR #970 (fabric data-plane commit message: the
  * segment replay runs the same per-chunk step as the prefill).
@@ -128,6 +132,7 @@ KDA_API kda_status kda_chunk_prefill(kda_dtype dt, int n_seqs, int total_tokens,
  * M S_in + D. No outputs o are produced and q is not read.
  *   seg_offsets device int32 [n_segs + 1].
  *   workspace   as for kda_chunk_prefill, sized by kda_chunk_workspace(dt, n_segs, ...).
+ *   k, v, g, beta, M and D 16-byte aligned.
  * Source: pegainfer PR #970, fabric data-plane commit message (the (M,D) package each
  * context-parallel member publishes for its segment).
  */
@@ -176,9 +181,11 @@ KDA_API kda_status kda_package_scan(int n_seqs, int n_segs, const int32_t* seq_s
  *   kda_package_scan_workspace(...) exceeds 64 MiB returns KDA_ERR_WORKSPACE (use
  *   kda_package_scan then). The call allocates nothing (no cudaMalloc or cudaFree).
  *   The first call on a device looks up the array's device address with that device
- *   current; make it before any stream capture. All calls share the one array and it keeps
- *   the last call's contents (the scan writes all scratch it reads, so no clearing is needed);
- *   calls that overlap on the GPU race on it.
+ *   current; make it before any stream capture. The address is kept for the life of the
+ *   process: do not call this entry point again after a cudaDeviceReset. All calls share
+ *   the one array and it keeps the last call's contents (the scan writes all scratch it
+ *   reads, so no clearing is needed); calls that overlap on the GPU race on it. Errors are
+ *   reported under this entry point's name.
  */
 KDA_API kda_status kda_package_scan_noalloc(int n_seqs, int n_segs,
                                             const int32_t* seq_seg_offsets,

@@ -51,16 +51,19 @@ size_t chunk_workspace(kda_dtype dt, int n_ranges, int total_tokens, int H, int 
   return chunk_tc_workspace_bytes(n_ranges, total_tokens, H);
 }
 
+// A shape with a positive workspace query runs on the tensor-core kernels and nowhere else:
+// if they cannot run (the driver lacks the tensor-map encoder), the call fails.
 kda_status chunked(const char* fn, const ChunkParams& p, kda_dtype dt, void* ws, size_t ws_bytes,
                    cudaStream_t s) {
   const size_t need = chunk_workspace(dt, p.n_ranges, p.total_tokens, p.H, p.dk, p.dv);
-  if (need > 0) {
-    KDA_REQUIRE(ws && ws_bytes >= need && aligned(ws, 256), KDA_ERR_WORKSPACE,
-                std::string(fn) + ": workspace missing, too small or not 256-byte aligned (need " +
-                    std::to_string(need) + " bytes)");
-  }
-  if (chunk_tc_supported(p, dt)) return launch_chunk_tc(p, dt, ws, ws_bytes, s);
-  return launch_chunk_simt(p, dt, s);
+  if (need == 0) return launch_chunk_simt(p, dt, s);
+  KDA_REQUIRE(ws && ws_bytes >= need && aligned(ws, 256), KDA_ERR_WORKSPACE,
+              std::string(fn) + ": workspace missing, too small or not 256-byte aligned (need " +
+                  std::to_string(need) + " bytes)");
+  KDA_REQUIRE(chunk_tc_available(), KDA_ERR_UNSUPPORTED,
+              std::string(fn) + ": the CUDA driver does not provide cuTensorMapEncodeTiled, "
+                                "which the tensor-core path needs");
+  return launch_chunk_tc(p, dt, ws, ws_bytes, s);
 }
 
 }  // namespace
@@ -96,12 +99,11 @@ kda_status kda_chunk_prefill(kda_dtype dt, int n_seqs, int total_tokens,
   if (n_seqs == 0) return KDA_OK;
   KDA_REQUIRE(total_tokens == 0 || (q && k && v && g && beta && o), KDA_ERR_INVALID_ARG,
               "kda_chunk_prefill: q, k, v, g, beta and o must be non-null");
-  const size_t es = dt == KDA_BF16 ? 2 : 4;
   KDA_REQUIRE(aligned(q, 16) && aligned(k, 16) && aligned(v, 16) && aligned(o, 16) &&
-                  aligned(g, 16) && aligned(beta, 4) && aligned(init_state, 16) &&
+                  aligned(g, 16) && aligned(beta, 16) && aligned(init_state, 16) &&
                   aligned(final_state, 16) && aligned(cu_seqlens, 4) && aligned(status, 4),
-              KDA_ERR_INVALID_ARG, "kda_chunk_prefill: pointers must be 16-byte aligned");
-  (void)es;
+              KDA_ERR_INVALID_ARG,
+              "kda_chunk_prefill: q, k, v, g, beta, o and the states must be 16-byte aligned");
   ChunkParams p{};
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
   p.offsets = cu_seqlens; p.n_ranges = n_seqs; p.total_tokens = total_tokens;
@@ -126,10 +128,11 @@ kda_status kda_segment_package(kda_dtype dt, int n_segs, int total_tokens,
               "kda_segment_package: seg_offsets, M and D must be non-null");
   KDA_REQUIRE(total_tokens == 0 || (k && v && g && beta), KDA_ERR_INVALID_ARG,
               "kda_segment_package: k, v, g and beta must be non-null");
-  KDA_REQUIRE(aligned(k, 16) && aligned(v, 16) && aligned(g, 16) && aligned(beta, 4) &&
+  KDA_REQUIRE(aligned(k, 16) && aligned(v, 16) && aligned(g, 16) && aligned(beta, 16) &&
                   aligned(M, 16) && aligned(D, 16) && aligned(seg_offsets, 4) &&
                   aligned(status, 4),
-              KDA_ERR_INVALID_ARG, "kda_segment_package: pointers must be 16-byte aligned");
+              KDA_ERR_INVALID_ARG,
+              "kda_segment_package: k, v, g, beta, M and D must be 16-byte aligned");
   ChunkParams p{};
   p.k = k; p.v = v; p.g = g; p.beta = beta;
   p.offsets = seg_offsets; p.n_ranges = n_segs; p.total_tokens = total_tokens;

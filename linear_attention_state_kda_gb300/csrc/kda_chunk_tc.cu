@@ -1329,10 +1329,7 @@ size_t chunk_tc_workspace_bytes(int n_ranges, int total_tokens, int H) {
   return items * kItemBytes + ((items * 4 + 255) & ~(size_t)255);  // records, then flags
 }
 
-bool chunk_tc_supported(const ChunkParams& p, kda_dtype dt) {
-  return chunk_tc_shape_ok(dt, p.n_ranges, p.total_tokens, p.H, p.dk, p.dv) &&
-         ((uintptr_t)p.beta % 16) == 0 && encode_fn() != nullptr;
-}
+bool chunk_tc_available() { return encode_fn() != nullptr; }
 
 kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, size_t ws_bytes,
                            cudaStream_t s, int phases) {

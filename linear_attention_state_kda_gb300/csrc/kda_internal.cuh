@@ -62,10 +62,11 @@ kda_status launch_chunk_simt(const ChunkParams& p, kda_dtype dt, cudaStream_t s)
 // Tensor-core (tcgen05/TMEM/TMA) chunk path for bf16 inputs with dk = dv = 128: a parallel
 // per-(chunk, head) prep kernel writing workspace records, then the in-order state kernel.
 // chunk_tc_shape_ok decides from shapes alone whether the path (and so the workspace)
-// applies; chunk_tc_supported also checks the pointers.
+// applies; chunk_tc_available tells whether the driver provides the tensor-map encoder the
+// path needs.
 bool chunk_tc_shape_ok(kda_dtype dt, int n_ranges, int total_tokens, int H, int dk, int dv);
 size_t chunk_tc_workspace_bytes(int n_ranges, int total_tokens, int H);
-bool chunk_tc_supported(const ChunkParams& p, kda_dtype dt);
+bool chunk_tc_available();
 // phases: kPhasePrep writes the records, kPhaseState walks them; both = one chunked call.
 constexpr int kPhasePrep = 1, kPhaseState = 2;
 kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, size_t ws_bytes,

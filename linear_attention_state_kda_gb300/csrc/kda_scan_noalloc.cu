@@ -18,6 +18,8 @@
 // The device address of the array is looked up once per device, on the first call made with
 // that device current (host code cannot pass the array's name to a kernel: in host code the
 // name is a stand-in, not a device address). Make that first call before any stream capture.
+// The cached address belongs to the device's current context: after cudaDeviceReset the
+// array lives at a new address and this entry point must not be called again in that process.
 #include <mutex>
 #include <string>
 
@@ -86,7 +88,14 @@ extern "C" KDA_API kda_status kda_package_scan_noalloc(
   void* ws = nullptr;
   kda_status st = scratch_address(&ws);
   if (st != KDA_OK) return st;
-  return kda_package_scan(n_seqs, n_segs, seq_seg_offsets, max_segs_per_seq, H, dk, dv, M, D,
-                          init_state, seg_init, final_state, ws, kNoAllocScratchBytes, status,
-                          stream);
+  st = kda_package_scan(n_seqs, n_segs, seq_seg_offsets, max_segs_per_seq, H, dk, dv, M, D,
+                        init_state, seg_init, final_state, ws, kNoAllocScratchBytes, status,
+                        stream);
+  if (st != KDA_OK) {  // report the failure under this entry point's name
+    std::string m = kda_last_error();
+    const std::string inner = "kda_package_scan";
+    if (m.rfind(inner, 0) == 0) m = std::string(fn) + m.substr(inner.size());
+    return set_error(st, m);
+  }
+  return st;
 }

@@ -185,3 +185,23 @@ def test_short_conv_checks(L):
     assert conv(out=p) == kda.KDA_ERR_INVALID_ARG              # out aliases x
     assert conv(x=None) == kda.KDA_ERR_INVALID_ARG
     assert conv(n=0) == kda.KDA_OK                             # nothing to do launches nothing
+
+
+def test_beta_alignment_fails_loudly(L):
+    """beta offset by 4 bytes (a view one head into a [T, H] array, say) is rejected before
+    any launch, on the tensor-core shapes and the CUDA-core ones alike: no call quietly runs
+    another implementation."""
+    from linear_attention_state_kda_gb300 import kda
+    p, pb = 4096, 4096 + 4
+    need = kda.chunk_workspace(torch.bfloat16, 1, 64, 4, 128, 128)
+    assert need > 0
+    for H, ws, nb in [(4, p, need), (2, None, 0)]:
+        assert L.kda_chunk_prefill(1, 1, 64, None, H, 128, 128, 64, 1.0, p, p, p, p, pb, None,
+                                   p, None, ws, nb, None, None) == kda.KDA_ERR_INVALID_ARG
+        assert "beta" in kda.last_error()
+        assert L.kda_segment_package(1, 1, 64, p, H, 128, 128, 64, p, p, p, pb, p, p, ws, nb,
+                                     None, None) == kda.KDA_ERR_INVALID_ARG
+        assert "beta" in kda.last_error()
+        assert L.kda_segment_replay(1, 1, 64, p, H, 128, 128, 64, 1.0, p, p, p, p, pb, None, p,
+                                    None, ws, nb, None, None) == kda.KDA_ERR_INVALID_ARG
+        assert kda.last_error().startswith("kda_segment_replay")
