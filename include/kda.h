@@ -6,6 +6,9 @@
  *     S_t = (I - beta_t k_t k_t^T) Diag(a_t) S_{t-1} + beta_t k_t v_t^T,   a_t = exp(g_t)
  *     o_t = scale * S_t^T q_t
  * g_t in R^{dk} is a per-key-channel log-decay (g <= 0), beta_t a scalar write strength.
+ * Every call accepts any g <= 0: the chunked calls compute a channel that decays by more than
+ * 160 nats within one 64-token chunk without the chunk's shared exponent frame, so no decay
+ * is too strong (results match the recurrence up to rounding).
  * This is the KDA linear-attention state that pegainfer PR #970 ("feat(k3): cross-process
  * CP whale gang - fleet-wide long-prompt prefill") prefills with FlashKDA per context-parallel
  * segment; each segment publishes its (M,D) package, and the packages are combined by an
@@ -67,9 +70,7 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype; /* dtype of q, k, v and o 
 
 /* Bits OR-ed into the optional device status word. */
 #define KDA_STATUS_BAD_SLOT 1u    /* decode: a slot id >= n_slots was skipped */
-#define KDA_STATUS_DECAY_RANGE 2u /* prefill/package/replay: within one 64-token chunk some
-                                     key channel decayed by more than 160 nats (sum of -g over
-                                     the chunk > 160); results for that chunk are unreliable */
+/* (bit 2u is not used) */
 #define KDA_STATUS_BAD_OFFSETS 4u /* an offset array was decreasing or out of range, or a
                                      sequence had more segments than max_segs_per_seq; the
                                      offending range was treated as empty */
@@ -109,7 +110,7 @@ KDA_API size_t kda_chunk_workspace(kda_dtype dt, int n_ranges, int total_tokens,
  *   workspace   device scratch of at least kda_chunk_workspace(dt, n_seqs, total_tokens, H,
  *               dk, dv) bytes, 256-byte aligned, contents need not be initialised; may be
  *               NULL when that query returns 0 (KDA_ERR_WORKSPACE otherwise).
- *   status      optional device word (KDA_STATUS_DECAY_RANGE).
+ *   status      optional device word (KDA_STATUS_BAD_OFFSETS, KDA_STATUS_TIMEOUT).
  * q, k, v, g, beta, o and the states must be 16-byte aligned (KDA_ERR_INVALID_ARG otherwise).
  * A shape whose workspace query is positive runs on the tensor-core kernels and on nothing
  * else: if the CUDA driver does not provide cuTensorMapEncodeTiled, the call returns
@@ -220,7 +221,7 @@ KDA_API kda_status kda_segment_replay(kda_dtype dt, int n_segs, int total_tokens
  *   workspace  at least kda_chunk_workspace(dt, n_ranges, total_tokens, H, dk, dv) bytes,
  *              256-byte aligned; the tensor-core shapes only (that query > 0), others return
  *              KDA_ERR_UNSUPPORTED.
- *   beta       16-byte aligned. status: optional device word (KDA_STATUS_DECAY_RANGE).
+ *   beta       16-byte aligned. status: optional device word (KDA_STATUS_TIMEOUT).
  * The pages have no separate counterpart: their context-parallel members prepare a segment
  * once and both publish its package and replay it with the same per-chunk step (pegainfer
  * PR #970, fabric data-plane commit message).

@@ -11,9 +11,14 @@
 //   A_kk[r,i] = beta_r Kh_r . Kb_i  (i < r),     A_qk[r,i] = Qh_r . Kb_i  (i <= r)
 //   T = (I + A_kk)^-1,  W = T diag(beta) Kh,  Ut = T diag(beta) V
 //   Sh = Diag(exp(rho)) S_0            (the chunk's state in the midpoint frame)
-//   U = Ut - W Sh,   O = scale (Qh Sh + A_qk U),   S_C = Diag(exp(gamma_C - rho)) (Sh + Kb^T U)
-// Every exponent stays within +-|gamma_C|/2, so a chunk whose channels decay by at most
-// 160 nats never overflows fp32; beyond that KDA_STATUS_DECAY_RANGE is raised.
+//   U = Ut - W Sh,   O = scale (Qh Sh + A_qk U),
+//   S_C = Diag(exp(gamma_C - rho)) Sh + Kb'^T U,   Kb'_r = k_r * exp(gamma_C - gamma_r)
+// Every exponent stays within +-|gamma_C|/2, so a channel that decays by at most 160 nats
+// over the chunk never overflows fp32. A channel that decays more ("strong") takes rho = 0
+// and Kb = 0, so it has no share in the Kh Kb^T products; its share of A_kk and A_qk is added
+// exactly, each pairwise factor exp(gamma_r - gamma_i) = a_{i+1} ... a_r built as a product
+// of the per-token decays a = exp(g) <= 1 (no overflow, and no loss to the cancellation of
+// large cumulative sums). Kb' comes from suffix sums of g for the same reason.
 //
 // A CTA owns one (range, head, 32-column tile) and walks the range's chunks in order; the
 // tile's state columns stay in shared memory. Columns are independent in the recurrence, so
@@ -32,7 +37,7 @@ constexpr int kThreads = 256;
 template <int DK>
 constexpr size_t simt_smem_floats() {
   return (size_t)4 * C * (DK + 1) + 3 * (size_t)C * LC + 2 * (size_t)C * LT +
-         (size_t)DK * LT + 2 * DK + C;
+         (size_t)DK * LT + 3 * DK + C;
 }
 
 template <int DK, class T>
@@ -53,6 +58,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(ChunkParams p) 
   float* rho = Ss + DK * LT;      // [DK]
   float* gC = rho + DK;           // [DK]
   float* bs = gC + DK;            // [C]
+  int* strong = reinterpret_cast<int*>(bs + C);  // [DK] channel decays beyond the frame
 
   const int tid = threadIdx.x;
   const int tile = blockIdx.x, h = blockIdx.y, sidx = blockIdx.z;
@@ -99,6 +105,7 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(ChunkParams p) 
     }
     __syncthreads();
     // ---- cumulative log-decay per channel
+    bool my_strong = false;
     if (tid < DK) {
       float acc = 0.0f;
       for (int r = 0; r < C; ++r) {
@@ -106,19 +113,20 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(ChunkParams p) 
         Gw[r * LDK + tid] = acc;
       }
       gC[tid] = acc;
-      rho[tid] = 0.5f * acc;
-      if (!(acc >= -kMaxChunkDecay) && p.status) atomicOr(p.status, KDA_STATUS_DECAY_RANGE);
+      my_strong = !(acc >= -kMaxChunkDecay);
+      strong[tid] = my_strong;
+      rho[tid] = my_strong ? 0.0f : 0.5f * acc;
     }
-    __syncthreads();
+    const bool any_strong = __syncthreads_or(my_strong) != 0;
     // ---- midpoint-frame operands and the state in the midpoint frame
     for (int idx = tid; idx < C * DK; idx += kThreads) {
       const int r = idx / DK, c = idx - r * DK;
       const float x = Gw[r * LDK + c] - rho[c];
-      const float e1 = expf(x), e2 = expf(-x);
+      const float e1 = expf(x);
       const int64_t e = ((int64_t)(t0 + r) * H + h) * DK + c;
       const float kv = (r < n) ? ld_elem(k, e) : 0.0f;
       Kh[r * LDK + c] = kv * e1;
-      Kb[r * LDK + c] = kv * e2;
+      Kb[r * LDK + c] = strong[c] ? 0.0f : kv * expf(-x);
       if (!pkg) Qh[r * LDK + c] = ((r < n) ? ld_elem(q, e) : 0.0f) * e1;
     }
     for (int idx = tid; idx < DK * TW; idx += kThreads) {
@@ -140,6 +148,39 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(ChunkParams p) 
       Akk[r * LC + i] = (i < r) ? bs[r] * akk : 0.0f;
       Aqk[r * LC + i] = (i <= r) ? aqk : 0.0f;
       X[r * LC + i] = (i == r) ? 1.0f : 0.0f;
+    }
+    __syncthreads();
+    // ---- the strong channels' exact shares: thread r owns row r of A_kk and A_qk and runs
+    // i from r down to 0 with f = exp(gamma_r - gamma_i) = f(i + 1) * a_{i + 1}
+    if (any_strong) {
+      if (tid < n) {
+        const int r = tid;
+        for (int c = 0; c < DK; ++c) {
+          if (!strong[c]) continue;
+          const int64_t er = ((int64_t)(t0 + r) * H + h) * DK + c;
+          const float kr = ld_elem(k, er);
+          const float qr = pkg ? 0.0f : ld_elem(q, er);
+          float f = 1.0f;
+          for (int i = r; i >= 0; --i) {
+            const int64_t ei = ((int64_t)(t0 + i) * H + h) * DK + c;
+            const float ki = ld_elem(k, ei);
+            if (i < r) Akk[r * LC + i] = fmaf(bs[r] * kr * ki, f, Akk[r * LC + i]);
+            if (!pkg) Aqk[r * LC + i] = fmaf(qr * ki, f, Aqk[r * LC + i]);
+            f *= expf(p.g[ei]);
+          }
+        }
+      }
+      __syncthreads();
+    }
+    // ---- Kb' = k exp(gamma_C - gamma_r) (Kb is read no more): suffix sums of g per channel
+    if (tid < DK) {
+      float suf = 0.0f;  // gamma_C - gamma_r = sum of g over the chunk's tokens after r
+      for (int r = C - 1; r >= 0; --r) {
+        const int64_t e = ((int64_t)(t0 + r) * H + h) * DK + tid;
+        const bool valid = r < n;
+        Kb[r * LDK + tid] = valid ? ld_elem(k, e) * expf(suf) : 0.0f;
+        if (valid) suf += p.g[e];
+      }
     }
     __syncthreads();
     // ---- X = (I + A_kk)^-1 by right-looking forward substitution over columns l
@@ -193,12 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1) chunk_simt_kernel(ChunkParams p) 
       }
       __syncthreads();
     }
-    // ---- S_C = Diag(exp(gamma_C - rho)) (Sh + Kb^T U)
+    // ---- S_C = Diag(exp(gamma_C - rho)) Sh + Kb'^T U
     for (int idx = tid; idx < DK * TW; idx += kThreads) {
       const int c = idx / TW, j = idx - c * TW;
-      float acc = Ss[c * LT + j];
+      float acc = Ss[c * LT + j] * expf(gC[c] - rho[c]);
       for (int i = 0; i < C; ++i) acc = fmaf(Kb[i * LDK + c], Us[i * LT + j], acc);
-      Ss[c * LT + j] = acc * expf(gC[c] - rho[c]);
+      Ss[c * LT + j] = acc;
     }
   }
   __syncthreads();

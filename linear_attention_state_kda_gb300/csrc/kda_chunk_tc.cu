@@ -11,23 +11,30 @@
 //   K'  = k e^gamma,  Kb' = k e^(gamma_C - gamma),  W = TB K',  U0 = TB V
 //   Aqk = tril(Qh Kb^T)  (query-key products weighted by e^(gamma_t - gamma_i), i <= t)
 //   P   = Aqk TB,  Q'' = scale (q e^gamma - P K'),  O0 = scale P V
-// where Kh = k e^(gamma - rho), Qh = q e^(gamma - rho), Kb = k e^(rho - gamma) and
-// rho = gamma_C / 2: in this midpoint frame every factor stays within e^(+-80) as long as a
-// chunk decays by at most 160 nats per channel (beyond it KDA_STATUS_DECAY_RANGE is raised).
+// where Kh = k e^(gamma - rho), Qh = q e^(gamma - rho), Kb = k e^(rho - gamma) and, per
+// channel, rho = gamma_C / 2: in this midpoint frame every factor stays within e^(+-80) as long
+// as the channel decays by at most 160 nats over the chunk. A channel that decays more (a
+// "strong" channel) takes frame rho = 0 and no share in the Kh Kb^T product (its Kb is zero);
+// its share of A_kk and A_qk is added exactly on CUDA cores from pairwise factors
+// e^(gamma_t - gamma_i) <= 1, and its Kb' is formed directly. Every g <= 0 is thus exact up
+// to rounding; chunks without strong channels never enter that code.
 //
 // Kernel 1 (prep) computes the state-independent factors of every (chunk, head) in parallel
 // (persistent CTAs, one item at a time, the next item's loads in flight) and writes them to a
 // workspace record. Kernel 2 (state) walks each range's chunks in order for one (range, head,
-// 32-column tile of the state): per chunk one MMA for [W; Q''] S, the U update on CUDA cores,
-// one MMA for Kb'^T U, and the state update, with the records streamed in by TMA two chunks
-// ahead. In package mode kernel 2 runs the same chunks on a 32-column tile of the augmented
-// state [M | D] (identity / zero start; M columns see zero values) and writes no outputs.
+// 128-column tile of the state) with the transposed state S^T in TMEM: per chunk one N = 128
+// product X^T = S^T [W; Q'']^T, the U update and the outputs on CUDA cores, one N = 128
+// product Y^T = U^T Kb', and the state update, with the records streamed in by TMA two chunks
+// ahead. In package mode kernel 2 runs the same chunks on the M or the D half of the
+// augmented state [M | D] (identity / zero start; M columns see zero values) and writes no
+// outputs. A fused cooperative launch runs both kernels' work side by side for few walks.
 //
-// All MMAs are kind::tf32 with fp32 accumulation; every shared-memory operand is K-major in
-// the 128-byte swizzle, and operands needed in the other orientation are written transposed
-// by the threads that produce them or staged in TMEM. Waits on mbarriers are bounded (2 s of
-// globaltimer); on expiry a CTA raises KDA_STATUS_TIMEOUT, drains its own MMAs and copies
-// (bounded), frees its TMEM and returns.
+// MMAs are kind::tf32 with fp32 accumulation, except U0^T = V^T TB^T, a kind::f16 product of
+// the bf16 v staging (read MN-major) and TB split into bf16 hi and lo parts. Every other
+// shared-memory operand is K-major in the 128-byte swizzle; operands needed in the other
+// orientation are written transposed by the threads that produce them or staged in TMEM.
+// Waits on mbarriers are bounded (2 s of globaltimer); on expiry a CTA raises
+// KDA_STATUS_TIMEOUT, drains its own MMAs and copies (bounded), frees its TMEM and returns.
 #include <cuda.h>
 
 #include <algorithm>
@@ -172,6 +179,9 @@ struct PrepMisc {
   // published; item -1 ends the stream)
   int pub_ring[4];
   uint32_t pub_head, pub_tail;
+  // the item's strong channels (bit c % 32 of word c / 32): those whose decay over the chunk
+  // exceeds kMaxChunkDecay nats, which the midpoint frame cannot hold
+  uint32_t smask[4];
   // read with 16-byte vector loads
   alignas(16) float part[2][DK];
   alignas(16) float erho[DK];
@@ -319,12 +329,16 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       if (tid < C) misc->beta[tid] = (tid < n) ? f32at(sm, P_STG_B)[tid * 4 + (h & 3)] : 0.0f;
       pbar();
       const float p0 = misc->part[0][c], p1 = misc->part[1][c];
-      const float rho2 = 0.5f * (p0 + p1);  // log2 units
+      const float gsum = p0 + p1;  // gamma_C, log2 units
+      // A strong channel (decay over the chunk beyond kMaxChunkDecay nats) takes frame 0: it
+      // is left out of the A1 product and its share of A_kk / A_qk is computed exactly below.
+      const bool strong = !(gsum >= -kMaxChunkDecay * kLog2e);
+      const float rho2 = strong ? 0.0f : 0.5f * gsum;  // log2 units
       if (half == 0) {
         misc->erho[c] = ex2_approx(rho2);
-        ws.dec[(size_t)item * DK + c] = ex2_approx(p0 + p1);
-        if (!((p0 + p1) >= -kMaxChunkDecay * kLog2e) && p.status)
-          atomicOr(p.status, KDA_STATUS_DECAY_RANGE);
+        ws.dec[(size_t)item * DK + c] = ex2_approx(gsum);
+        const uint32_t m = __ballot_sync(0xffffffffu, strong);  // warps 0..3: channels 32 w ..
+        if (lane == 0) misc->smask[warp] = m;
       }
       // gamma - rho (log2 units) in place of g: each element has one owner
       float gam = half ? p0 : 0.0f;
@@ -336,6 +350,8 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     }
     if (tid == kLoader) bulk_wait_read1();  // the previous record's Q'' has left its staging
     pbar();
+    const uint32_t* smask = misc->smask;
+    const bool any_strong = (smask[0] | smask[1] | smask[2] | smask[3]) != 0u;
     // ================= operands (row role: token t; key rows in warps 0,1,4,5, query rows
     // in warps 2,3,6,7; channel half chh)
     {
@@ -365,10 +381,28 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       };
       auto kb_out = [&](int c0, const float* x, const float* kv, const float* er) {
         float kb[8];
+        if (!any_strong) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          kb[e] = (valid ? kv[e] : 0.0f) * ex2_approx(-x[e]);
-          kbt_out[(size_t)(c0 + e) * C] = kb[e] * er[e];
+          for (int e = 0; e < 8; ++e) {
+            kb[e] = (valid ? kv[e] : 0.0f) * ex2_approx(-x[e]);
+            kbt_out[(size_t)(c0 + e) * C] = kb[e] * er[e];
+          }
+        } else {
+          // a strong channel has no share in the A1 product (Kb = 0); its Kb' = k 2^(gamma_C -
+          // gamma) directly (frame 0: x = gamma), a factor at most 1
+          const uint32_t bits = (smask[c0 >> 5] >> (c0 & 31)) & 0xFFu;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float kk = valid ? kv[e] : 0.0f;
+            if ((bits >> e) & 1u) {
+              kb[e] = 0.0f;
+              const float gc = misc->part[0][c0 + e] + misc->part[1][c0 + e];
+              kbt_out[(size_t)(c0 + e) * C] = kk * ex2_approx(gc - x[e]);
+            } else {
+              kb[e] = kk * ex2_approx(-x[e]);
+              kbt_out[(size_t)(c0 + e) * C] = kb[e] * er[e];
+            }
+          }
         }
         *reinterpret_cast<float4*>(sm + P_KB + sw128_off32(t, c0, P_KB_KB)) =
             make_float4(kb[0], kb[1], kb[2], kb[3]);
@@ -461,8 +495,10 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       mma_commit(&misc->bar_a);
     }
     if (tid == kLoader && !misc->abort) {
-      tma_out = advance(item + stride);
-      tma_par = par ^ 1u;
+      if (!any_strong) {  // else the exact strong-channel terms still read the staging
+        tma_out = advance(item + stride);
+        tma_par = par ^ 1u;
+      }
       bulk_wait_read0();  // the previous record's W has left its staging (the solve's scratch)
       // Hand the previous item to the publishing warp: its record's store group was committed
       // a phase ago (this item's group is not committed yet), and the generic stores of its
@@ -477,11 +513,72 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     }
     if (!mbar_wait(&misc->bar_a, par)) misc->abort = 1;
     tc_fence_after();
+    // Strong channels' exact shares of A_kk and A_qk, frame-free: for i <= t,
+    //   sum_c k_ic (k_tc or q_tc) 2^(gamma_tc - gamma_ic),
+    // every factor at most 1 (gamma is non-increasing). Rows t >= 32 against columns i < 32
+    // factor through token 31 as 2^(gamma_t - gamma_31) 2^(gamma_31 - gamma_i); the second
+    // factor times k_i is shared by all those rows and tabled first (at P_TBT: the previous
+    // record's W left that staging before the loader's wait above). Pairs inside a diagonal
+    // 32 x 32 block are taken one by one. The staging still holds this item's q, k and gamma.
+    auto sg = [&](int t, int c) -> float {  // gamma_t of channel c (log2 units, frame 0)
+      return *f32at(sm, P_STG_G + (uint32_t)(c >> 5) * 8192u + (uint32_t)t * 128u +
+                            (((((uint32_t)c & 31u) >> 2) ^ ((uint32_t)t & 7u)) << 4) +
+                            ((uint32_t)c & 3u) * 4u);
+    };
+    auto sbf = [&](uint32_t stg, int t, int c) -> float {  // staged bf16 of row t, channel c
+      const uint32_t off = stg + (uint32_t)(c >> 6) * 8192u + (uint32_t)t * 128u +
+                           (((((uint32_t)c & 63u) >> 3) ^ ((uint32_t)t & 7u)) << 4) +
+                           ((uint32_t)c & 7u) * 2u;
+      return __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(sm + off));
+    };
+    float* ptab = f32at(sm, P_TBT);  // [strong channel s][32]
+    if (any_strong) {
+      pbar();
+      int s = 0;
+      for (int w4 = 0; w4 < 4; ++w4) {
+        for (uint32_t m = smask[w4]; m; m &= m - 1u, ++s) {
+          if ((s & 7) != warp) continue;
+          const int c = w4 * 32 + __ffs(m) - 1;
+          const float kj = lane < n ? sbf(P_STG_K, lane, c) : 0.0f;
+          ptab[s * 32 + lane] = kj * ex2_approx(sg(31, c) - sg(lane, c));
+        }
+      }
+      pbar();
+    }
     // ================= beta_r A_kk -> scratch; TMEM A1 rows -> [0 ; tril(Aqk)]
     {
       float v[32];
       tmem_ld32(tbase + lane_base + TM_A1 + chh * 32, v);
       const int R = qd * 32 + lane;
+      if (any_strong) {
+        const int t = R & (C - 1), i0 = chh * 32;
+        const bool qrow = R >= C;
+        if (t >= i0 && (!qrow || need_out)) {  // (rows above the block are masked anyway)
+          const bool diag = t < i0 + 32;     // uniform per warp, as are the other conditions
+          const uint32_t stg = qrow ? P_STG_Q : P_STG_K;
+          int s = 0;
+          for (int w4 = 0; w4 < 4; ++w4) {
+            for (uint32_t m = smask[w4]; m; m &= m - 1u, ++s) {
+              const int c = w4 * 32 + __ffs(m) - 1;
+              const float gt = sg(t, c);
+              const float own = t < n ? sbf(stg, t, c) : 0.0f;
+              if (diag) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  const int i = i0 + j;
+                  const float ki = i < n ? sbf(P_STG_K, i, c) : 0.0f;
+                  const float f = i <= t ? ex2_approx(gt - sg(i, c)) : 0.0f;
+                  v[j] = fmaf(own * ki, f, v[j]);
+                }
+              } else {
+                const float ft = own * ex2_approx(gt - sg(31, c));
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = fmaf(ft, ptab[s * 32 + j], v[j]);
+              }
+            }
+          }
+        }
+      }
       if (R < C) {
         const float br = misc->beta[R];
         float* arow = f32at(sm, SCR_A) + R * LA + chh * 32;
@@ -504,6 +601,10 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       tmem_st_wait();
     }
     psync();
+    if (any_strong && tid == kLoader && !misc->abort) {  // the staging is read no more
+      tma_out = advance(item + stride);
+      tma_par = par ^ 1u;
+    }
     // ================= T = (I + A_kk)^-1 in 16 x 16 blocks
     {
       const float* Akk = f32at(sm, SCR_A);

@@ -52,8 +52,8 @@ struct ChunkParams {
 
 // Chunk size of every chunked kernel.
 constexpr int kChunk = 64;
-// Decay spread (nats over one chunk, per key channel) the chunk kernels accept; beyond it
-// KDA_STATUS_DECAY_RANGE is raised.
+// Decay (nats over one chunk, per key channel) up to which the chunk kernels use the log-
+// midpoint frame for that channel; a channel that decays more is computed frame-free.
 constexpr float kMaxChunkDecay = 160.0f;
 
 // FFMA (CUDA-core) chunk kernel: fp32 arithmetic throughout; any dtype.

@@ -18,7 +18,7 @@ KDA_F32, KDA_BF16 = 0, 1
 DECODE_BETA_LOGIT = 1
 CONV_SILU = 1
 MAX_WINDOW = 16
-STATUS_BAD_SLOT, STATUS_DECAY_RANGE, STATUS_BAD_OFFSETS = 1, 2, 4
+STATUS_BAD_SLOT, STATUS_BAD_OFFSETS, STATUS_TIMEOUT = 1, 4, 8
 
 _lib = None
 

@@ -54,18 +54,6 @@ def test_strong_coupling_variant():
     _check(x)
 
 
-def test_decay_range_status():
-    x = inputs.make_prefill([128], H=1, dk=64, dv=64, dtype="f32", seed=24, device=DEV)
-    status = torch.zeros(1, dtype=torch.int32, device=DEV)
-    g = x.g.clone()
-    g[:64, 0, 5] = -3.0  # 192 nats over the first chunk in channel 5
-    kda.chunk_prefill(x.q, x.k, x.v, g, x.beta, status=status)
-    assert status.item() & kda.STATUS_DECAY_RANGE
-    status.zero_()
-    kda.chunk_prefill(x.q, x.k, x.v, x.g, x.beta, status=status)
-    assert status.item() == 0
-
-
 def test_full_prefill_16k_sampled_heads():
     """The 16k-token, 32-head workload in the launch configuration the benchmark times;
     the oracle checks two sampled heads (heads are independent)."""
