@@ -252,6 +252,27 @@ KDA_API kda_status kda_segment_replay_prepared(kda_dtype dt, int n_segs, int tot
                                                uint32_t* status, kda_stream_t stream);
 
 /*
+ * kda_debug_flag_wait: a diagnostic of the bounded waits. The state walk of
+ * kda_segment_replay_prepared over the same records, except that before loading each record
+ * the walk waits for that record's 4-byte ready flag to be non-zero, as the walk of a fused
+ * prefill does, giving up after limit_ns nanoseconds (1e6 .. 4e9). The flags follow the
+ * R = (total_tokens / 64 + n_segs) * H records: record r (chunk slot r / H, head r % H) has
+ * its flag in the uint32 at byte R * 147968 + 4 r of the workspace. kda_chunk_prepare leaves
+ * them as they were, so the caller sets them.
+ * All flags non-zero: the results equal those of kda_segment_replay_prepared, bit for bit.
+ * A zero flag: every walk that reaches it gives up, raises KDA_STATUS_TIMEOUT in *status,
+ * lets its own copies and tensor-core work finish, frees its tensor memory and returns; its
+ * outputs from that record on are not written. The device stays usable. The pages have no
+ * counterpart: this exists so that the error path of the waits can be run without a fault.
+ */
+KDA_API kda_status kda_debug_flag_wait(kda_dtype dt, int n_segs, int total_tokens,
+                                       const int32_t* seg_offsets, int H, int dk, int dv,
+                                       int chunk, const float* seg_init, void* o,
+                                       float* seg_final, const void* workspace,
+                                       size_t ws_bytes, uint64_t limit_ns, uint32_t* status,
+                                       kda_stream_t stream);
+
+/*
  * kda_decode_step: one token per batch row over a slot-addressed fp32 state pool,
  * updated in place: for row b and head h, S = pool[slot_ids[b], h] becomes its successor
  * and o[b, h] = scale * S_new^T q.

@@ -287,6 +287,30 @@ kda_status kda_segment_replay_prepared(kda_dtype dt, int n_segs, int total_token
                          kPhaseState);
 }
 
+kda_status kda_debug_flag_wait(kda_dtype dt, int n_segs, int total_tokens,
+                               const int32_t* seg_offsets, int H, int dk, int dv, int chunk,
+                               const float* seg_init, void* o, float* seg_final,
+                               const void* workspace, size_t ws_bytes, uint64_t limit_ns,
+                               uint32_t* status, kda_stream_t stream) {
+  const char* fn = "kda_debug_flag_wait";
+  kda_status st = check_prepared(fn, dt, n_segs, total_tokens, seg_offsets, H, dk, dv, chunk,
+                                 workspace, ws_bytes);
+  if (st != KDA_OK || n_segs == 0 || total_tokens == 0) return st;
+  KDA_REQUIRE(limit_ns >= 1000000ull && limit_ns <= 4000000000ull, KDA_ERR_INVALID_ARG,
+              "kda_debug_flag_wait: limit_ns must be in [1e6, 4e9]");
+  KDA_REQUIRE(o && aligned(o, 16) && aligned(seg_init, 16) && aligned(seg_final, 16) &&
+                  aligned(status, 4),
+              KDA_ERR_INVALID_ARG, "kda_debug_flag_wait: o must be non-null, pointers "
+                                   "16-byte aligned");
+  ChunkParams p{};
+  p.offsets = seg_offsets; p.n_ranges = n_segs; p.total_tokens = total_tokens;
+  p.H = H; p.dk = dk; p.dv = dv; p.scale = 1.0f;
+  p.init = seg_init; p.o = o; p.final_state = seg_final; p.status = status; p.package = 0;
+  p.flag_wait_ns = limit_ns;
+  return launch_chunk_tc(p, dt, const_cast<void*>(workspace), ws_bytes, (cudaStream_t)stream,
+                         kPhaseState | kPhaseFlags);
+}
+
 kda_status kda_decode_step(kda_dtype dt, int batch, int H, int dk, int dv, float scale,
                            const void* q, const void* k, const void* v, const float* g,
                            const float* beta, const int32_t* slot_ids, float* state_pool,

@@ -1019,7 +1019,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
       auto issue_tma = [&](int j) -> bool {  // chunk j into stage j & 1 and decay slot j % 3
         const int item = (slot0 + j) * H + h;
         if (flags) {  // the record is published by the prep CTA that wrote it
-          if (!wait_flag(flags + item)) return false;
+          if (!wait_flag(flags + item, p.flag_wait_ns)) return false;
           fence_proxy_async_global();
         }
         uint8_t* st = sm + (j & 1) * S_STAGE;
@@ -1052,11 +1052,11 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
         const uint32_t st = (uint32_t)(j & 1) * S_STAGE;
         const uint64_t d_wq = sdesc_sw128(sbase + st + S_WQ, 16, 1024);
         const uint64_t d_kbt = sdesc_sw128(sbase + st + S_KBT, 16, 1024);
-        ok = mbar_wait(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u);
+        ok = mbar_wait_or(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u, &misc->abort);
         // X^T = S^T [W ; Q'']^T, channel half by channel half as S^T is written
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          ok = ok && mbar_wait(&misc->s_ready[hh], par);
+          ok = ok && mbar_wait_or(&misc->s_ready[hh], par, &misc->abort);
           tc_fence_after();
           if (ok) {
 #pragma unroll
@@ -1072,7 +1072,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
         // Y^T = U^T Kb', token half by token half as U^T is written
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          ok = ok && mbar_wait(&misc->u_ready[hh], par);
+          ok = ok && mbar_wait_or(&misc->u_ready[hh], par, &misc->abort);
           tc_fence_after();
           if (ok) {
 #pragma unroll
@@ -1087,7 +1087,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
         mma_commit(&misc->bar_y);
         // the stage is free once Y has completed: load chunk j + 2 into it
         if (j + 2 < nch) {
-          ok = mbar_wait(&misc->bar_y, par) && issue_tma(j + 2);
+          ok = mbar_wait_or(&misc->bar_y, par, &misc->abort) && issue_tma(j + 2);
           if (ok) tma_last = j + 2;
         }
       }
@@ -1128,7 +1128,8 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
       if (flags) {
         // The issuer acquired the record's flag before its arrive on this chunk's stage
         // barrier (a release): acquiring that phase orders these loads after the record.
-        if (!mbar_wait(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u)) misc->abort = 1;
+        if (!mbar_wait_or(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u, &misc->abort))
+          misc->abort = 1;
       }
       if (vcol >= 0) {
         const float4* src = reinterpret_cast<const float4*>(ws.u0 + item * 8192) + hf * 8 * 128 + vcol;
@@ -1157,7 +1158,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
       const int nvalid = min(C, t_end - t0);
       const uint32_t par = (uint32_t)j & 1u;
       // ================= U^T = U0^T - (W S)^T (tokens 32 hf ..), then the outputs
-      if (!mbar_wait_relaxed(&misc->bar_x, par)) misc->abort = 1;
+      if (!mbar_wait_relaxed_or(&misc->bar_x, par, &misc->abort)) misc->abort = 1;
       tc_fence_after();
       {
         float x[32];
@@ -1191,7 +1192,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
         }
       }
       // ================= S^T = S^T Diag(e^gamma_C) + Y^T (channels 64 hf ..)
-      if (!mbar_wait_relaxed(&misc->bar_y, par)) misc->abort = 1;
+      if (!mbar_wait_relaxed_or(&misc->bar_y, par, &misc->abort)) misc->abort = 1;
       tc_fence_after();
       {
         const float* dec = f32at(sm, S_DEC + (j % 3) * 512);
@@ -1218,8 +1219,8 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
         if (lane == 0 && j + 1 < nch) mbar_arrive_relaxed(&misc->s_ready[hf]);
       }
       // outputs, after the state update has released the next chunk's X product: token t of
-      // column n (32 lanes = 64 contiguous bytes of one token's row)
-      if (!pkg && p.o) {
+      // column n (32 lanes = 64 contiguous bytes of one token's row); none once the CTA gave up
+      if (!pkg && p.o && !misc->abort) {
         __nv_bfloat16* o = (__nv_bfloat16*)p.o + ((int64_t)t0 * H + h) * DK + n;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -1260,8 +1261,9 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 chunk_state_kernel(const __grid_constant__ ChunkParams p,
                    const __grid_constant__ CUtensorMap twq,
                    const __grid_constant__ CUtensorMap tkbt,
-                   const __grid_constant__ CUtensorMap tdec, const Ws ws) {
-  state_run(p, twq, tkbt, tdec, ws, blockIdx.x, blockIdx.y, blockIdx.z, nullptr);
+                   const __grid_constant__ CUtensorMap tdec, const Ws ws,
+                   const uint32_t* flags) {
+  state_run(p, twq, tkbt, tdec, ws, blockIdx.x, blockIdx.y, blockIdx.z, flags);
 }
 
 // ============================================================================ fused launch
@@ -1450,6 +1452,8 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   uint32_t* flags = (uint32_t*)(base + (size_t)n_items * kItemBytes);
 
   const bool do_prep = (phases & kPhasePrep) != 0, do_state = (phases & kPhaseState) != 0;
+  ChunkParams pp = p;
+  if (pp.flag_wait_ns == 0) pp.flag_wait_ns = 4000000000ull;
   CUtensorMap mq, mk, mv, mg, mb, mwq, mkbt, mdec, swq;
   const uint64_t rows128 = (uint64_t)n_items * 128;
   bool maps_ok = true;
@@ -1500,7 +1504,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, chunk_fused_kernel, p, mq, mk, mv, mg, mb, swq, mwq, mkbt, mdec,
+    e = cudaLaunchKernelEx(&cfg, chunk_fused_kernel, pp, mq, mk, mv, mg, mb, swq, mwq, mkbt, mdec,
                            ws, (int)n_items, (int)n_state, flags);
     if (e == cudaSuccess) {
       count_launches(1);
@@ -1510,14 +1514,15 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   }
   if (do_prep) {
     const int grid1 = (int)std::min<int64_t>(n_items, sms);
-    chunk_prep_kernel<<<grid1, kThreads, P_SMEM, s>>>(p, mq, mk, mv, mg, mb, swq, ws,
+    chunk_prep_kernel<<<grid1, kThreads, P_SMEM, s>>>(pp, mq, mk, mv, mg, mb, swq, ws,
                                                        (int)n_items);
     count_launches(1);
     kda_status st = check_launch("tensor-core chunk prep kernel");
     if (st != KDA_OK || !do_state) return st;
   }
   dim3 grid2(tiles, p.H, p.n_ranges);
-  chunk_state_kernel<<<grid2, kStateThreads, S_SMEM, s>>>(p, mwq, mkbt, mdec, ws);
+  chunk_state_kernel<<<grid2, kStateThreads, S_SMEM, s>>>(
+      pp, mwq, mkbt, mdec, ws, (phases & kPhaseFlags) ? flags : nullptr);
   count_launches(1);
   return check_launch("tensor-core chunk state kernel");
 }

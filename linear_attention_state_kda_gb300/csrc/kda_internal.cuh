@@ -48,6 +48,7 @@ struct ChunkParams {
   float* D;               // package mode: [n_ranges, H, dk, dv]
   uint32_t* status;       // optional device status word
   int package;            // 1 = package mode
+  uint64_t flag_wait_ns;  // limit of a walk's wait for a record's ready flag (0: default)
 };
 
 // Chunk size of every chunked kernel.
@@ -68,7 +69,9 @@ bool chunk_tc_shape_ok(kda_dtype dt, int n_ranges, int total_tokens, int H, int 
 size_t chunk_tc_workspace_bytes(int n_ranges, int total_tokens, int H);
 bool chunk_tc_available();
 // phases: kPhasePrep writes the records, kPhaseState walks them; both = one chunked call.
-constexpr int kPhasePrep = 1, kPhaseState = 2;
+// kPhaseFlags (with kPhaseState alone) makes the walk wait for each record's ready flag in
+// the workspace, as the fused launch's walk does (the flag-wait diagnostic).
+constexpr int kPhasePrep = 1, kPhaseState = 2, kPhaseFlags = 4;
 kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, size_t ws_bytes,
                            cudaStream_t s, int phases = kPhasePrep | kPhaseState);
 

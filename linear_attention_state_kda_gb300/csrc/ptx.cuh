@@ -89,6 +89,31 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// mbar_wait / mbar_wait_relaxed that also give up as soon as the CTA's shared abort word
+// becomes non-zero (another thread of the CTA has already given up), so that one expired wait
+// unwinds the whole CTA promptly instead of every other waiter running out its own limit.
+__device__ __forceinline__ bool mbar_wait_or(uint64_t* bar, uint32_t parity, const int* abort,
+                                             uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*(const volatile int*)abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+__device__ __forceinline__ bool mbar_wait_relaxed_or(uint64_t* bar, uint32_t parity,
+                                                     const int* abort,
+                                                     uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait_relaxed(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_relaxed(bar, parity)) return true;
+    if (*(const volatile int*)abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+}
+
 // ---------------------------------------------------------------- proxy fences
 // Makes this thread's generic-proxy shared-memory writes visible to the async proxy
 // (tensor core operand reads, TMA).

@@ -68,6 +68,9 @@ def lib():
     L.kda_segment_package_prepared.argtypes = [I, I, I, P, I, I, I, I, P, P, P, Z, P, P]
     L.kda_segment_replay_prepared.restype = I
     L.kda_segment_replay_prepared.argtypes = [I, I, I, P, I, I, I, I, P, P, P, P, Z, P, P]
+    L.kda_debug_flag_wait.restype = I
+    L.kda_debug_flag_wait.argtypes = [I, I, I, P, I, I, I, I, P, P, P, P, Z, ctypes.c_uint64,
+                                      P, P]
     L.kda_decode_step.restype = I
     L.kda_decode_step.argtypes = [I, I, I, I, I, F, P, P, P, P, P, P, P, I64, P, P, P]
     L.kda_decode_window.restype = I
@@ -297,6 +300,35 @@ def segment_replay_prepared(workspace, seg_offsets, seg_init, T, H, dk, dv, o=No
                                              _ptr(seg_init), _ptr(o), _ptr(seg_final),
                                              _ptr(workspace), workspace.numel(), _ptr(status),
                                              _stream(stream)))
+    return o, seg_final
+
+
+RECORD_BYTES = 147968  # one (64-token chunk, head) record of the tensor-core chunk path
+
+
+def record_flags(workspace, n_ranges, T, H):
+    """The ready flags after the records in a chunk workspace (an int32 view)."""
+    R = (T // 64 + n_ranges) * H
+    return workspace[R * RECORD_BYTES:R * RECORD_BYTES + 4 * R].view(torch.int32)
+
+
+def debug_flag_wait(workspace, seg_offsets, seg_init, T, H, dk, dv, limit_ns, o=None,
+                    seg_final=None, want_final=False, status=None, dtype=torch.bfloat16,
+                    chunk=64, stream=None):
+    """kda_debug_flag_wait: the prepared replay walk, each record gated by its ready flag
+    (bounded by limit_ns). Returns (o, seg_final)."""
+    _contig(seg_offsets, seg_init, o, seg_final)
+    P = seg_offsets.numel() - 1
+    dev = workspace.device
+    if o is None:
+        o = torch.zeros(T, H, dv, dtype=dtype, device=dev)
+    if seg_final is None and want_final:
+        seg_final = torch.empty(P, H, dk, dv, dtype=torch.float32, device=dev)
+    dt = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    _check(lib().kda_debug_flag_wait(dt, P, T, _ptr(seg_offsets), H, dk, dv, chunk,
+                                     _ptr(seg_init), _ptr(o), _ptr(seg_final), _ptr(workspace),
+                                     workspace.numel(), int(limit_ns), _ptr(status),
+                                     _stream(stream)))
     return o, seg_final
 
 
