@@ -418,8 +418,8 @@ kda_status kda_short_conv(kda_dtype dt, int n_seqs, int total_tokens, const int3
               "kda_short_conv: slot tables need conv_state and n_slots > 0");
   KDA_REQUIRE(total_tokens == 0 || (x && weight && out), KDA_ERR_INVALID_ARG,
               "kda_short_conv: x, weight and out must be non-null");
-  KDA_REQUIRE((int64_t)total_tokens / 64 + n_seqs <= 0x7fffffffLL, KDA_ERR_INVALID_ARG,
-              "kda_short_conv: too many tokens");
+  KDA_REQUIRE(((int64_t)total_tokens / 16 + n_seqs) * ((channels + 511) / 512) <= 0x7fffffffLL,
+              KDA_ERR_INVALID_ARG, "kda_short_conv: too many tokens x channels for one launch");
   KDA_REQUIRE(aligned(x, 16) && aligned(out, 16) && aligned(conv_state, 16) &&
                   aligned(weight, 4) && aligned(cu_seqlens, 4) && aligned(read_slots, 4) &&
                   aligned(write_slots, 4) && aligned(status, 4),

@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libkda.so.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -68,6 +69,10 @@ kda_status launch_chunk_simt(const ChunkParams& p, kda_dtype dt, cudaStream_t s)
 bool chunk_tc_shape_ok(kda_dtype dt, int n_ranges, int total_tokens, int H, int dk, int dv);
 size_t chunk_tc_workspace_bytes(int n_ranges, int total_tokens, int H);
 bool chunk_tc_available();
+// A row-major [rows][cols] array (bf16, or fp32 when f32) as a 2-D tensor map without swizzle,
+// box [box_rows][box_cols]; false when the driver lacks the encoder or rejects the layout.
+bool make_map_rows(CUtensorMap* m, const void* ptr, bool f32, uint64_t cols, uint64_t rows,
+                   uint32_t box_cols, uint32_t box_rows);
 // phases: kPhasePrep writes the records, kPhaseState walks them; both = one chunked call.
 // kPhaseFlags (with kPhaseState alone) makes the walk wait for each record's ready flag in
 // the workspace, as the fused launch's walk does (the flag-wait diagnostic).
