@@ -228,9 +228,34 @@ struct TileCtx {
   bool ok;
 };
 
-// out tile = A o B (bm null: state application, out.D = A.M S + A.D with S = bd; bd null as
-// well: out.D = A.D). TMEM and the barrier come with the context (allocated once per CTA).
-__device__ void tile_combine(TileCtx& cx, const float* A, const float* bm, const float* bd,
+// A.M (row-major 128 x 128) -> the A operand in shared memory, split 3xTF32 (hi / lo, K-major).
+// Every load is issued before the first shared-memory store (one round trip to L2).
+__device__ void load_a(const float* A) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  const int tid = threadIdx.x;
+  float4 a[16];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {  // element e = tid + 256 u
+    const int e = tid + u * kThreads;
+    a[u] = *reinterpret_cast<const float4*>(A + (e >> 5) * DK + (e & 31) * 4);
+  }
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const int e = tid + u * kThreads;
+    const float4 hh = make_float4(hi(a[u].x), hi(a[u].y), hi(a[u].z), hi(a[u].w));
+    const uint32_t off = sw128_off32(e >> 5, (e & 31) * 4, A_KB);
+    *reinterpret_cast<float4*>(sm + AH + off) = hh;
+    *reinterpret_cast<float4*>(sm + AL + off) =
+        make_float4(a[u].x - hh.x, a[u].y - hh.y, a[u].z - hh.z, a[u].w - hh.w);
+  }
+}
+
+// One 64-column tile of out = A o B with A.M already in shared memory (load_a, then a barrier
+// that orders it before the product): tiles 0, 1 are out.M = A.M B.M, tiles 2, 3 out.D =
+// A.M B.D + A.D (bm null: a state application, out.D = A.M S + A.D with S = bd; bd null as well:
+// out.D = A.D). ad is A.D. TMEM and the barrier come with the context.
+__device__ void tile_product(TileCtx& cx, const float* ad_pkg, const float* bm, const float* bd,
                              float* om, float* od, int tile, uint32_t* status) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
@@ -239,30 +264,22 @@ __device__ void tile_combine(TileCtx& cx, const float* A, const float* bm, const
   const int col0 = (mtile ? tile : tile - DK / NT) * NT;
   float* out = mtile ? om : od;
   const float* B = mtile ? bm : bd;
-  if (B) {
-    // every load of the two operands is issued before the first shared-memory store, so that a
-    // combine waits for one round trip to L2 rather than one per loop step
-    float4 a[16], b[8];
+  // A.D's part of this tile (D tiles), loaded now so that its latency hides under the product
+  float4 adv[8];
+  const int r = (warp & 3) * 32 + lane, cb = (warp >> 2) * 32;
+  if (!mtile) {
+    const float4* ad = reinterpret_cast<const float4*>(ad_pkg + r * DK + col0 + cb);
 #pragma unroll
-    for (int u = 0; u < 16; ++u) {  // A.M, row-major: element e = tid + 256 u
-      const int e = tid + u * kThreads;
-      a[u] = *reinterpret_cast<const float4*>(A + (e >> 5) * DK + (e & 31) * 4);
-    }
+    for (int j = 0; j < 8; ++j) adv[j] = ad[j];
+  }
+  if (B) {
     // the B tile: element e = tid + 256 u is row k = (e & 127) of columns n4 .. n4 + 3,
     // n4 = 4 (e >> 7), so that a warp's transposed stores below fill whole 128-byte rows
+    float4 b[8];
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int e = tid + u * kThreads;
       b[u] = *reinterpret_cast<const float4*>(B + (e & 127) * DK + col0 + (e >> 7) * 4);
-    }
-#pragma unroll
-    for (int u = 0; u < 16; ++u) {  // A.M -> hi / lo, K-major [r][k]
-      const int e = tid + u * kThreads;
-      const float4 hh = make_float4(hi(a[u].x), hi(a[u].y), hi(a[u].z), hi(a[u].w));
-      const uint32_t off = sw128_off32(e >> 5, (e & 31) * 4, A_KB);
-      *reinterpret_cast<float4*>(sm + AH + off) = hh;
-      *reinterpret_cast<float4*>(sm + AL + off) =
-          make_float4(a[u].x - hh.x, a[u].y - hh.y, a[u].z - hh.z, a[u].w - hh.w);
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {  // B tile, transposed (row n, 32 consecutive k per warp)
@@ -306,7 +323,6 @@ __device__ void tile_combine(TileCtx& cx, const float* A, const float* bm, const
     tc_fence_after();
   }
   {  // warp w: rows 32 (w % 4).., columns 32 (w / 4)..; D tiles add A.D
-    const int r = (warp & 3) * 32 + lane, cb = (warp >> 2) * 32;
     float v[32];
     if (B) {
       tmem_ld32(cx.tbase + ((uint32_t)((warp & 3) * 32) << 16) + cb, v);
@@ -314,24 +330,41 @@ __device__ void tile_combine(TileCtx& cx, const float* A, const float* bm, const
 #pragma unroll
       for (int j = 0; j < 32; ++j) v[j] = 0.0f;
     }
-    const float* ad = A + DK * DK + r * DK + col0 + cb;
-    float* dst = out + r * DK + col0 + cb;
-    if (!mtile) {  // all eight loads of A.D first
-      float4 a[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) a[j] = reinterpret_cast<const float4*>(ad)[j];
+    if (!mtile) {
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        v[4 * j] += a[j].x; v[4 * j + 1] += a[j].y; v[4 * j + 2] += a[j].z; v[4 * j + 3] += a[j].w;
+        v[4 * j] += adv[j].x; v[4 * j + 1] += adv[j].y; v[4 * j + 2] += adv[j].z;
+        v[4 * j + 3] += adv[j].w;
       }
     }
+    float* dst = out + r * DK + col0 + cb;
 #pragma unroll
     for (int j = 0; j < 32; j += 4)
       *reinterpret_cast<float4*>(dst + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
   }
   tc_fence_before();
-  __syncthreads();  // the operand buffers and TMEM are reused by the next call
+  __syncthreads();  // the B buffers and TMEM are reused by the next tile
   tc_fence_after();
+}
+
+// Work of one tree level with `pairs` combines, over the cluster's 4 CTAs: with 4 or more
+// combines a CTA takes whole combines (its A operand loaded once for all 4 tiles); with 2, two
+// CTAs share a combine (2 tiles each); with 1, each CTA takes one tile. Returns the tiles of
+// round `round` for this CTA: combine index `pair`, tiles [t0, t0 + nt).
+__device__ __forceinline__ bool level_work(int pairs, int rank, int round, int& pair, int& t0,
+                                           int& nt) {
+  if (pairs >= 4) {
+    pair = rank + 4 * round;
+    t0 = 0;
+    nt = 4;
+    return pair < pairs;
+  }
+  if (round > 0) return false;
+  const int per = 4 / pairs;  // CTAs per combine
+  pair = rank / per;
+  nt = 4 / per;
+  t0 = (rank % per) * nt;
+  return true;
 }
 
 // Copy column tile `tile` (0, 1: M columns; 2, 3: D columns) of a package: src_m / src_d are
@@ -400,54 +433,79 @@ scan_tree_tc(Tree t, const int32_t* seq_off, const float* M, const float* D, con
     }
   }
   cluster_sync_all();
-  // up-sweep: a[i] = a[i] o a[i - d]
+  // up-sweep: a[i] = a[i] o a[i - d], written in place: every CTA working on a combine has its
+  // A operand (a[i].M) in shared memory before any of them writes (the cluster barrier), and no
+  // combine of the level reads another's a[i]
+  const int rank = tile;
   for (int d = 1; d < t.P2; d <<= 1) {
-    for (int pair = 0; pair < t.P2 / (2 * d); ++pair) {
+    const int pairs = t.P2 / (2 * d);
+    for (int round = 0; round * 4 < pairs || round == 0; ++round) {
+      int pair, t0, nt;
+      const bool mine = level_work(pairs, rank, round, pair, t0, nt);
       const int i = (2 * pair + 2) * d - 1;
-      const float* A = t.node(s, i, h);
-      const float* B = t.node(s, i - d, h);
-      float* o = t.tnode(s, pair, h);
-      tile_combine(cx, A, B, B + sd, o, o + sd, tile, status);
+      if (mine) load_a(t.node(s, i, h));
+      __syncthreads();
+      cluster_sync_all();
+      if (mine) {
+        float* A = t.node(s, i, h);
+        const float* B = t.node(s, i - d, h);
+        for (int tt = t0; tt < t0 + nt; ++tt)
+          tile_product(cx, A + sd, B, B + sd, A, A + sd, tt, status);
+      }
+      cluster_sync_all();
     }
-    cluster_sync_all();
-    for (int pair = 0; pair < t.P2 / (2 * d); ++pair)
-      tile_move(t.tnode(s, pair, h), t.node(s, (2 * pair + 2) * d - 1, h), tile);
-    cluster_sync_all();
   }
   // root: the exit state (D tiles), then (I, 0)
   float* root = t.node(s, t.P2 - 1, h);
   if (final_state && tile >= DK / NT) {
     float* fo = final_state + ((int64_t)s * t.H + h) * sd;
-    tile_combine(cx, root, nullptr, init ? init + ((int64_t)s * t.H + h) * sd : nullptr, nullptr,
-                 fo, tile, status);
+    load_a(root);
+    __syncthreads();
+    tile_product(cx, root + sd, nullptr, init ? init + ((int64_t)s * t.H + h) * sd : nullptr,
+                 nullptr, fo, tile, status);
   }
   cluster_sync_all();
   tile_copy(nullptr, nullptr, root, tile);
   cluster_sync_all();
-  // down-sweep: (a[i - d], a[i]) <- (a[i], a[i - d] o a[i])
+  // down-sweep: (a[i - d], a[i]) <- (a[i], a[i - d] o a[i]); the combines go to tmp nodes,
+  // then each CTA moves the tiles it computed
   for (int d = t.P2 / 2; d >= 1; d >>= 1) {
-    for (int pair = 0; pair < t.P2 / (2 * d); ++pair) {
-      const int i = (2 * pair + 2) * d - 1;
-      const float* A = t.node(s, i - d, h);
-      const float* B = t.node(s, i, h);
-      float* o = t.tnode(s, pair, h);
-      tile_combine(cx, A, B, B + sd, o, o + sd, tile, status);
+    const int pairs = t.P2 / (2 * d);
+    for (int round = 0; round * 4 < pairs || round == 0; ++round) {
+      int pair, t0, nt;
+      if (level_work(pairs, rank, round, pair, t0, nt)) {
+        const int i = (2 * pair + 2) * d - 1;
+        const float* A = t.node(s, i - d, h);
+        const float* B = t.node(s, i, h);
+        float* o = t.tnode(s, pair, h);
+        load_a(A);
+        __syncthreads();
+        for (int tt = t0; tt < t0 + nt; ++tt)
+          tile_product(cx, A + sd, B, B + sd, o, o + sd, tt, status);
+      }
     }
     cluster_sync_all();
-    for (int pair = 0; pair < t.P2 / (2 * d); ++pair) {
+    for (int round = 0; round * 4 < pairs || round == 0; ++round) {
+      int pair, t0, nt;
+      if (!level_work(pairs, rank, round, pair, t0, nt)) continue;
       const int i = (2 * pair + 2) * d - 1;
-      tile_move(t.node(s, i, h), t.node(s, i - d, h), tile);
-      tile_move(t.tnode(s, pair, h), t.node(s, i, h), tile);
+      for (int tt = t0; tt < t0 + nt; ++tt) {
+        tile_move(t.node(s, i, h), t.node(s, i - d, h), tt);
+        tile_move(t.tnode(s, pair, h), t.node(s, i, h), tt);
+      }
     }
     cluster_sync_all();
   }
-  // entry states: leaf j's prefix applied to the sequence's entry state; the two D tiles of
-  // each leaf are spread over the four CTAs
-  for (int j = tile >> 1; j < cnt; j += 2) {
-    const int dt = DK / NT + (tile & 1);
+  // entry states: leaf j's prefix applied to the sequence's entry state, both D tiles of a
+  // leaf by one CTA (its prefix's M loaded once)
+  for (int j = rank; j < cnt; j += 4) {
+    const float* pre = t.node(s, j, h);
     float* so = seg_init + ((int64_t)(first + j) * t.H + h) * sd;
-    tile_combine(cx, t.node(s, j, h), nullptr,
-                 init ? init + ((int64_t)s * t.H + h) * sd : nullptr, nullptr, so, dt, status);
+    load_a(pre);
+    __syncthreads();
+    for (int dt = DK / NT; dt < 2 * (DK / NT); ++dt)
+      tile_product(cx, pre + sd, nullptr, init ? init + ((int64_t)s * t.H + h) * sd : nullptr,
+                   nullptr, so, dt, status);
   }
   tc_fence_before();
   __syncthreads();
