@@ -571,7 +571,8 @@ def run_reference(args):
 def run_profile_case(args):
     """A small case of one call (inputs still larger than L2, a few GB on the device at most)
     for ncu captures: `--profile-case prefill|package|replay|scan|decode|window|slots|conv`,
-    `--launches N`."""
+    `--launches N`; `prefill16k` is the benchmark's full prefill launch, for single-pass
+    counters only."""
     import torch
     from linear_attention_state_kda_gb300 import inputs, kda
     dev = torch.device("cuda", 0)
@@ -593,6 +594,9 @@ def run_profile_case(args):
         d = inputs.make_decode(256, 32, D, D, 1024, seed=1004, device=dev)
         image = torch.empty(256, 32, D, D, device=dev)
         fns = [lambda: kda.slot_copy(d.pool, d.slot_ids, image, None)]
+    elif case == "prefill16k":  # the benchmark's own prefill launch (about 2 GB on the device)
+        x = inputs.make_workload("prefill_16k", device=dev)
+        fns = [lambda: kda.chunk_prefill(x.q, x.k, x.v, x.g, x.beta)]
     else:
         x = inputs.make_prefill([4096], 32, D, D, "bf16", seed=1001, device=dev)
         offs = torch.tensor([0, 2048, 4096], dtype=torch.int32, device=dev)
@@ -621,8 +625,8 @@ def run_profile_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--profile-case", default=None,
-                    choices=["prefill", "package", "scan", "replay", "decode", "window",
-                             "slots", "conv"])
+                    choices=["prefill", "prefill16k", "package", "scan", "replay", "decode",
+                             "window", "slots", "conv"])
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)

@@ -1123,7 +1123,9 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
     }
     // per-chunk register operands, loaded one chunk ahead: U0^T[n][32 hf ..] (32 fp32) and
     // O0^T[n][32 hf ..] (32 bf16)
-    auto load_regs = [&](int j, float4* u0, uint4* o0) {
+    // U0^T first (needed by the U step), O0^T second (needed by the outputs), each issued as
+    // soon as the previous chunk's registers are consumed
+    auto load_u0 = [&](int j, float4* u0) {
       const int64_t item = (int64_t)(slot0 + j) * H + h;
       if (flags) {
         // The issuer acquired the record's flag before its arrive on this chunk's stage
@@ -1139,6 +1141,9 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
 #pragma unroll
         for (int i = 0; i < 8; ++i) u0[i] = make_float4(0.f, 0.f, 0.f, 0.f);
       }
+    };
+    auto load_o0 = [&](int j, uint4* o0) {  // after load_u0 of the same chunk (its acquire)
+      const int64_t item = (int64_t)(slot0 + j) * H + h;
       if (!pkg) {
         const uint4* src = reinterpret_cast<const uint4*>(ws.o0 + item * 8192) + hf * 4 * 128 + n;
 #pragma unroll
@@ -1151,7 +1156,10 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
     for (int i = 0; i < 8; ++i) u0[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < 4; ++i) o0[i] = make_uint4(0, 0, 0, 0);
-    if (nch > 0) load_regs(0, u0, o0);
+    if (nch > 0) {
+      load_u0(0, u0);
+      load_o0(0, o0);
+    }
 
     for (int j = 0; j < nch; ++j) {
       const int t0 = t_begin + j * C;
@@ -1175,7 +1183,9 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
         __syncwarp();
         if (lane == 0) mbar_arrive_relaxed(&misc->u_ready[hf]);
       }
-      // output values of tokens 32 hf .. 32 hf + 31: O^T[n][t] = (Q'' S)^T + O0^T
+      if (j + 1 < nch) load_u0(j + 1, u0);  // this chunk's U0^T is consumed
+      // output values of tokens 32 hf .. 32 hf + 31: O^T[n][t] = (Q'' S)^T + O0^T, packed as
+      // bf16 pairs of adjacent tokens
       uint32_t ob16[16];
       if (!pkg && p.o) {
         float x[32];
@@ -1191,6 +1201,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
           }
         }
       }
+      if (j + 1 < nch) load_o0(j + 1, o0);  // this chunk's O0^T is consumed
       // ================= S^T = S^T Diag(e^gamma_C) + Y^T (channels 64 hf ..)
       if (!mbar_wait_relaxed_or(&misc->bar_y, par, &misc->abort)) misc->abort = 1;
       tc_fence_after();
@@ -1220,19 +1231,21 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
       }
       // outputs, after the state update has released the next chunk's X product: token t of
       // column n (32 lanes = 64 contiguous bytes of one token's row); none once the CTA gave up
+      // Lanes l and l ^ 1 trade halves so that the even lane holds columns (n, n + 1) of the
+      // even tokens and the odd lane those of the odd tokens: 16 four-byte stores per thread.
       if (!pkg && p.o && !misc->abort) {
-        __nv_bfloat16* o = (__nv_bfloat16*)p.o + ((int64_t)t0 * H + h) * DK + n;
+        const bool odd = (lane & 1) != 0;
+        __nv_bfloat16* o = (__nv_bfloat16*)p.o + ((int64_t)t0 * H + h) * DK + (n & ~1);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const int t = hf * 32 + 2 * i;
-          const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162*>(&ob16[i]);
-          if (t < nvalid) o[(int64_t)t * H * DK] = b.x;
-          if (t + 1 < nvalid) o[(int64_t)(t + 1) * H * DK] = b.y;
+          const uint32_t mine = ob16[i];  // (token 2i, token 2i + 1) of column n
+          const uint32_t give = odd ? (mine & 0xFFFFu) : (mine >> 16);
+          const uint32_t got = __shfl_xor_sync(0xFFFFFFFFu, give, 1);
+          const uint32_t pair = odd ? (got | (mine & 0xFFFF0000u)) : ((mine & 0xFFFFu) | (got << 16));
+          const int t = hf * 32 + 2 * i + (odd ? 1 : 0);
+          if (t < nvalid) *reinterpret_cast<uint32_t*>(o + (int64_t)t * H * DK) = pair;
         }
       }
-      // the next chunk's register operands (this chunk's are consumed), loaded while the next
-      // chunk's X is on the tensor core (the issuer has brought them into L2)
-      if (j + 1 < nch) load_regs(j + 1, u0, o0);
       if (misc->abort) break;
     }
   }
