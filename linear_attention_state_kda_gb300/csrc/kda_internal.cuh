@@ -50,6 +50,7 @@ struct ChunkParams {
   uint32_t* status;       // optional device status word
   int package;            // 1 = package mode
   uint64_t flag_wait_ns;  // limit of a walk's wait for a record's ready flag (0: default)
+  int discard;            // the walk drops each record's L2 lines once done (records private)
 };
 
 // Chunk size of every chunked kernel.

@@ -203,6 +203,12 @@ __device__ __forceinline__ void bulk_wait0() {
 }
 // Waits until all but the most recently committed bulk-store group of this thread completed.
 
+// Drops the 128-byte L2 line at `p` (global, 128-byte aligned) without writing it back: its
+// contents become undefined. For scratch that no one reads again.
+__device__ __forceinline__ void discard_l2_line(const void* p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"((uint64_t)p) : "memory");
+}
+
 // ---------------------------------------------------------------- cross-CTA flags
 // Orders this thread's generic-proxy accesses of global memory with its async-proxy ones.
 __device__ __forceinline__ void fence_proxy_async_global() {
