@@ -145,21 +145,28 @@ KDA_API kda_status kda_segment_package(kda_dtype dt, int n_segs, int total_token
 
 /*
  * kda_package_scan: segmented exclusive prefix over packages with the composition
- * (M2, D2) o (M1, D1) = (M2 M1, M2 D1 + D2), evaluated as a work-efficient (Blelloch)
- * up-sweep/down-sweep tree per (sequence, head), then applied to the entry state:
+ * (M2, D2) o (M1, D1) = (M2 M1, M2 D1 + D2), applied to the entry state:
  *     seg_init[j]    = M_{<j} S_init + D_{<j}   (the state entering segment j)
  *     final_state[s] = M_{all} S_init + D_{all} (the state after the sequence)
  * Segments [seq_seg_offsets[s], seq_seg_offsets[s+1]) belong to sequence s, in token order.
+ * Two schedules of the same prefix (equal up to rounding order): for dk = dv = 128 and
+ * max_segs_per_seq <= 256, the sequential chain S_{j+1} = M_j S_j + D_j (one dependent product
+ * per segment, the state's columns split over CTAs); otherwise a work-efficient (Blelloch)
+ * up-sweep/down-sweep tree per (sequence, head).
  *   seq_seg_offsets   device int32 [n_seqs + 1] (last = n_segs).
- *   max_segs_per_seq  host upper bound on any sequence's segment count (1..65536); it sets
- *                     the number of tree levels launched.
+ *   max_segs_per_seq  host upper bound on any sequence's segment count (1..65536); it picks
+ *                     the schedule and sets the number of tree levels launched. A sequence
+ *                     with more segments is malformed (KDA_STATUS_BAD_OFFSETS).
  *   init_state        [n_seqs, H, dk, dv] or NULL (zeros).
  *   seg_init          [n_segs, H, dk, dv] output.  final_state [n_seqs, H, dk, dv] or NULL.
+ *   M, D, init_state, seg_init, final_state: 16-byte aligned.
  *   workspace         device scratch of at least kda_package_scan_workspace(...) bytes,
  *                     256-byte aligned; contents need not be initialised. It holds the
  *                     padded tree: n_seqs * (3/2) * P2 * H packages of (dk*dk + dk*dv) fp32,
- *                     P2 = max_segs_per_seq rounded up to a power of two.
- *   status            optional device word (KDA_STATUS_BAD_OFFSETS).
+ *                     P2 = max_segs_per_seq rounded up to a power of two (the sequential
+ *                     chain leaves it untouched).
+ *   status            optional device word (KDA_STATUS_BAD_OFFSETS; KDA_STATUS_TIMEOUT if a
+ *                     tensor-core CTA's bounded wait expired).
  * Source: pegainfer PR #970, whale-rendezvous commit message (a Blelloch prefix scan over the
  * packages as the lower-traffic way to combine them).
  */

@@ -486,12 +486,13 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     // ================= A1 = [Kh; Qh] Kb^T; the staging is free: load the next item
     if (tid == 0 && !misc->abort) {
       const uint32_t ida = idesc_make(kFmtTF32, 128, 64, false, false);
+      // one base descriptor per operand, advanced by constants: computing each MMA's
+      // descriptor from the address would put a chain of integer ops in front of every issue
+      const uint64_t dkb = sdesc_sw128(sbase + P_KB, 16, 1024);
 #pragma unroll
-      for (int s = 0; s < 16; ++s) {
-        const uint64_t b =
-            sdesc_sw128(sbase + P_KB + (s >> 2) * P_KB_KB + (s & 3) * 32, 16, 1024);
-        mma_tf32_ts(tbase + TM_A1, tbase + TM_XA + s * 8, b, ida, s > 0);
-      }
+      for (int s = 0; s < 16; ++s)
+        mma_tf32_ts(tbase + TM_A1, tbase + TM_XA + s * 8,
+                    desc_add(dkb, (s >> 2) * P_KB_KB + (s & 3) * 32), ida, s > 0);
       mma_commit(&misc->bar_a);
     }
     if (tid == kLoader && !misc->abort) {
@@ -758,46 +759,46 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     if (tid == 0 && !misc->abort) {
       const uint32_t id64 = idesc_make(kFmtTF32, 128, 64, false, false);
       const uint32_t id128 = idesc_make(kFmtTF32, 128, 128, false, false);
+      const uint64_t dtbt = sdesc_sw128(sbase + P_TBT, 16, 1024);
 #pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const uint32_t kb = (s >> 2) * P_TBT_KB + (s & 3) * 32;
-        mma_tf32_ts(tbase + TM_E, tbase + TM_A1 + s * 8, sdesc_sw128(sbase + P_TBT + kb, 16, 1024),
-                    id64, 1);
-      }
+      for (int s = 0; s < 8; ++s)
+        mma_tf32_ts(tbase + TM_E, tbase + TM_A1 + s * 8,
+                    desc_add(dtbt, (s >> 2) * P_TBT_KB + (s & 3) * 32), id64, 1);
       mma_commit(&misc->bar_p);
       // U0^T = V^T (TB_hi + TB_lo)^T: A is the v staging read MN-major (value channel c of
       // token t at row t; the two 64-channel boxes 8 KiB apart), 16 tokens per K-step
       bool ok = mbar_wait(&misc->bar_v, par);
       if (ok) {
         const uint32_t idv = idesc_make(kFmtBF16, 128, 64, true, false);
+        const uint64_t dv = sdesc_sw128(sbase + P_STG_V, 8192, 1024);
+        const uint64_t dtbn = sdesc_sw128(sbase + P_TBN, 16, 1024);
 #pragma unroll
         for (int s = 0; s < 4; ++s) {
-          const uint64_t a = sdesc_sw128(sbase + P_STG_V + s * 2048, 8192, 1024);
-          mma_f16(tbase + TM_U0T, a, sdesc_sw128(sbase + P_TBN + s * 32, 16, 1024), idv, s > 0);
-          mma_f16(tbase + TM_U0T, a, sdesc_sw128(sbase + P_TBN + 8192 + s * 32, 16, 1024), idv, 1);
+          const uint64_t a = desc_add(dv, s * 2048);
+          mma_f16(tbase + TM_U0T, a, desc_add(dtbn, s * 32), idv, s > 0);
+          mma_f16(tbase + TM_U0T, a, desc_add(dtbn, 8192 + s * 32), idv, 1);
         }
       }
       mma_commit(&misc->bar_u);
       ok = ok && mbar_wait(&misc->bar_p, par);
       tc_fence_after();
       if (ok) {
+        const uint64_t dbe = sdesc_sw128(sbase + P_BE, 16, 1024);
 #pragma unroll
-        for (int s = 0; s < 8; ++s) {
-          const uint32_t kbe = (s >> 2) * P_BE_KB + (s & 3) * 32;
+        for (int s = 0; s < 8; ++s)
           mma_tf32_ts(tbase + TM_R, tbase + TM_E + s * 8,
-                      sdesc_sw128(sbase + P_BE + kbe, 16, 1024), id128, s > 0);
-        }
+                      desc_add(dbe, (s >> 2) * P_BE_KB + (s & 3) * 32), id128, s > 0);
       }
       mma_commit(&misc->bar_r);  // R (and the products before it): the record can start
       if (ok && need_out) {
         ok = mbar_wait(&misc->bar_u, par);
         tc_fence_after();
         if (ok) {
+          const uint64_t dpn = sdesc_sw128(sbase + P_PN, 16, 1024);
 #pragma unroll
           for (int s = 0; s < 8; ++s)
             mma_tf32_ts(tbase + TM_O0T, tbase + TM_U0T + s * 8,
-                        sdesc_sw128(sbase + P_PN + (s >> 2) * 8192 + (s & 3) * 32, 16, 1024),
-                        id64, s > 0);
+                        desc_add(dpn, (s >> 2) * 8192 + (s & 3) * 32), id64, s > 0);
         }
       }
       if (!ok) misc->abort = 1;
@@ -951,10 +952,6 @@ struct StateMisc {
   int abort;
 };
 static_assert(sizeof(StateMisc) <= 256, "misc overflow");
-
-// Shared-memory descriptor advanced by a byte offset (the start-address field is the low 14
-// bits of address >> 4; no carry for offsets that keep the operand inside shared memory).
-__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
 
 // Compute warp w (0..7): TMEM lane quarter w % 4, so state column n = 32 (w % 4) + lane of the
 // tile; half h = w / 4 of the channels (S update) and of the tokens (U and outputs). The issuer

@@ -33,12 +33,12 @@ __host__ __device__ inline int64_t pkg_floats(int dk, int dv) {
 struct Tree {
   float* base;    // [n_seqs][P2][H] packages (M then D)
   float* tmp;     // [n_seqs][P2/2][H] packages
-  int P2, H, dk, dv, n_segs;
+  int P2, H, dk, dv, n_segs, max_segs;
   // Segment range of sequence s, or an empty range if the offsets are malformed.
   __device__ bool seq_range(const int32_t* off, int s, int& first, int& cnt) const {
     first = off[s];
     cnt = off[s + 1] - first;
-    if (first < 0 || cnt < 0 || cnt > P2 || first + cnt > n_segs) {
+    if (first < 0 || cnt < 0 || cnt > max_segs || first + cnt > n_segs) {
       first = 0;
       cnt = 0;
       return false;
@@ -301,13 +301,13 @@ __device__ void tile_product(TileCtx& cx, const float* ad_pkg, const float* bm, 
     if (tid == 0) {
       const uint32_t sb = smem_u32(sm);
       const uint32_t idesc = idesc_make(kFmtTF32, 128, NT, false, false);
-#pragma unroll 1
+      const uint64_t dah = sdesc_sw128(sb + AH, 16, 1024), dal = sdesc_sw128(sb + AL, 16, 1024);
+      const uint64_t dbh = sdesc_sw128(sb + BH, 16, 1024), dbl = sdesc_sw128(sb + BL, 16, 1024);
+#pragma unroll
       for (int s = 0; s < 16; ++s) {
         const uint32_t ka = (s >> 2) * A_KB + (s & 3) * 32, kb = (s >> 2) * B_KB + (s & 3) * 32;
-        const uint64_t ah = sdesc_sw128(sb + AH + ka, 16, 1024);
-        const uint64_t al = sdesc_sw128(sb + AL + ka, 16, 1024);
-        const uint64_t bh = sdesc_sw128(sb + BH + kb, 16, 1024);
-        const uint64_t bl = sdesc_sw128(sb + BL + kb, 16, 1024);
+        const uint64_t ah = desc_add(dah, ka), al = desc_add(dal, ka);
+        const uint64_t bh = desc_add(dbh, kb), bl = desc_add(dbl, kb);
         mma_tf32(cx.tbase, ah, bh, idesc, s > 0 ? 1u : 0u);
         mma_tf32(cx.tbase, ah, bl, idesc, 1);
         mma_tf32(cx.tbase, al, bh, idesc, 1);
@@ -514,6 +514,311 @@ scan_tree_tc(Tree t, const int32_t* seq_off, const float* M, const float* D, con
 
 }  // namespace tc
 
+// ------------------------------------------------------------ sequential chain
+// For the segment counts of real prompts (a 2048-token segment floor gives tens of segments per
+// sequence) the plain left fold is the faster schedule: S_0 = S_init, seg_init[j] = S_j,
+// S_{j+1} = M_j S_j + D_j, final = S_cnt, one dependent 128 x 128 x 128 product per segment
+// (the tree has 2 log2 P dependent levels, each a heavier product spread over only 4 CTAs).
+// The columns of the state are independent, so a CTA owns 64 of them and needs nothing from
+// another CTA. Per step, on tcgen05 in 3xTF32 (A = M_j from TMEM, B = S_j from shared memory):
+//   * warps 8..11 stream M_j in K-blocks of 32 columns into a ring of 3 TMEM slots (hi and lo
+//     parts), each block as soon as the MMAs that read its slot's last occupant are done, so
+//     the next step's operand is in place before its state is;
+//   * warps 0..7 read the accumulator, add D_j, write S_{j+1} out (seg_init or the final state)
+//     and store its hi / lo parts transposed as the next B operand; then one thread issues the
+//     next step's 48 MMAs.
+namespace seqtc {
+
+using namespace ptx;
+
+constexpr int DK = 128;
+constexpr int NT = 64;                       // state columns per CTA
+constexpr int kThreads = 384;                // 8 state warps + 4 M warps
+constexpr uint32_t B_KB = NT * 128;          // B operand K-block: 64 rows x 128 B
+constexpr uint32_t BH = 0, BL = 4 * B_KB;
+// per-warp staging of a 32-row x 128-byte tile (12 warps x 4 KiB), 128-byte swizzle: global
+// memory is read and written in whole 512-byte runs, each thread's row in shared memory
+constexpr uint32_t STG = 8 * B_KB;
+constexpr uint32_t SMEM = STG + 12 * 4096 + 1024;  // + alignment slack
+constexpr int kSlots = 3;                    // TMEM ring of M K-blocks
+constexpr uint32_t TM_ACC = 0, TM_SLOT = NT, kTmemCols = 256;
+static_assert(TM_SLOT + kSlots * 64 <= kTmemCols, "TMEM overflow");
+
+__device__ __forceinline__ float hi(float x) {
+  return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
+// Tile of 32 rows x 32 floats (row stride `ld` floats) between global memory and a warp's
+// staging buffer: lane l moves rows 4u + l / 8, 16-byte chunk l % 8 (coalesced); then each lane
+// owns row l. The 128-byte swizzle keeps both access patterns free of bank conflicts.
+__device__ __forceinline__ uint32_t stg_off(int row, int chunk) {
+  return (uint32_t)row * 128u + ((uint32_t)(chunk ^ (row & 7)) << 4);
+}
+__device__ __forceinline__ void tile_ld(const float* src, int64_t ld, int lane, float4* g) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    g[u] = *reinterpret_cast<const float4*>(src + (int64_t)(4 * u + (lane >> 3)) * ld +
+                                            (lane & 7) * 4);
+}
+__device__ __forceinline__ void stage_in(uint8_t* stg, const float4* g, int lane) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    *reinterpret_cast<float4*>(stg + stg_off(4 * u + (lane >> 3), lane & 7)) = g[u];
+}
+__device__ __forceinline__ void row_out(const uint8_t* stg, int lane, float* v) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const float4 x = *reinterpret_cast<const float4*>(stg + stg_off(lane, u));
+    v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+  }
+}
+__device__ __forceinline__ void row_in(uint8_t* stg, int lane, const float* v) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    *reinterpret_cast<float4*>(stg + stg_off(lane, u)) =
+        make_float4(v[4 * u], v[4 * u + 1], v[4 * u + 2], v[4 * u + 3]);
+}
+__device__ __forceinline__ void tile_st(float* dst, int64_t ld, int lane, const uint8_t* stg) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    *reinterpret_cast<float4*>(dst + (int64_t)(4 * u + (lane >> 3)) * ld + (lane & 7) * 4) =
+        *reinterpret_cast<const float4*>(stg + stg_off(4 * u + (lane >> 3), lane & 7));
+}
+
+// Named barrier 1 over the 256 state threads; returns whether any of them passed true.
+__device__ __forceinline__ bool state_bar_or(bool x) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 q, %1, 0;\n\t"
+      "bar.red.or.pred p, 1, 256, q;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)x)
+      : "memory");
+  return r != 0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+scan_seq_tc(const int32_t* seq_off, int n_segs, int max_segs, int H, const float* M,
+            const float* D, const float* init, float* seg_init, float* final_state,
+            uint32_t* status) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  __shared__ uint64_t full[kSlots], empty[kSlots], acc_bar, drain;
+  __shared__ uint32_t tslot;
+  __shared__ int abort_flag;
+  const int tile = blockIdx.x, h = blockIdx.y, s = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q = warp & 3;
+  const int r = q * 32 + lane;  // row of the state (and of M) this thread's TMEM lane holds
+  const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+  if (warp == 0) {
+    tmem_alloc(&tslot, kTmemCols);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(&full[i], 4);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(&acc_bar, 1);
+    mbar_init(&drain, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tslot;
+  const uint32_t sbase = smem_u32(sm);
+  uint8_t* stg = sm + STG + warp * 4096;
+
+  int first = seq_off[s], cnt = seq_off[s + 1] - first;
+  if (first < 0 || cnt < 0 || cnt > max_segs || first + cnt > n_segs) {
+    if (tile == 0 && h == 0 && tid == 0 && status) atomicOr(status, KDA_STATUS_BAD_OFFSETS);
+    first = 0;
+    cnt = 0;
+  }
+  const int64_t sd = (int64_t)DK * DK;
+  auto fail = [&]() {
+    abort_flag = 1;
+    if (status) atomicOr(status, KDA_STATUS_TIMEOUT);
+  };
+
+  if (warp < 8) {
+    // ------------------------------------------------ state warps: row r, 32 columns
+    const int cb = (warp >> 2) * 32;
+    const int col = tile * NT + cb;  // first global state column of this thread
+    auto ld8 = [&](const float* src, float* v) {
+      const float4* p = reinterpret_cast<const float4*>(src);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4 x = p[u];
+        v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+      }
+    };
+    // a state (or D) tile of this warp: rows 32 q .., columns col .. col + 31
+    const int64_t toff = (int64_t)(q * 32) * DK + col;
+    auto put = [&](float* base, const float* v) {  // v = this lane's row -> global, coalesced
+      __syncwarp();
+      row_in(stg, lane, v);
+      __syncwarp();
+      tile_st(base + toff, DK, lane, stg);
+    };
+    auto get_d = [&](int seg, float* d) {  // D_seg's tile -> this lane's row
+      float4 g[8];
+      tile_ld(D + ((int64_t)seg * H + h) * sd + toff, DK, lane, g);
+      __syncwarp();
+      stage_in(stg, g, lane);
+      __syncwarp();
+      row_out(stg, lane, d);
+    };
+    // B = S (row n = state column, K = state row r), split hi / lo, transposed
+    auto store_b = [&](const float* v) {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const uint32_t off = sw128_off32((uint32_t)(cb + j), (uint32_t)r, B_KB);
+        const float hh = hi(v[j]);
+        *reinterpret_cast<float*>(sm + BH + off) = hh;
+        *reinterpret_cast<float*>(sm + BL + off) = v[j] - hh;
+      }
+    };
+    auto issue = [&](int j) {  // one thread: S_{j+1} = M_j S_j in the accumulator
+      const uint32_t idesc = idesc_make(kFmtTF32, 128, NT, false, false);
+      const uint64_t dbh = sdesc_sw128(sbase + BH, 16, 1024);
+      const uint64_t dbl = sdesc_sw128(sbase + BL, 16, 1024);
+#pragma unroll
+      for (int kb = 0; kb < 4; ++kb) {
+        const int b = 4 * j + kb, slot = b % kSlots, use = b / kSlots;
+        if (!mbar_wait_relaxed_or(&full[slot], (uint32_t)use & 1u, &abort_flag)) {
+          fail();
+          return;
+        }
+        tc_fence_after();
+        const uint32_t a = tbase + TM_SLOT + (uint32_t)slot * 64u;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bh = desc_add(dbh, kb * B_KB + ks * 32);
+          const uint64_t bl = desc_add(dbl, kb * B_KB + ks * 32);
+          mma_tf32_ts(tbase + TM_ACC, a + ks * 8, bh, idesc, (kb | ks) != 0 ? 1u : 0u);
+          mma_tf32_ts(tbase + TM_ACC, a + ks * 8, bl, idesc, 1u);
+          mma_tf32_ts(tbase + TM_ACC, a + 32 + ks * 8, bh, idesc, 1u);
+        }
+        mma_commit(&empty[slot]);
+      }
+      mma_commit(&acc_bar);
+    };
+    float v[32], d[32];
+    if (init) {
+      ld8(init + ((int64_t)s * H + h) * sd + (int64_t)r * DK + col, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+    }
+    if (cnt == 0) {
+      if (final_state) put(final_state + ((int64_t)s * H + h) * sd, v);
+    } else {
+      put(seg_init + ((int64_t)first * H + h) * sd, v);
+      store_b(v);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      state_bar_or(false);
+      tc_fence_after();
+      if (tid == 0) issue(0);
+      get_d(first, d);
+      for (int j = 0; j < cnt; ++j) {
+        __syncwarp();
+        bool ok = mbar_wait_relaxed_or(&acc_bar, (uint32_t)j & 1u, &abort_flag);
+        ok = __all_sync(0xFFFFFFFFu, ok);
+        tc_fence_after();
+        const bool last = j + 1 == cnt;
+        if (ok) {
+          tmem_ld32(tbase + lane_base + TM_ACC + cb, v);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) v[e] += d[e];
+          if (!last) {
+            store_b(v);
+            fence_proxy_async_smem();
+          }
+        } else if (lane == 0) {
+          fail();
+        }
+        tc_fence_before();
+        const bool stop = state_bar_or(!ok);
+        tc_fence_after();
+        if (stop) break;
+        if (!last && tid == 0) issue(j + 1);
+        float* out = last ? (final_state ? final_state + ((int64_t)s * H + h) * sd : nullptr)
+                          : seg_init + ((int64_t)(first + j + 1) * H + h) * sd;
+        if (out) put(out, v);
+        if (!last) get_d(first + j + 1, d);
+      }
+    }
+  } else if (cnt > 0) {
+    // ------------------------------------------------ M warps: row r, K-blocks of 32 columns
+    const int nb = 4 * cnt;
+    auto ldm = [&](int b, float4* x) {  // block b of this warp's 32 rows, coalesced
+      tile_ld(M + ((int64_t)(first + b / 4) * H + h) * sd + (int64_t)(q * 32) * DK + (b & 3) * 32,
+              DK, lane, x);
+    };
+    // three register buffers in fixed roles (the loop is unrolled by three so that no buffer
+    // is copied: a copy would wait for its loads), each block's loads two blocks ahead
+    float4 buf[3][8];
+    ldm(0, buf[0]);
+    if (nb > 1) ldm(1, buf[1]);
+    bool stop = false;
+    for (int b0 = 0; b0 < nb && !stop; b0 += kSlots) {
+#pragma unroll
+      for (int k = 0; k < kSlots; ++k) {
+        const int b = b0 + k;  // block b goes to slot k (kSlots = 3 divides b0)
+        if (b >= nb || stop) break;
+        if (b + 2 < nb) ldm(b + 2, buf[(k + 2) % kSlots]);
+        const int use = b / kSlots;
+        if (use > 0 && !mbar_wait_relaxed_or(&empty[k], (uint32_t)(use - 1) & 1u, &abort_flag)) {
+          if (lane == 0) fail();
+          stop = true;
+          break;
+        }
+        tc_fence_after();
+        float xh[32], xl[32];
+        __syncwarp();
+        stage_in(stg, buf[k], lane);
+        __syncwarp();
+        row_out(stg, lane, xl);  // row r of the block
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          xh[c] = hi(xl[c]);
+          xl[c] -= xh[c];
+        }
+        const uint32_t a = tbase + lane_base + TM_SLOT + (uint32_t)k * 64u;
+        tmem_st32_nowait(a, xh);
+        tmem_st32_nowait(a + 32, xl);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_relaxed(&full[k]);
+      }
+    }
+  }
+  // every MMA this CTA issued has completed before TMEM is freed
+  if (tid == 0) {
+    mma_commit(&drain);
+    if (!mbar_wait(&drain, 0) && status) atomicOr(status, KDA_STATUS_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tbase, kTmemCols);
+}
+
+}  // namespace seqtc
+
+// Sequences of at most this many segments take the sequential chain (one product per segment);
+// longer ones the tree.
+constexpr int kSeqScanMaxSegs = 256;
+constexpr int DK_TILES_SEQ = 128 / seqtc::NT;
+
 int next_pow2(int x) {
   int p = 1;
   while (p < x) p <<= 1;
@@ -531,6 +836,7 @@ kda_status run_tc(int n_seqs, int n_segs, const int32_t* seq_off, int max_segs, 
   t.dk = DK;
   t.dv = DV;
   t.n_segs = n_segs;
+  t.max_segs = max_segs;
   t.base = (float*)ws;
   t.tmp = t.base + (int64_t)n_seqs * t.P2 * H * pkg_floats(DK, DV);
   const int smem = (int)tc::SMEM;
@@ -552,6 +858,7 @@ kda_status run(int n_seqs, int n_segs, const int32_t* seq_off, int max_segs, int
   t.dk = DK;
   t.dv = DV;
   t.n_segs = n_segs;
+  t.max_segs = max_segs;
   t.base = (float*)ws;
   t.tmp = t.base + (int64_t)n_seqs * t.P2 * H * pkg_floats(DK, DV);
   const int rb = DK / kRows;
@@ -585,6 +892,15 @@ kda_status launch_scan(int n_seqs, int n_segs, const int32_t* seq_seg_offsets, i
                        void* ws, size_t ws_bytes, uint32_t* status, cudaStream_t s) {
   (void)ws_bytes;
   if (n_seqs == 0) return KDA_OK;
+  if (dk == 128 && dv == 128 && max_segs <= kSeqScanMaxSegs && n_seqs <= 65535 &&
+      H <= 65535) {
+    const int smem = (int)seqtc::SMEM;
+    cudaFuncSetAttribute(seqtc::scan_seq_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    seqtc::scan_seq_tc<<<dim3(DK_TILES_SEQ, H, n_seqs), seqtc::kThreads, smem, s>>>(
+        seq_seg_offsets, n_segs, max_segs, H, M, D, init_state, seg_init, final_state, status);
+    count_launches(1);
+    return check_launch("kda_package_scan (sequential, tensor cores)");
+  }
   if (dk == 128 && dv == 128 && (int64_t)n_seqs * H <= 65535)
     return run_tc(n_seqs, n_segs, seq_seg_offsets, max_segs, H, M, D, init_state, seg_init,
                   final_state, ws, status, s);

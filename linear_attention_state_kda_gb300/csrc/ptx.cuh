@@ -475,6 +475,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t start, uint32_t lbo, ui
   return d;
 }
 
+// A descriptor `bytes` further on (a multiple of 16; the start field cannot carry over for
+// shared-memory addresses below 256 KiB).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 // Byte offset of 32-bit element (row, col) in a K-major 128B-swizzled tile whose K-blocks
 // (32 elements = 128 B of each row) are `kblk_stride` bytes apart: row = M/N index,
 // col = K index.
