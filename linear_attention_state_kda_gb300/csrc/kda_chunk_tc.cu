@@ -1226,21 +1226,6 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
         __syncwarp();
         if (lane == 0 && j + 1 < nch) mbar_arrive_relaxed(&misc->s_ready[hf]);
       }
-      if (p.discard) {
-        // the chunk's record is read no more (both products done, U0^T / O0^T in registers):
-        // drop its lines from L2 instead of letting them be written back, 4-5 lines a thread
-        const int64_t item = (int64_t)(slot0 + j) * H + h;
-        const int ct = tid;  // 0 .. 255 (compute warps)
-        const uint8_t* r_wq = reinterpret_cast<const uint8_t*>(ws.wq + item * 128 * 128);
-        const uint8_t* r_kb = reinterpret_cast<const uint8_t*>(ws.kbt + item * 128 * 64);
-        const uint8_t* r_u0 = reinterpret_cast<const uint8_t*>(ws.u0 + item * 8192);
-        const uint8_t* r_o0 = reinterpret_cast<const uint8_t*>(ws.o0 + item * 8192);
-        for (int l = ct; l < 512; l += 256) discard_l2_line(r_wq + (int64_t)l * 128);
-        discard_l2_line(r_kb + (int64_t)ct * 128);
-        discard_l2_line(r_u0 + (int64_t)ct * 128);
-        if (ct < 128) discard_l2_line(r_o0 + (int64_t)ct * 128);
-        if (ct < 4) discard_l2_line(reinterpret_cast<const uint8_t*>(ws.dec + item * 128) + ct * 128);
-      }
       // outputs, after the state update has released the next chunk's X product: token t of
       // column n (32 lanes = 64 contiguous bytes of one token's row); none once the CTA gave up
       // Lanes l and l ^ 1 trade halves so that the even lane holds columns (n, n + 1) of the
@@ -1257,6 +1242,22 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
           const int t = hf * 32 + 2 * i + (odd ? 1 : 0);
           if (t < nvalid) *reinterpret_cast<uint32_t*>(o + (int64_t)t * H * DK) = pair;
         }
+      }
+      if (p.discard) {
+        // the chunk's record is read no more (both products done, U0^T / O0^T in registers):
+        // drop its lines from L2 instead of letting them be written back, 4-5 lines a thread
+        // (after the stores, so that these waits overlap the next chunk's X product)
+        const int64_t item = (int64_t)(slot0 + j) * H + h;
+        const int ct = tid;  // 0 .. 255 (compute warps)
+        const uint8_t* r_wq = reinterpret_cast<const uint8_t*>(ws.wq + item * 128 * 128);
+        const uint8_t* r_kb = reinterpret_cast<const uint8_t*>(ws.kbt + item * 128 * 64);
+        const uint8_t* r_u0 = reinterpret_cast<const uint8_t*>(ws.u0 + item * 8192);
+        const uint8_t* r_o0 = reinterpret_cast<const uint8_t*>(ws.o0 + item * 8192);
+        for (int l = ct; l < 512; l += 256) discard_l2_line(r_wq + (int64_t)l * 128);
+        discard_l2_line(r_kb + (int64_t)ct * 128);
+        discard_l2_line(r_u0 + (int64_t)ct * 128);
+        if (ct < 128) discard_l2_line(r_o0 + (int64_t)ct * 128);
+        if (ct < 4) discard_l2_line(reinterpret_cast<const uint8_t*>(ws.dec + item * 128) + ct * 128);
       }
       if (misc->abort) break;
     }
@@ -1495,9 +1496,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
   const bool do_prep = (phases & kPhasePrep) != 0, do_state = (phases & kPhaseState) != 0;
   ChunkParams pp = p;
   if (pp.flag_wait_ns == 0) pp.flag_wait_ns = 4000000000ull;
-  // a call that both prepares and walks owns its records: the walk can drop them from L2
-  // (one reader per record: not in package mode, where the M and D tiles read the same one)
-  pp.discard = (do_prep && do_state && !p.package) ? 1 : 0;
+  pp.discard = 0;
   CUtensorMap mq, mk, mv, mg, mb, mwq, mkbt, mdec, swq;
   const uint64_t rows128 = (uint64_t)n_items * 128;
   bool maps_ok = true;
@@ -1538,6 +1537,11 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
     if (e != cudaSuccess)
       return set_error(KDA_ERR_CUDA, std::string("tensor-core chunk path flags: ") +
                                          cudaGetErrorString(e));
+    // the fused launch owns its records and its walks read them while they are still in L2:
+    // the walk drops each one once read (one reader per record: not in package mode, where the
+    // M and D tiles read the same one; with two launches the records have long left L2)
+    ChunkParams pf = pp;
+    pf.discard = p.package ? 0 : 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)sms);
     cfg.blockDim = dim3(kStateThreads);
@@ -1548,7 +1552,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, chunk_fused_kernel, pp, mq, mk, mv, mg, mb, swq, mwq, mkbt, mdec,
+    e = cudaLaunchKernelEx(&cfg, chunk_fused_kernel, pf, mq, mk, mv, mg, mb, swq, mwq, mkbt, mdec,
                            ws, (int)n_items, (int)n_state, flags);
     if (e == cudaSuccess) {
       count_launches(1);
