@@ -381,28 +381,10 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       };
       auto kb_out = [&](int c0, const float* x, const float* kv, const float* er) {
         float kb[8];
-        if (!any_strong) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            kb[e] = (valid ? kv[e] : 0.0f) * ex2_approx(-x[e]);
-            kbt_out[(size_t)(c0 + e) * C] = kb[e] * er[e];
-          }
-        } else {
-          // a strong channel has no share in the A1 product (Kb = 0); its Kb' = k 2^(gamma_C -
-          // gamma) directly (frame 0: x = gamma), a factor at most 1
-          const uint32_t bits = (smask[c0 >> 5] >> (c0 & 31)) & 0xFFu;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float kk = valid ? kv[e] : 0.0f;
-            if ((bits >> e) & 1u) {
-              kb[e] = 0.0f;
-              const float gc = misc->part[0][c0 + e] + misc->part[1][c0 + e];
-              kbt_out[(size_t)(c0 + e) * C] = kk * ex2_approx(gc - x[e]);
-            } else {
-              kb[e] = kk * ex2_approx(-x[e]);
-              kbt_out[(size_t)(c0 + e) * C] = kb[e] * er[e];
-            }
-          }
+        for (int e = 0; e < 8; ++e) {
+          kb[e] = (valid ? kv[e] : 0.0f) * ex2_approx(-x[e]);
+          kbt_out[(size_t)(c0 + e) * C] = kb[e] * er[e];
         }
         *reinterpret_cast<float4*>(sm + P_KB + sw128_off32(t, c0, P_KB_KB)) =
             make_float4(kb[0], kb[1], kb[2], kb[3]);
@@ -410,7 +392,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
             make_float4(kb[4], kb[5], kb[6], kb[7]);
       };
       if (qd < 2) {
-#pragma unroll 2
+#pragma unroll 1
         for (int cb = 0; cb < 64; cb += 16) {
           float kh[16];
 #pragma unroll
@@ -434,7 +416,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
           tmem_st16(tbase + lane_base + TM_XA + chh * 64 + cb, kh);
         }
       } else {
-#pragma unroll 2
+#pragma unroll 1
         for (int cb = 0; cb < 64; cb += 16) {
           float qh[16];
 #pragma unroll
@@ -470,6 +452,29 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
           }
           tmem_st16(tbase + lane_base + TM_XA + chh * 64 + cb, qh);
         }
+      }
+    }
+    if (any_strong) {
+      // strong channels, rewritten by the thread that wrote them above (key-row threads: the
+      // first 32 channels of their half, query-row threads the last 32): no share in the A1
+      // product (Kb = 0), and Kb' = k 2^(gamma_C - gamma) directly (frame 0: the staging holds
+      // gamma), a factor at most 1. Kept apart so that the hot loops above carry no branch.
+      const int t = (qd & 1) * 32 + lane;
+      const int cw = chh * 64 + (qd < 2 ? 0 : 32);  // 32 channels, one mask word
+      float* kbt_out = ws.kbt + (size_t)item * DK * C + t;
+      for (uint32_t m = smask[cw >> 5]; m; m &= m - 1u) {
+        const int c = cw + __ffs(m) - 1;
+        const uint32_t tsw = (uint32_t)t & 7u;
+        const float gam = *f32at(sm, P_STG_G + (uint32_t)(c >> 5) * 8192u + (uint32_t)t * 128u +
+                                         (((((uint32_t)c & 31u) >> 2) ^ tsw) << 4) +
+                                         ((uint32_t)c & 3u) * 4u);
+        const float kk = t < n ? __bfloat162float(*reinterpret_cast<const __nv_bfloat16*>(
+                                     sm + P_STG_K + (uint32_t)(c >> 6) * 8192u + (uint32_t)t * 128u +
+                                     (((((uint32_t)c & 63u) >> 3) ^ tsw) << 4) +
+                                     ((uint32_t)c & 7u) * 2u))
+                               : 0.0f;
+        *f32at(sm, P_KB + sw128_off32(t, c, P_KB_KB)) = 0.0f;
+        kbt_out[(size_t)c * C] = kk * ex2_approx(misc->part[0][c] + misc->part[1][c] - gam);
       }
     }
     if (qd >= 2 && !((qd & 1) * 32 + lane < n)) {
