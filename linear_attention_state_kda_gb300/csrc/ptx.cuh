@@ -135,15 +135,6 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
-// Prefetch a 3-D tile into L2 (no shared-memory destination, no completion tracking).
-__device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* m, int c0, int c1,
-                                                   int c2) {
-  asm volatile(
-      "cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"((uint64_t)m),
-      "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
 // Prefetch `bytes` (multiple of 16, 16-byte aligned) of global memory into L2.
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"((uint64_t)src), "r"(bytes)
@@ -174,15 +165,6 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* s
   asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::
                    "l"((uint64_t)m),
                "r"(c0), "r"(c1), "r"(smem_u32(src))
-               : "memory");
-}
-// 3-D tiled bulk-tensor store from shared memory (see tma_store_2d).
-// Contiguous bulk copy shared -> global (both 16-byte aligned, size a multiple of 16), tracked
-// by this thread's bulk groups.
-__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
-                   (uint64_t)dst),
-               "r"(smem_u32(src)), "r"(bytes)
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() {
@@ -356,21 +338,6 @@ __device__ __forceinline__ void tmem_st32_nowait(uint32_t taddr, const float* v)
       "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
-}
-
-// TMEM -> registers, 16 consecutive 32-bit columns.
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // registers -> TMEM: lane (warp's quarter + laneid), 32 consecutive 32-bit columns.
