@@ -15,9 +15,10 @@
 // both are arguments.
 //
 // HBM-bound stencil (W <= 4 multiply-adds per element). A CTA owns one tile of R tokens of
-// one sequence (R = 32 for bf16, 16 for fp32) and 512 channels. It first copies the tile's
-// rows and its W - 1 halo rows into shared memory with cp.async (16-byte copies that hold no
-// registers, so ~36 KiB per CTA and ~5 CTAs per SM are in flight), then each thread computes
+// one sequence (R = 32 for bf16, 16 for fp32) and 512 channels. One thread first brings the
+// tile's rows and its W - 1 halo rows into shared memory with bulk tensor copies (boxes of
+// [W - 1 + R rows][512 B] over the packed rows, completion on an mbarrier, bounded wait;
+// ~35 KiB per CTA, so ~6 CTAs per SM have their copies in flight), then each thread computes
 // 4 consecutive channels of every row from shared memory and stores them with streaming
 // stores (a warp writes 32 x 4 contiguous elements per row). With bf16 the SiLU costs one
 // special-function operation per element (see act()). The halo rows are the sequence's
