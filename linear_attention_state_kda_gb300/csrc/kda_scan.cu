@@ -4,19 +4,24 @@
 // two consecutive packages combine as (M2, D2) o (M1, D1) = (M2 M1, M2 D1 + D2) ("apply 1,
 // then 2"). pegainfer PR #970 (whale-rendezvous and fabric data-plane commit messages)
 // exchanges these KDA (M,D) packages between context-parallel ranks and names a Blelloch
-// prefix scan as the lower-traffic way to combine them; this file runs that work-efficient
-// scan on one GPU, per (sequence, head):
-//   * the sequence's packages are copied into a power-of-two tree, padded with (I, 0);
-//   * up-sweep: at stride d, node i (i+1 multiple of 2d) becomes a[i] o a[i-d];
-//   * the root (the whole sequence's package) gives the exit state, then becomes (I, 0);
-//   * down-sweep: at stride d, (a[i-d], a[i]) <- (a[i], a[i-d] o a[i]);
-//   * leaf j then holds the exclusive prefix (M_<j, D_<j), and the segment's entry state is
-//     M_<j S_init + D_<j.
-// Every combine is a dk x dk times dk x (dk + dv) product. For dk = dv = 128 the whole tree of
-// a (sequence, head) runs in one launch, one cluster of 4 CTAs per tree, every combine and
-// entry-state application on tcgen05 tensor cores with a 3xTF32 split (namespace tc below).
-// The CUDA-core version (dk = 64) has a CTA compute a 32-row block of one combine's result: it
-// reads only its own rows of the left operand, so that storage can take the result in place.
+// prefix scan as the lower-traffic way to combine them. On one GPU this file offers two
+// schedules of the same prefix (equal up to rounding order), per (sequence, head):
+//   * the sequential chain (namespace seqtc, dk = dv = 128, up to 256 segments per sequence):
+//     S_0 = S_init, seg_init[j] = S_j, S_{j+1} = M_j S_j + D_j, one dependent tensor-core
+//     product per segment, the state's columns split over CTAs;
+//   * the work-efficient (Blelloch) tree, for longer sequences and for dk = dv = 64:
+//       - the sequence's packages are copied into a power-of-two tree, padded with (I, 0);
+//       - up-sweep: at stride d, node i (i+1 multiple of 2d) becomes a[i] o a[i-d];
+//       - the root (the whole sequence's package) gives the exit state, then becomes (I, 0);
+//       - down-sweep: at stride d, (a[i-d], a[i]) <- (a[i], a[i-d] o a[i]);
+//       - leaf j then holds the exclusive prefix (M_<j, D_<j), and the segment's entry state
+//         is M_<j S_init + D_<j.
+//     Every combine is a dk x dk times dk x (dk + dv) product. For dk = dv = 128 the whole
+//     tree of a (sequence, head) runs in one launch, one cluster of 4 CTAs per tree, every
+//     combine and entry-state application on tcgen05 tensor cores with a 3xTF32 split
+//     (namespace tc). The CUDA-core version (dk = 64) has a CTA compute a 32-row block of one
+//     combine's result: it reads only its own rows of the left operand, so that storage can
+//     take the result in place.
 #include "kda_internal.cuh"
 #include "ptx.cuh"
 
