@@ -1208,23 +1208,32 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
       if (!mbar_wait_relaxed_or(&misc->bar_y, par, &misc->abort)) misc->abort = 1;
       tc_fence_after();
       {
+        // four pieces of 16 columns, the next piece's loads in flight while the current one is
+        // updated (a load wait covers every load before it, so one piece ahead is the depth)
         const float* dec = f32at(sm, S_DEC + (j % 3) * 512);
-#pragma unroll 1
-        for (int cc = hf * 64; cc < hf * 64 + 64; cc += 32) {
-          uint32_t y[32], sr[32];
-          tmem_ld32_nowait(tbase + lane_base + TS_Y + cc, y);
-          tmem_ld32_nowait(tbase + lane_base + TS_S + cc, sr);
-          tmem_ld_wait();
-          float s[32];
+        const int c0 = hf * 64;
+        uint32_t y[2][16], sr[2][16];
+        tmem_ld16_nowait(tbase + lane_base + TS_Y + c0, y[0]);
+        tmem_ld16_nowait(tbase + lane_base + TS_S + c0, sr[0]);
+        tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(dec + cc + i);
-            s[i] = fmaf(d4.x, __uint_as_float(sr[i]), __uint_as_float(y[i]));
-            s[i + 1] = fmaf(d4.y, __uint_as_float(sr[i + 1]), __uint_as_float(y[i + 1]));
-            s[i + 2] = fmaf(d4.z, __uint_as_float(sr[i + 2]), __uint_as_float(y[i + 2]));
-            s[i + 3] = fmaf(d4.w, __uint_as_float(sr[i + 3]), __uint_as_float(y[i + 3]));
+        for (int k = 0; k < 4; ++k) {
+          const int cc = c0 + 16 * k;
+          if (k + 1 < 4) {
+            tmem_ld16_nowait(tbase + lane_base + TS_Y + cc + 16, y[(k + 1) & 1]);
+            tmem_ld16_nowait(tbase + lane_base + TS_S + cc + 16, sr[(k + 1) & 1]);
           }
-          tmem_st32_nowait(tbase + lane_base + TS_S + cc, s);
+          float s[16];
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dec + cc + i);
+            s[i] = fmaf(d4.x, __uint_as_float(sr[k & 1][i]), __uint_as_float(y[k & 1][i]));
+            s[i + 1] = fmaf(d4.y, __uint_as_float(sr[k & 1][i + 1]), __uint_as_float(y[k & 1][i + 1]));
+            s[i + 2] = fmaf(d4.z, __uint_as_float(sr[k & 1][i + 2]), __uint_as_float(y[k & 1][i + 2]));
+            s[i + 3] = fmaf(d4.w, __uint_as_float(sr[k & 1][i + 3]), __uint_as_float(y[k & 1][i + 3]));
+          }
+          tmem_st16(tbase + lane_base + TS_S + cc, s);
+          if (k + 1 < 4) tmem_ld_wait();
         }
         tmem_st_wait();
         tc_fence_before();
