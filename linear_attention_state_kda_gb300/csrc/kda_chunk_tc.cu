@@ -193,7 +193,7 @@ static_assert(offsetof(PrepMisc, part) % 16 == 0 && offsetof(PrepMisc, erho) % 1
               "vector-loaded arrays must be 16-byte aligned");
 
 // The prep CTA's 256 threads synchronise on named barrier 1 (a fused launch runs them next to
-// a ninth, idle warp).
+// its publishing warp and an idle tenth warp).
 __device__ __forceinline__ void pbar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ void psync() {
   tc_fence_before();
@@ -275,9 +275,11 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     if (it < n_items) issue_tma(t0, hh);
     return it < n_items;
   };
-  // Loads are issued by the loader thread (warp 1), MMAs by thread 0, so that the next item's
-  // loads go out while thread 0 is issuing the A1 product.
-  constexpr int kLoader = 32;
+  // Loads are issued by the loader thread, MMAs by thread 0, so that the next item's loads go
+  // out while thread 0 is issuing the A1 product. The loader sits in warp 5, the warp with the
+  // least work on the item's critical path (its key rows do the light operand iterations first,
+  // and it has no share in the solve's substitution or the extraction's longest rows).
+  constexpr int kLoader = 160;
   bool tma_out = false;  // loader: a load is in flight, completing phase parity tma_par
   uint32_t tma_par = 0;
   bool v_issued = false;  // loader: a v load was issued, the last completing phase v_par
@@ -354,16 +356,20 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     const bool any_strong = (smask[0] | smask[1] | smask[2] | smask[3]) != 0u;
     // ================= operands (row role: token t; key rows in warps 0,1,4,5, query rows
     // in warps 2,3,6,7; channel half chh)
+    // Of the 64 channels of its half, the thread forms Kb, Kb'^T and K'^T for 32 (offset hoff):
+    // key rows the first 32 in half 0 and the last 32 in half 1, query rows the others. Warps
+    // w and w + 4 share an SMSP, so each SMSP runs one warp's heavy iterations next to the
+    // other's light ones.
+    const int hoff = ((qd < 2) == (chh == 0)) ? 0 : 32;
     {
       const int t = (qd & 1) * 32 + lane;
       const bool valid = t < n;
       const uint32_t tsw = (uint32_t)(t & 7);
       const uint32_t grow = P_STG_G + (uint32_t)t * 128u;
       const uint32_t brow = (uint32_t)t * 128u;
-      // Kb (the B operand of A1), Kb'^T (workspace) and K'^T (B operand of R) of token t:
-      // key-row threads cover the first 32 channels of their half, query-row threads the last
-      // 32 (reusing the query's e^x), so both roles issue 96 exponentials and 32 transposed
-      // stores per thread
+      // Kb (the B operand of A1), Kb'^T (workspace) and K'^T (B operand of R) of token t, for
+      // channels hoff .. hoff + 31 of the half (query rows reuse the query's e^x), so both roles
+      // issue 96 exponentials and 32 transposed stores per thread
       float* kbt_out = ws.kbt + (size_t)item * DK * C + t;
       auto load_x = [&](int c0, float* x) {  // gamma - rho of channels c0 .. c0 + 7
         const uint32_t g0 = grow + (uint32_t)(c0 >> 5) * 8192u;
@@ -403,7 +409,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
             load_bf8(P_STG_K, c0, kv);
 #pragma unroll
             for (int e = 0; e < 8; ++e) kh[u + e] = (valid ? kv[e] : 0.0f) * ex2_approx(x[e]);
-            if (cb < 32) {
+            if ((cb & 32) == hoff) {
               const float4 ea = *reinterpret_cast<const float4*>(misc->erho + c0);
               const float4 eb = *reinterpret_cast<const float4*>(misc->erho + c0 + 4);
               const float er[8] = {ea.x, ea.y, ea.z, ea.w, eb.x, eb.y, eb.z, eb.w};
@@ -423,7 +429,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
           for (int u = 0; u < 16; u += 8) {
             const int c0 = chh * 64 + cb + u;
             float x[8], ex[8];
-            if (need_out || cb >= 32) {
+            if (need_out || (cb & 32) == hoff) {
               load_x(c0, x);
 #pragma unroll
               for (int e = 0; e < 8; ++e) ex[e] = ex2_approx(x[e]);
@@ -437,7 +443,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
 #pragma unroll
               for (int e = 0; e < 8; ++e) qh[u + e] = 0.0f;
             }
-            if (cb >= 32) {
+            if ((cb & 32) == hoff) {
               float kv[8];
               load_bf8(P_STG_K, c0, kv);
               const float4 ea = *reinterpret_cast<const float4*>(misc->erho + c0);
@@ -455,12 +461,12 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       }
     }
     if (any_strong) {
-      // strong channels, rewritten by the thread that wrote them above (key-row threads: the
-      // first 32 channels of their half, query-row threads the last 32): no share in the A1
+      // strong channels, rewritten by the thread that wrote them above (channels hoff ..
+      // hoff + 31 of its half): no share in the A1
       // product (Kb = 0), and Kb' = k 2^(gamma_C - gamma) directly (frame 0: the staging holds
       // gamma), a factor at most 1. Kept apart so that the hot loops above carry no branch.
       const int t = (qd & 1) * 32 + lane;
-      const int cw = chh * 64 + (qd < 2 ? 0 : 32);  // 32 channels, one mask word
+      const int cw = chh * 64 + hoff;  // 32 channels, one mask word
       float* kbt_out = ws.kbt + (size_t)item * DK * C + t;
       for (uint32_t m = smask[cw >> 5]; m; m &= m - 1u) {
         const int c = cw + __ffs(m) - 1;
@@ -643,7 +649,8 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       // product a warp-level 3xTF32 MMA (fp32-level accuracy) on a 16 x 8 column half:
       //   T11 = [X00 0; X10 X11], X10 = -X11 A10 X00;  T22 = [X22 0; X32 X33], X32 = -X33 A32 X22
       //   T21 = -T22 (A21 T11)  (A21 = rows 32..63, columns 0..31 of A)
-      // so the chain is four dependent products deep.
+      // so the chain is four dependent products deep; the terms of A21 T11 that need only the
+      // diagonal blocks run next to X10 and X32.
       const int gq = lane >> 2, tq = lane & 3;
       // d += A_IL (16 x 16 block of M, row stride LA) * B rows L*16.., columns n0 .. n0 + 7
       auto blk = [&](float* d, const float* M, int I, int L, const float* B, int bstride, int n0) {
@@ -672,13 +679,27 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
         float e[4] = {0.f, 0.f, 0.f, 0.f};
         blk(e, X, I, I, Pw, 8, 0);
         put(X + I * 16 * LA + n0, LA, e, -1.0f);
+      } else {
+        // meanwhile warps 4..7 form the terms of Y = A21 T11 that do not need X10 (the L = J
+        // term of every tile of the next step), parked in T21's own blocks of X, which are
+        // written only at the end
+#pragma unroll 1
+        for (int tt = 2 * (warp - 4); tt < 2 * (warp - 4) + 2; ++tt) {
+          const int Iy = 2 + (tt >> 2), Jy = (tt >> 1) & 1, ny = Jy * 16 + (tt & 1) * 8;
+          float d[4] = {0.f, 0.f, 0.f, 0.f};
+          blk(d, Akk, Iy, Jy, X + Jy * 16 * LA, LA, ny);
+          put(X + Iy * 16 * LA + ny, LA, d, 1.0f);
+        }
       }
       pbar();
       // warp w: block (I, J) = (2 + w / 4, (w / 2) % 2) of T21, column half w % 2
       const int I2 = 2 + (warp >> 2), J2 = (warp >> 1) & 1, n2 = J2 * 16 + (warp & 1) * 8;
-      {  // Y_IJ = sum_{L=J}^{1} A_IL X_LJ  (A21 T11)
-        float d[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int L = J2; L < 2; ++L) blk(d, Akk, I2, L, X + L * 16 * LA, LA, n2);
+      {  // Y_IJ = sum_{L=J}^{1} A_IL X_LJ  (A21 T11): the L = J term is parked in X; the
+         // L = 1 term of the J = 0 tiles needs X10
+        const float* yp = X + I2 * 16 * LA + n2;
+        float d[4] = {yp[gq * LA + 2 * tq], yp[gq * LA + 2 * tq + 1], yp[(gq + 8) * LA + 2 * tq],
+                      yp[(gq + 8) * LA + 2 * tq + 1]};
+        if (J2 == 0) blk(d, Akk, I2, 1, X + 16 * LA, LA, n2);
         put(Pw, 8, d, 1.0f);
       }
       pbar();
@@ -946,7 +967,9 @@ constexpr uint32_t TS_S = 0;     // 128: S^T
 constexpr uint32_t TS_X = 128;   // 128: X^T
 constexpr uint32_t TS_Y = 256;   // 128: Y^T
 constexpr uint32_t TS_U = 384;   // 64: U^T
-constexpr int kStateThreads = kThreads + 32;  // 8 compute warps + 1 issuer warp
+// 8 compute warps + 1 issuer warp + 1 warp that drops consumed records from L2 (fused launch).
+// Ten warps cost no registers over nine: either way three share an SMSP's register file.
+constexpr int kStateThreads = kThreads + 64;
 
 struct StateMisc {
   uint64_t full[2];     // TMA: chunk j's record landed in stage j & 1 (and decay slot j % 3)
@@ -955,13 +978,15 @@ struct StateMisc {
   uint64_t bar_x, bar_y, bar_drain;
   uint32_t tmem_base;
   int abort;
+  uint32_t consumed;  // compute-warp arrivals: 8 per chunk whose record they are done with
 };
 static_assert(sizeof(StateMisc) <= 256, "misc overflow");
 
 // Compute warp w (0..7): TMEM lane quarter w % 4, so state column n = 32 (w % 4) + lane of the
 // tile; half h = w / 4 of the channels (S update) and of the tokens (U and outputs). The issuer
 // warp (8) waits on the per-half barriers and issues the MMAs and the TMA loads. The compute
-// warps synchronise with it through mbarriers only.
+// warps synchronise with it through mbarriers only. With p.discard, warp 9 drops each chunk's
+// record from L2 once the compute warps have counted it consumed.
 // With `flags`, waits (acquire) for each item's record before reading it.
 __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMap& twq,
                                           const CUtensorMap& tkbt, const CUtensorMap& tdec,
@@ -972,6 +997,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
   StateMisc* misc = reinterpret_cast<StateMisc*>(sm + S_MISC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool issuer = warp == 8;
+  const bool discarder = warp == 9;
   const int qd = warp & 3, hf = (warp >> 2) & 1;
   const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
   const int H = p.H;
@@ -1006,6 +1032,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
     mbar_init(&misc->bar_y, 1);
     mbar_init(&misc->bar_drain, 1);
     misc->abort = 0;
+    misc->consumed = 0;
     fence_mbar_init();
   }
   cta_sync();
@@ -1099,6 +1126,45 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
         mbar_wait(&misc->bar_drain, 0, 100000000ull);
         for (int j = tma_last > 0 ? tma_last - 1 : 0; j <= tma_last; ++j)
           mbar_wait(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u, 100000000ull);
+      }
+    }
+  } else if (discarder) {
+    // ------------------------------------------------------------ discarding warp
+    // The records of a fused launch are read once, from L2: drop each chunk's lines once the
+    // compute warps are done with it (both products complete, U0^T / O0^T in registers), so
+    // that they are never written back to DRAM. A discard holds its thread for a while, so
+    // they run here, off the compute warps' chain; if this warp falls more than two chunks
+    // behind, it skips ahead (a skipped record is merely written back).
+    if (p.discard) {
+      for (int j = 0; j < nch; ++j) {
+        const uint64_t t0 = globaltimer_ns();
+        uint32_t c;
+        while ((c = ld_acquire_cta(&misc->consumed)) < 8u * (uint32_t)(j + 1)) {  // bounded
+          if (*(volatile int*)&misc->abort) break;
+          if (globaltimer_ns() - t0 > 4000000000ull) {
+            misc->abort = 1;
+            break;
+          }
+          __nanosleep(64);
+        }
+        if (*(volatile int*)&misc->abort) break;
+        const int behind = (int)(c >> 3) - (j + 1);
+        if (behind > 2) j += behind - 2;
+        const int64_t item = (int64_t)(slot0 + j) * H + h;
+        const uint8_t* r_wq = reinterpret_cast<const uint8_t*>(ws.wq + item * 128 * 128);
+        const uint8_t* r_kb = reinterpret_cast<const uint8_t*>(ws.kbt + item * 128 * 64);
+        const uint8_t* r_u0 = reinterpret_cast<const uint8_t*>(ws.u0 + item * 8192);
+        const uint8_t* r_o0 = reinterpret_cast<const uint8_t*>(ws.o0 + item * 8192);
+        const uint8_t* r_dc = reinterpret_cast<const uint8_t*>(ws.dec + item * 128);
+        // 512 lines of [W ; Q''], 256 of Kb'^T, 256 of U0^T, 128 of O0^T, 4 of the decays
+        for (int l = lane; l < 1156; l += 32) {
+          const uint8_t* a = l < 512    ? r_wq + l * 128
+                             : l < 768  ? r_kb + (l - 512) * 128
+                             : l < 1024 ? r_u0 + (l - 768) * 128
+                             : l < 1152 ? r_o0 + (l - 1024) * 128
+                                        : r_dc + (l - 1152) * 128;
+          discard_l2_line(a);
+        }
       }
     }
   } else {
@@ -1259,25 +1325,18 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
       }
       if (p.discard) {
         // the chunk's record is read no more (both products done, U0^T / O0^T in registers):
-        // drop its lines from L2 instead of letting them be written back, 4-5 lines a thread
-        // (after the stores, so that these waits overlap the next chunk's X product)
-        const int64_t item = (int64_t)(slot0 + j) * H + h;
-        const int ct = tid;  // 0 .. 255 (compute warps)
-        const uint8_t* r_wq = reinterpret_cast<const uint8_t*>(ws.wq + item * 128 * 128);
-        const uint8_t* r_kb = reinterpret_cast<const uint8_t*>(ws.kbt + item * 128 * 64);
-        const uint8_t* r_u0 = reinterpret_cast<const uint8_t*>(ws.u0 + item * 8192);
-        const uint8_t* r_o0 = reinterpret_cast<const uint8_t*>(ws.o0 + item * 8192);
-        for (int l = ct; l < 512; l += 256) discard_l2_line(r_wq + (int64_t)l * 128);
-        discard_l2_line(r_kb + (int64_t)ct * 128);
-        discard_l2_line(r_u0 + (int64_t)ct * 128);
-        if (ct < 128) discard_l2_line(r_o0 + (int64_t)ct * 128);
-        if (ct < 4) discard_l2_line(reinterpret_cast<const uint8_t*>(ws.dec + item * 128) + ct * 128);
+        // count it consumed for the discarding warp (release: the warp's loads came first)
+        __syncwarp();
+        if (lane == 0) {
+          __threadfence_block();
+          atomicAdd(&misc->consumed, 1u);
+        }
       }
       if (misc->abort) break;
     }
   }
   cta_sync();
-  if (!issuer && !misc->abort) {  // exit state rows c of column n (coalesced across lanes)
+  if (!issuer && !discarder && !misc->abort) {  // exit state rows c of column n (coalesced)
     const int64_t sh = (int64_t)ridx * H + h;
     float* dst = nullptr;
     if (pkg) dst = mcols ? p.M + sh * DK * DK + n : p.D + sh * DK * DK + n;
@@ -1330,7 +1389,8 @@ chunk_fused_kernel(const __grid_constant__ ChunkParams p, const __grid_constant_
     const int tiles = p.package ? 2 : 1;
     state_run(p, twq, tkbt, tdec, ws, b % tiles, (b / tiles) % p.H, b / (tiles * p.H), flags);
   } else {
-    // the prep work uses 8 warps; the ninth publishes the finished items' flags
+    // the prep work uses 8 warps; the ninth publishes the finished items' flags (the tenth,
+    // which discards records in the state CTAs, has nothing to do here)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     PrepMisc* misc = reinterpret_cast<PrepMisc*>(sm + P_MISC);
