@@ -231,7 +231,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     mbar_init(&misc->bar_u, 1);
     mbar_init(&misc->bar_r, 1);
     mbar_init(&misc->bar_e, 1);
-    mbar_init(&misc->bar_drain, 1);
+    mbar_init(&misc->bar_drain, 2);  // both MMA-issuing threads drain into it
     misc->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmk);
@@ -780,8 +780,11 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     tmem_st_wait();
     fence_proxy_async_smem();
     psync();
-    // ================= E = [TB ; 0] + [0 ; Aqk] TB = [TB ; P] and U0^T = V^T TB^T; then
-    // R = E K' = [W ; P K'] and O0^T = U0^T Aqk^T, each issued once its TMEM operand is complete
+    // ================= two independent chains of products, issued at once by two threads (one
+    // thread issues an N = 64 MMA about every 50 cycles, slower than the tensor pipe runs it):
+    //   thread 0:  E = [TB ; 0] + [0 ; Aqk] TB = [TB ; P], then R = E K' = [W ; P K']
+    //   loader:    U0^T = V^T TB^T, then O0^T = U0^T Aqk^T
+    // each product issued once its TMEM operand is complete
     if (tid == 0 && !misc->abort) {
       const uint32_t id64 = idesc_make(kFmtTF32, 128, 64, false, false);
       const uint32_t id128 = idesc_make(kFmtTF32, 128, 128, false, false);
@@ -791,6 +794,18 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
         mma_tf32_ts(tbase + TM_E, tbase + TM_A1 + s * 8,
                     desc_add(dtbt, (s >> 2) * P_TBT_KB + (s & 3) * 32), id64, 1);
       mma_commit(&misc->bar_p);
+      const bool ok = mbar_wait(&misc->bar_p, par);
+      tc_fence_after();
+      if (ok) {
+        const uint64_t dbe = sdesc_sw128(sbase + P_BE, 16, 1024);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          mma_tf32_ts(tbase + TM_R, tbase + TM_E + s * 8,
+                      desc_add(dbe, (s >> 2) * P_BE_KB + (s & 3) * 32), id128, s > 0);
+      }
+      if (!ok) misc->abort = 1;
+      mma_commit(&misc->bar_r);  // the record can start
+    } else if (tid == kLoader && !misc->abort) {
       // U0^T = V^T (TB_hi + TB_lo)^T: A is the v staging read MN-major (value channel c of
       // token t at row t; the two 64-channel boxes 8 KiB apart), 16 tokens per K-step
       bool ok = mbar_wait(&misc->bar_v, par);
@@ -806,26 +821,20 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
         }
       }
       mma_commit(&misc->bar_u);
-      ok = ok && mbar_wait(&misc->bar_p, par);
+      ok = ok && mbar_wait(&misc->bar_u, par);
       tc_fence_after();
-      if (ok) {
-        const uint64_t dbe = sdesc_sw128(sbase + P_BE, 16, 1024);
+      if (ok && misc->nxt[0] < n_items) {
+        issue_v(misc->nxt[1], misc->nxt[3]);  // the U0^T product has read this item's v
+        v_issued = true;
+        v_par = par ^ 1u;
+      }
+      if (ok && need_out) {
+        const uint32_t id64 = idesc_make(kFmtTF32, 128, 64, false, false);
+        const uint64_t dpn = sdesc_sw128(sbase + P_PN, 16, 1024);
 #pragma unroll
         for (int s = 0; s < 8; ++s)
-          mma_tf32_ts(tbase + TM_R, tbase + TM_E + s * 8,
-                      desc_add(dbe, (s >> 2) * P_BE_KB + (s & 3) * 32), id128, s > 0);
-      }
-      mma_commit(&misc->bar_r);  // R (and the products before it): the record can start
-      if (ok && need_out) {
-        ok = mbar_wait(&misc->bar_u, par);
-        tc_fence_after();
-        if (ok) {
-          const uint64_t dpn = sdesc_sw128(sbase + P_PN, 16, 1024);
-#pragma unroll
-          for (int s = 0; s < 8; ++s)
-            mma_tf32_ts(tbase + TM_O0T, tbase + TM_U0T + s * 8,
-                        desc_add(dpn, (s >> 2) * 8192 + (s & 3) * 32), id64, s > 0);
-        }
+          mma_tf32_ts(tbase + TM_O0T, tbase + TM_U0T + s * 8,
+                      desc_add(dpn, (s >> 2) * 8192 + (s & 3) * 32), id64, s > 0);
       }
       if (!ok) misc->abort = 1;
       mma_commit(&misc->bar_e);
@@ -834,11 +843,6 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     if (misc->abort) break;
     if (!mbar_wait(&misc->bar_r, par)) misc->abort = 1;
     tc_fence_after();
-    if (tid == kLoader && !misc->abort && misc->nxt[0] < n_items) {
-      issue_v(misc->nxt[1], misc->nxt[3]);  // the U0^T product has read this item's v
-      v_issued = true;
-      v_par = par ^ 1u;
-    }
     // ================= workspace record: rows staged in shared memory in the boxes'
     // 128-byte swizzle (16-byte chunk j of row r at ((j ^ (r & 7)) << 4)), then bulk stores
     {
@@ -866,6 +870,8 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       // U0^T and O0^T: value column n = TMEM lane, tokens chh * 32 .. + 31, stored straight to
       // the interleaved records (32 lanes = 32 consecutive columns = 512 contiguous bytes)
       const int nn = qd * 32 + lane;
+      if (!mbar_wait(&misc->bar_u, par)) misc->abort = 1;  // long complete: O0^T came after it
+      tc_fence_after();
       {
         float v[32];
         tmem_ld32(tbase + lane_base + TM_U0T + chh * 32, v);
@@ -915,8 +921,8 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     ++k_it;
   }
   if (misc->abort) {
-    if (tid == 0) {
-      if (p.status) atomicOr(p.status, KDA_STATUS_TIMEOUT);
+    if (tid == 0 || tid == kLoader) {  // the two threads that issue MMAs
+      if (tid == 0 && p.status) atomicOr(p.status, KDA_STATUS_TIMEOUT);
       mma_commit(&misc->bar_drain);
       mbar_wait(&misc->bar_drain, 0, 100000000ull);
     }
