@@ -165,7 +165,7 @@ static_assert(P_KB % 1024 == 0 && P_BE % 1024 == 0 && P_TBT % 1024 == 0, "alignm
 constexpr uint32_t TM_XA = 0;    // 128: [Kh ; Qh] (lanes = tokens), the A operand of A1
 constexpr uint32_t TM_A1 = 128;  // 64: [Kh ; Qh] Kb^T -> [0 ; Aqk], the A operand of P
 constexpr uint32_t TM_E = 192;   // 64: [TB ; 0] + [0 ; Aqk] TB = [TB ; P], the A operand of E
-constexpr uint32_t TM_R = 256;   // 128: [TB ; P] K' = [W ; P K']
+constexpr uint32_t TM_R = 256;   // 128: [0 ; -Q'] + [TB ; P] K' = [W ; P K' - Q']
 constexpr uint32_t TM_U0T = 384;  // 64: V^T TB^T = U0^T (lanes = value columns)
 constexpr uint32_t TM_O0T = 448;  // 64: U0^T A_qk^T = (A_qk TB V)^T = (P V)^T
 
@@ -610,6 +610,24 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       }
       tmem_st16(tbase + lane_base + TM_A1 + chh * 32, v);
       tmem_st16(tbase + lane_base + TM_A1 + chh * 32 + 16, v + 16);
+      if (R >= C && need_out) {
+        // the query rows of R start at -Q' = -Qh Diag(e^rho), so that the R product leaves
+        // P K' - Q' = -Q'' / scale there (done here, where the query rows have the least work)
+#pragma unroll 1
+        for (int cc = chh * 64; cc < chh * 64 + 64; cc += 32) {
+          float qh[32];
+          tmem_ld32(tbase + lane_base + TM_XA + cc, qh);
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            const float4 e4 = *reinterpret_cast<const float4*>(misc->erho + cc + j);
+            qh[j] = -qh[j] * e4.x;
+            qh[j + 1] = -qh[j + 1] * e4.y;
+            qh[j + 2] = -qh[j + 2] * e4.z;
+            qh[j + 3] = -qh[j + 3] * e4.w;
+          }
+          tmem_st32(tbase + lane_base + TM_R + cc, qh);
+        }
+      }
       tmem_st_wait();
     }
     psync();
@@ -726,6 +744,13 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
       }
       tmem_st16(tbase + lane_base + TM_E + chh * 32, v);
       tmem_st16(tbase + lane_base + TM_E + chh * 32 + 16, v + 16);
+      if (need_out) {  // the W rows of R start at zero (R accumulates onto all 128 rows)
+        float z[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0.0f;
+        tmem_st32(tbase + lane_base + TM_R + chh * 64, z);
+        tmem_st32(tbase + lane_base + TM_R + chh * 64 + 32, z);
+      }
 #pragma unroll
       for (int j = 0; j < 16; ++j)  // TB^T, first 16 of the 32 columns (the rest: warps qd >= 2)
         *f32at(sm, P_TBT + sw128_off32(chh * 32 + j, r, P_TBT_KB)) = v[j];
@@ -782,7 +807,8 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
     psync();
     // ================= two independent chains of products, issued at once by two threads (one
     // thread issues an N = 64 MMA about every 50 cycles, slower than the tensor pipe runs it):
-    //   thread 0:  E = [TB ; 0] + [0 ; Aqk] TB = [TB ; P], then R = E K' = [W ; P K']
+    //   thread 0:  E = [TB ; 0] + [0 ; Aqk] TB = [TB ; P], then R = [0 ; -Q'] + E K'
+    //              = [W ; P K' - Q'] (with outputs; else R = E K')
     //   loader:    U0^T = V^T TB^T, then O0^T = U0^T Aqk^T
     // each product issued once its TMEM operand is complete
     if (tid == 0 && !misc->abort) {
@@ -801,7 +827,7 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
 #pragma unroll
         for (int s = 0; s < 8; ++s)
           mma_tf32_ts(tbase + TM_R, tbase + TM_E + s * 8,
-                      desc_add(dbe, (s >> 2) * P_BE_KB + (s & 3) * 32), id128, s > 0);
+                      desc_add(dbe, (s >> 2) * P_BE_KB + (s & 3) * 32), id128, need_out || s > 0);
       }
       if (!ok) misc->abort = 1;
       mma_commit(&misc->bar_r);  // the record can start
@@ -854,11 +880,9 @@ __device__ __forceinline__ void prep_run(const ChunkParams& p, const CUtensorMap
         for (int cc = chh * 64; cc < chh * 64 + 64; cc += 32) {
           float v[32];
           tmem_ld32(tbase + lane_base + TM_R + cc, v);
-          if (qd >= 2) {
-            float qh[32];
-            tmem_ld32(tbase + lane_base + TM_XA + cc, qh);
+          if (qd >= 2) {  // R holds P K' - Q' there
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = p.scale * (qh[j] * misc->erho[cc + j] - v[j]);
+            for (int j = 0; j < 32; ++j) v[j] = -p.scale * v[j];
           }
           const uint32_t box = dst + (uint32_t)(cc >> 5) * 8192u + (uint32_t)t * 128u;
 #pragma unroll
