@@ -993,18 +993,21 @@ constexpr uint32_t S_MISC = S_DEC + 3 * 512;
 // carve-out the 28 KiB left for L1 stalled those loads for about a thousand cycles a chunk.
 constexpr uint32_t S_SMEM = S_MISC + 256 + 1024;
 static_assert(S_SMEM + 1024 <= 196 * 1024, "state kernel shared memory above the 196 KiB carve-out");
-constexpr uint32_t TS_S = 0;     // 128: S^T
-constexpr uint32_t TS_X = 128;   // 128: X^T
-constexpr uint32_t TS_Y = 256;   // 128: Y^T
+constexpr uint32_t TS_S = 0;     // 2 x 128: S^T, chunk j reading buffer j & 1 and writing j + 1's
+constexpr uint32_t TS_X = 256;   // 128: X^T
 constexpr uint32_t TS_U = 384;   // 64: U^T
-// 8 compute warps + 1 issuer warp + 1 warp that drops consumed records from L2 (fused launch).
-// Ten warps cost no registers over nine: either way three share an SMSP's register file.
-constexpr int kStateThreads = kThreads + 64;
+// 8 compute warps + 1 MMA-issuing warp + 1 warp that drops consumed records from L2 (fused
+// launch) + 1 warp that loads the records. Eleven warps cost no registers over nine: either way
+// three share an SMSP's register file.
+constexpr int kStateThreads = kThreads + 96;
 
 struct StateMisc {
   uint64_t full[2];     // TMA: chunk j's record landed in stage j & 1 (and decay slot j % 3)
-  uint64_t s_ready[2];  // compute warps: S^T channels 64 h .. 64 h + 63 written
+  uint64_t s_ready;     // compute warps: the initial S^T written
+  uint64_t r_ready;     // compute warps: S^T Diag(e^gamma_C) written into the next buffer
   uint64_t u_ready[2];  // compute warps: U^T tokens 32 h .. 32 h + 31 written
+  uint64_t x_free;      // compute warps: done reading X^T
+  uint64_t empty[2];    // MMAs: stage s read by its chunk's products (the next load may come)
   uint64_t bar_x, bar_y, bar_drain;
   uint32_t tmem_base;
   int abort;
@@ -1018,6 +1021,11 @@ static_assert(sizeof(StateMisc) <= 256, "misc overflow");
 // warps synchronise with it through mbarriers only. With p.discard, warp 9 drops each chunk's
 // record from L2 once the compute warps have counted it consumed.
 // With `flags`, waits (acquire) for each item's record before reading it.
+// kDeferOut: store a chunk's outputs during the next chunk's X product (the standalone walk,
+// which reads its records from memory: ~15% faster on a 256-chunk walk) or at once (the fused
+// launch, where the walk trails the prep CTAs and storing at once measured better). A template
+// parameter, so that each kernel carries one form and no registers for the other.
+template <bool kDeferOut>
 __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMap& twq,
                                           const CUtensorMap& tkbt, const CUtensorMap& tdec,
                                           const Ws& ws, const int tile, const int h,
@@ -1028,6 +1036,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool issuer = warp == 8;
   const bool discarder = warp == 9;
+  const bool loader = warp == 10;
   const int qd = warp & 3, hf = (warp >> 2) & 1;
   const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
   const int H = p.H;
@@ -1054,10 +1063,13 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
   if (tid == 0) {
     mbar_init(&misc->full[0], 1);
     mbar_init(&misc->full[1], 1);
-    mbar_init(&misc->s_ready[0], 4);
-    mbar_init(&misc->s_ready[1], 4);
+    mbar_init(&misc->s_ready, 8);
+    mbar_init(&misc->r_ready, 8);
     mbar_init(&misc->u_ready[0], 4);
     mbar_init(&misc->u_ready[1], 4);
+    mbar_init(&misc->x_free, 8);
+    mbar_init(&misc->empty[0], 1);
+    mbar_init(&misc->empty[1], 1);
     mbar_init(&misc->bar_x, 1);
     mbar_init(&misc->bar_y, 1);
     mbar_init(&misc->bar_drain, 1);
@@ -1070,12 +1082,70 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
   const uint32_t sbase = smem_u32(sm);
 
   if (issuer) {
-    // ------------------------------------------------------------ issuer warp (lane 0)
+    // ------------------------------------------------------------ MMA-issuing warp (lane 0)
+    if (lane == 0) {
+      const uint32_t idesc = idesc_make(kFmtTF32, 128, 128, false, false);
+      const uint32_t idesc_x = pkg ? idesc_make(kFmtTF32, 128, 64, false, false) : idesc;
+      bool ok = true;
+      for (int j = 0; j < nch && ok; ++j) {
+        const uint32_t par = (uint32_t)j & 1u;
+        const uint32_t st = (uint32_t)(j & 1) * S_STAGE;
+        const uint64_t d_wq = sdesc_sw128(sbase + st + S_WQ, 16, 1024);
+        const uint64_t d_kbt = sdesc_sw128(sbase + st + S_KBT, 16, 1024);
+        const uint32_t s_cur = tbase + TS_S + par * 128u, s_nxt = tbase + TS_S + (par ^ 1u) * 128u;
+        ok = mbar_wait_or(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u, &misc->abort);
+        // X^T = S_j^T [W ; Q'']^T once S_j is complete (the initial state, or the previous
+        // chunk's Y product) and the compute warps are done with the previous X^T
+        if (j == 0) {
+          ok = ok && mbar_wait_or(&misc->s_ready, 0, &misc->abort);
+        } else {
+          ok = ok && mbar_wait_or(&misc->bar_y, par ^ 1u, &misc->abort) &&
+               mbar_wait_or(&misc->x_free, par ^ 1u, &misc->abort);
+        }
+        tc_fence_after();
+        if (!ok) break;
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks)  // K-step: channels 8 ks .. 8 ks + 7
+          mma_tf32_ts(tbase + TS_X, s_cur + ks * 8,
+                      desc_add(d_wq, (ks >> 2) * 16384 + (ks & 3) * 32), idesc_x, ks > 0);
+        mma_commit(&misc->bar_x);
+        // S_{j+1}^T = S_j^T Diag(e^gamma_C) + U^T Kb': accumulated onto the decayed state that
+        // the compute warps wrote into the other buffer, token half by token half as U^T is
+        // written
+        ok = mbar_wait_or(&misc->r_ready, par, &misc->abort);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          ok = ok && mbar_wait_or(&misc->u_ready[hh], par, &misc->abort);
+          tc_fence_after();
+          if (ok) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const int ks = hh * 4 + k;  // K-step: tokens 8 ks .. 8 ks + 7
+              mma_tf32_ts(s_nxt, tbase + TS_U + ks * 8,
+                          desc_add(d_kbt, (ks >> 2) * 16384 + (ks & 3) * 32), idesc, 1);
+            }
+          }
+        }
+        if (!ok) break;
+        mma_commit(&misc->bar_y);
+        mma_commit(&misc->empty[j & 1]);  // both products have read the stage
+      }
+      if (!ok) {
+        misc->abort = 1;
+        mma_commit(&misc->bar_drain);
+        mbar_wait(&misc->bar_drain, 0, 100000000ull);
+      }
+    }
+  } else if (loader) {
+    // ------------------------------------------------------------ loading warp (lane 0)
+    // Chunk j's record into stage j & 1 (and decay slot j % 3), two chunks ahead: chunk j + 2
+    // as soon as chunk j's products have read the stage. Kept off the MMA-issuing thread, whose
+    // chain the stage's release, a record's flag and the copies' issue would otherwise lengthen.
     if (lane == 0) {
       tma_prefetch_desc(&twq);
       tma_prefetch_desc(&tkbt);
       tma_prefetch_desc(&tdec);
-      auto issue_tma = [&](int j) -> bool {  // chunk j into stage j & 1 and decay slot j % 3
+      auto issue_tma = [&](int j) -> bool {
         const int item = (slot0 + j) * H + h;
         if (flags) {  // the record is published by the prep CTA that wrote it
           if (!wait_flag(flags + item, p.flag_wait_ns)) return false;
@@ -1100,60 +1170,14 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
       };
       int tma_last = -1;
       bool ok = true;
-      for (int j = 0; j < 2 && j < nch && ok; ++j) {
-        ok = issue_tma(j);
-        if (ok) tma_last = j;
-      }
-      const uint32_t idesc = idesc_make(kFmtTF32, 128, 128, false, false);
-      const uint32_t idesc_x = pkg ? idesc_make(kFmtTF32, 128, 64, false, false) : idesc;
       for (int j = 0; j < nch && ok; ++j) {
-        const uint32_t par = (uint32_t)j & 1u;
-        const uint32_t st = (uint32_t)(j & 1) * S_STAGE;
-        const uint64_t d_wq = sdesc_sw128(sbase + st + S_WQ, 16, 1024);
-        const uint64_t d_kbt = sdesc_sw128(sbase + st + S_KBT, 16, 1024);
-        ok = mbar_wait_or(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u, &misc->abort);
-        // X^T = S^T [W ; Q'']^T, channel half by channel half as S^T is written
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          ok = ok && mbar_wait_or(&misc->s_ready[hh], par, &misc->abort);
-          tc_fence_after();
-          if (ok) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-              const int ks = hh * 8 + k;  // K-step: channels 8 ks .. 8 ks + 7
-              mma_tf32_ts(tbase + TS_X, tbase + TS_S + ks * 8,
-                          desc_add(d_wq, (ks >> 2) * 16384 + (ks & 3) * 32), idesc_x, ks > 0);
-            }
-          }
-        }
-        if (!ok) break;
-        mma_commit(&misc->bar_x);
-        // Y^T = U^T Kb', token half by token half as U^T is written
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          ok = ok && mbar_wait_or(&misc->u_ready[hh], par, &misc->abort);
-          tc_fence_after();
-          if (ok) {
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              const int ks = hh * 4 + k;  // K-step: tokens 8 ks .. 8 ks + 7
-              mma_tf32_ts(tbase + TS_Y, tbase + TS_U + ks * 8,
-                          desc_add(d_kbt, (ks >> 2) * 16384 + (ks & 3) * 32), idesc, ks > 0);
-            }
-          }
-        }
-        if (!ok) break;
-        mma_commit(&misc->bar_y);
-        // the stage is free once Y has completed: load chunk j + 2 into it
-        if (j + 2 < nch) {
-          ok = mbar_wait_or(&misc->bar_y, par, &misc->abort) && issue_tma(j + 2);
-          if (ok) tma_last = j + 2;
-        }
+        if (j >= 2) ok = mbar_wait_or(&misc->empty[j & 1], ((uint32_t)(j - 2) >> 1) & 1u, &misc->abort);
+        ok = ok && issue_tma(j);
+        if (ok) tma_last = j;
       }
       if (!ok) {
         misc->abort = 1;
-        mma_commit(&misc->bar_drain);
-        mbar_wait(&misc->bar_drain, 0, 100000000ull);
+        // this warp's copies in flight land before the CTA lets go of its shared memory
         for (int j = tma_last > 0 ? tma_last - 1 : 0; j <= tma_last; ++j)
           mbar_wait(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u, 100000000ull);
       }
@@ -1217,7 +1241,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&misc->s_ready[hf]);
+      if (lane == 0) mbar_arrive(&misc->s_ready);
     }
     // per-chunk register operands, loaded one chunk ahead: U0^T[n][32 hf ..] (32 fp32) and
     // O0^T[n][32 hf ..] (32 bf16)
@@ -1258,12 +1282,71 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
       load_u0(0, u0);
       load_o0(0, o0);
     }
+    // A chunk's outputs (bf16 pairs of adjacent tokens of column n): token t of column n, 32
+    // lanes = 64 contiguous bytes of one token's row; none once the CTA gave up. Lanes l and
+    // l ^ 1 trade halves so that the even lane holds columns (n, n + 1) of the even tokens and
+    // the odd lane those of the odd tokens: 16 four-byte stores per thread.
+    uint32_t ob16[16];
+    int prev_t0 = 0, prev_nvalid = 0;
+    auto store_out = [&](int ot0, int onvalid) {
+      if (!pkg && p.o && !misc->abort) {
+        const bool odd = (lane & 1) != 0;
+        __nv_bfloat16* o = (__nv_bfloat16*)p.o + ((int64_t)ot0 * H + h) * DK + (n & ~1);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t mine = ob16[i];  // (token 2i, token 2i + 1) of column n
+          const uint32_t give = odd ? (mine & 0xFFFFu) : (mine >> 16);
+          const uint32_t got = __shfl_xor_sync(0xFFFFFFFFu, give, 1);
+          const uint32_t pair = odd ? (got | (mine & 0xFFFF0000u)) : ((mine & 0xFFFFu) | (got << 16));
+          const int t = hf * 32 + 2 * i + (odd ? 1 : 0);
+          if (t < onvalid) *reinterpret_cast<uint32_t*>(o + (int64_t)t * H * DK) = pair;
+        }
+      }
+    };
 
     for (int j = 0; j < nch; ++j) {
       const int t0 = t_begin + j * C;
       const int nvalid = min(C, t_end - t0);
       const uint32_t par = (uint32_t)j & 1u;
-      // ================= U^T = U0^T - (W S)^T (tokens 32 hf ..), then the outputs
+      const uint32_t s_cur = tbase + lane_base + TS_S + par * 128u;
+      const uint32_t s_nxt = tbase + lane_base + TS_S + (par ^ 1u) * 128u;
+      // ================= S_j^T Diag(e^gamma_C) into the other buffer (channels 64 hf ..), while
+      // the X product reads S_j^T; the Y product then accumulates onto it. S_j^T is complete
+      // with the previous chunk's Y product; the decays came with this chunk's record.
+      if (j > 0 && !mbar_wait_relaxed_or(&misc->bar_y, par ^ 1u, &misc->abort)) misc->abort = 1;
+      if (!mbar_wait_or(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u, &misc->abort))
+        misc->abort = 1;
+      tc_fence_after();
+      {
+        // the thread's 64 channels in four loads of 16 columns, all in flight at once
+        const float* dec = f32at(sm, S_DEC + (j % 3) * 512);
+        const int c0 = hf * 64;
+        uint32_t sr[4][16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tmem_ld16_nowait(s_cur + c0 + 16 * k, sr[k]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int cc = c0 + 16 * k;
+          float sd[16];
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const float4 d4 = *reinterpret_cast<const float4*>(dec + cc + i);
+            sd[i] = d4.x * __uint_as_float(sr[k][i]);
+            sd[i + 1] = d4.y * __uint_as_float(sr[k][i + 1]);
+            sd[i + 2] = d4.z * __uint_as_float(sr[k][i + 2]);
+            sd[i + 3] = d4.w * __uint_as_float(sr[k][i + 3]);
+          }
+          tmem_st16(s_nxt + cc, sd);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_relaxed(&misc->r_ready);
+      }
+      // the previous chunk's outputs, while the X product runs
+      if (kDeferOut && j > 0) store_out(prev_t0, prev_nvalid);
+      // ================= U^T = U0^T - (W S)^T (tokens 32 hf ..), then the output values
       if (!mbar_wait_relaxed_or(&misc->bar_x, par, &misc->abort)) misc->abort = 1;
       tc_fence_after();
       {
@@ -1283,8 +1366,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
       }
       if (j + 1 < nch) load_u0(j + 1, u0);  // this chunk's U0^T is consumed
       // output values of tokens 32 hf .. 32 hf + 31: O^T[n][t] = (Q'' S)^T + O0^T, packed as
-      // bf16 pairs of adjacent tokens
-      uint32_t ob16[16];
+      // bf16 pairs of adjacent tokens, stored during the next chunk's X product
       if (!pkg && p.o) {
         float x[32];
         tmem_ld32(tbase + lane_base + TS_X + 64 + hf * 32, x);
@@ -1299,62 +1381,18 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
           }
         }
       }
+      tc_fence_before();  // this warp is done with X^T
+      __syncwarp();
+      if (lane == 0) mbar_arrive_relaxed(&misc->x_free);
       if (j + 1 < nch) load_o0(j + 1, o0);  // this chunk's O0^T is consumed
-      // ================= S^T = S^T Diag(e^gamma_C) + Y^T (channels 64 hf ..)
-      if (!mbar_wait_relaxed_or(&misc->bar_y, par, &misc->abort)) misc->abort = 1;
-      tc_fence_after();
-      {
-        // four pieces of 16 columns, the next piece's loads in flight while the current one is
-        // updated (a load wait covers every load before it, so one piece ahead is the depth)
-        const float* dec = f32at(sm, S_DEC + (j % 3) * 512);
-        const int c0 = hf * 64;
-        uint32_t y[2][16], sr[2][16];
-        tmem_ld16_nowait(tbase + lane_base + TS_Y + c0, y[0]);
-        tmem_ld16_nowait(tbase + lane_base + TS_S + c0, sr[0]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int cc = c0 + 16 * k;
-          if (k + 1 < 4) {
-            tmem_ld16_nowait(tbase + lane_base + TS_Y + cc + 16, y[(k + 1) & 1]);
-            tmem_ld16_nowait(tbase + lane_base + TS_S + cc + 16, sr[(k + 1) & 1]);
-          }
-          float s[16];
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const float4 d4 = *reinterpret_cast<const float4*>(dec + cc + i);
-            s[i] = fmaf(d4.x, __uint_as_float(sr[k & 1][i]), __uint_as_float(y[k & 1][i]));
-            s[i + 1] = fmaf(d4.y, __uint_as_float(sr[k & 1][i + 1]), __uint_as_float(y[k & 1][i + 1]));
-            s[i + 2] = fmaf(d4.z, __uint_as_float(sr[k & 1][i + 2]), __uint_as_float(y[k & 1][i + 2]));
-            s[i + 3] = fmaf(d4.w, __uint_as_float(sr[k & 1][i + 3]), __uint_as_float(y[k & 1][i + 3]));
-          }
-          tmem_st16(tbase + lane_base + TS_S + cc, s);
-          if (k + 1 < 4) tmem_ld_wait();
-        }
-        tmem_st_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0 && j + 1 < nch) mbar_arrive_relaxed(&misc->s_ready[hf]);
-      }
-      // outputs, after the state update has released the next chunk's X product: token t of
-      // column n (32 lanes = 64 contiguous bytes of one token's row); none once the CTA gave up
-      // Lanes l and l ^ 1 trade halves so that the even lane holds columns (n, n + 1) of the
-      // even tokens and the odd lane those of the odd tokens: 16 four-byte stores per thread.
-      if (!pkg && p.o && !misc->abort) {
-        const bool odd = (lane & 1) != 0;
-        __nv_bfloat16* o = (__nv_bfloat16*)p.o + ((int64_t)t0 * H + h) * DK + (n & ~1);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const uint32_t mine = ob16[i];  // (token 2i, token 2i + 1) of column n
-          const uint32_t give = odd ? (mine & 0xFFFFu) : (mine >> 16);
-          const uint32_t got = __shfl_xor_sync(0xFFFFFFFFu, give, 1);
-          const uint32_t pair = odd ? (got | (mine & 0xFFFF0000u)) : ((mine & 0xFFFFu) | (got << 16));
-          const int t = hf * 32 + 2 * i + (odd ? 1 : 0);
-          if (t < nvalid) *reinterpret_cast<uint32_t*>(o + (int64_t)t * H * DK) = pair;
-        }
+      if (kDeferOut) {
+        prev_t0 = t0;
+        prev_nvalid = nvalid;
+      } else {
+        store_out(t0, nvalid);
       }
       if (p.discard) {
-        // the chunk's record is read no more (both products done, U0^T / O0^T in registers):
+        // the chunk's record is read no more (its tensor copies landed, U0^T / O0^T used):
         // count it consumed for the discarding warp (release: the warp's loads came first)
         __syncwarp();
         if (lane == 0) {
@@ -1364,18 +1402,24 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
       }
       if (misc->abort) break;
     }
+    if (kDeferOut && nch > 0) store_out(prev_t0, prev_nvalid);  // the last chunk's outputs
   }
   cta_sync();
-  if (!issuer && !discarder && !misc->abort) {  // exit state rows c of column n (coalesced)
+  if (!issuer && !discarder && !loader && !misc->abort) {  // exit state rows c of column n
     const int64_t sh = (int64_t)ridx * H + h;
     float* dst = nullptr;
     if (pkg) dst = mcols ? p.M + sh * DK * DK + n : p.D + sh * DK * DK + n;
     else if (p.final_state) dst = p.final_state + sh * DK * DK + n;
+    // the final state is in buffer nch & 1, complete with the last Y product
+    if (dst && nch > 0 &&
+        !mbar_wait_relaxed_or(&misc->bar_y, (uint32_t)(nch - 1) & 1u, &misc->abort))
+      dst = nullptr;
+    tc_fence_after();
     if (dst) {
 #pragma unroll 1
       for (int cc = hf * 64; cc < hf * 64 + 64; cc += 32) {
         float s[32];
-        tmem_ld32(tbase + lane_base + TS_S + cc, s);
+        tmem_ld32(tbase + lane_base + TS_S + (uint32_t)(nch & 1) * 128u + cc, s);
 #pragma unroll
         for (int i = 0; i < 32; ++i) dst[(int64_t)(cc + i) * DK] = s[i];
       }
@@ -1392,7 +1436,7 @@ chunk_state_kernel(const __grid_constant__ ChunkParams p,
                    const __grid_constant__ CUtensorMap tkbt,
                    const __grid_constant__ CUtensorMap tdec, const Ws ws,
                    const uint32_t* flags) {
-  state_run(p, twq, tkbt, tdec, ws, blockIdx.x, blockIdx.y, blockIdx.z, flags);
+  state_run<true>(p, twq, tkbt, tdec, ws, blockIdx.x, blockIdx.y, blockIdx.z, flags);
 }
 
 // ============================================================================ fused launch
@@ -1417,10 +1461,10 @@ chunk_fused_kernel(const __grid_constant__ ChunkParams p, const __grid_constant_
   const int b = blockIdx.x;
   if (b < n_state) {
     const int tiles = p.package ? 2 : 1;
-    state_run(p, twq, tkbt, tdec, ws, b % tiles, (b / tiles) % p.H, b / (tiles * p.H), flags);
+    state_run<false>(p, twq, tkbt, tdec, ws, b % tiles, (b / tiles) % p.H, b / (tiles * p.H), flags);
   } else {
-    // the prep work uses 8 warps; the ninth publishes the finished items' flags (the tenth,
-    // which discards records in the state CTAs, has nothing to do here)
+    // the prep work uses 8 warps; the ninth publishes the finished items' flags (the tenth and
+    // eleventh, which discard and load records in the state CTAs, have nothing to do here)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     PrepMisc* misc = reinterpret_cast<PrepMisc*>(sm + P_MISC);
