@@ -193,7 +193,7 @@ static_assert(offsetof(PrepMisc, part) % 16 == 0 && offsetof(PrepMisc, erho) % 1
               "vector-loaded arrays must be 16-byte aligned");
 
 // The prep CTA's 256 threads synchronise on named barrier 1 (a fused launch runs them next to
-// its publishing warp and an idle tenth warp).
+// its publishing warp and three idle warps).
 __device__ __forceinline__ void pbar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 __device__ __forceinline__ void psync() {
   tc_fence_before();
@@ -996,10 +996,10 @@ static_assert(S_SMEM + 1024 <= 196 * 1024, "state kernel shared memory above the
 constexpr uint32_t TS_S = 0;     // 2 x 128: S^T, chunk j reading buffer j & 1 and writing j + 1's
 constexpr uint32_t TS_X = 256;   // 128: X^T
 constexpr uint32_t TS_U = 384;   // 64: U^T
-// 8 compute warps + 1 MMA-issuing warp + 1 warp that drops consumed records from L2 (fused
-// launch) + 1 warp that loads the records. Eleven warps cost no registers over nine: either way
+// 8 compute warps + 1 MMA-issuing warp + 1 warp that loads the records + 2 warps that drop
+// consumed records from L2 (fused launch). Twelve warps cost no registers over nine: either way
 // three share an SMSP's register file.
-constexpr int kStateThreads = kThreads + 96;
+constexpr int kStateThreads = kThreads + 128;
 
 struct StateMisc {
   uint64_t full[2];     // TMA: chunk j's record landed in stage j & 1 (and decay slot j % 3)
@@ -1016,10 +1016,11 @@ struct StateMisc {
 static_assert(sizeof(StateMisc) <= 256, "misc overflow");
 
 // Compute warp w (0..7): TMEM lane quarter w % 4, so state column n = 32 (w % 4) + lane of the
-// tile; half h = w / 4 of the channels (S update) and of the tokens (U and outputs). The issuer
-// warp (8) waits on the per-half barriers and issues the MMAs and the TMA loads. The compute
-// warps synchronise with it through mbarriers only. With p.discard, warp 9 drops each chunk's
-// record from L2 once the compute warps have counted it consumed.
+// tile; half h = w / 4 of the channels (state update) and of the tokens (U and outputs). Warp 8
+// issues the MMAs, warp 10 the records' TMA loads (two chunks ahead, each stage refilled once
+// the products have read it); they and the compute warps synchronise through mbarriers only.
+// With p.discard, warps 9 and 11 drop each chunk's record from L2 once the compute warps have
+// counted it consumed.
 // With `flags`, waits (acquire) for each item's record before reading it.
 // kDeferOut: store a chunk's outputs during the next chunk's X product (the standalone walk,
 // which reads its records from memory: ~15% faster on a 256-chunk walk) or at once (the fused
@@ -1035,7 +1036,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
   StateMisc* misc = reinterpret_cast<StateMisc*>(sm + S_MISC);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool issuer = warp == 8;
-  const bool discarder = warp == 9;
+  const bool discarder = warp == 9 || warp == 11;
   const bool loader = warp == 10;
   const int qd = warp & 3, hf = (warp >> 2) & 1;
   const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
@@ -1183,13 +1184,15 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
       }
     }
   } else if (discarder) {
-    // ------------------------------------------------------------ discarding warp
+    // ------------------------------------------------------------ discarding warps
     // The records of a fused launch are read once, from L2: drop each chunk's lines once the
     // compute warps are done with it (both products complete, U0^T / O0^T in registers), so
-    // that they are never written back to DRAM. A discard holds its thread for a while, so
-    // they run here, off the compute warps' chain; if this warp falls more than two chunks
-    // behind, it skips ahead (a skipped record is merely written back).
+    // that they are never written back to DRAM. A discard holds its thread for ~100 cycles, so
+    // they run here, off the compute warps' chain, in two warps (one takes every record's first
+    // 578 lines, the other the rest: one warp fell behind the walk); a warp more than two
+    // chunks behind skips ahead (a skipped record is merely written back).
     if (p.discard) {
+      const int l0 = warp == 9 ? 0 : 578, l1 = warp == 9 ? 578 : 1156;
       for (int j = 0; j < nch; ++j) {
         const uint64_t t0 = globaltimer_ns();
         uint32_t c;
@@ -1211,7 +1214,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
         const uint8_t* r_o0 = reinterpret_cast<const uint8_t*>(ws.o0 + item * 8192);
         const uint8_t* r_dc = reinterpret_cast<const uint8_t*>(ws.dec + item * 128);
         // 512 lines of [W ; Q''], 256 of Kb'^T, 256 of U0^T, 128 of O0^T, 4 of the decays
-        for (int l = lane; l < 1156; l += 32) {
+        for (int l = l0 + lane; l < l1; l += 32) {
           const uint8_t* a = l < 512    ? r_wq + l * 128
                              : l < 768  ? r_kb + (l - 512) * 128
                              : l < 1024 ? r_u0 + (l - 768) * 128
@@ -1463,8 +1466,8 @@ chunk_fused_kernel(const __grid_constant__ ChunkParams p, const __grid_constant_
     const int tiles = p.package ? 2 : 1;
     state_run<false>(p, twq, tkbt, tdec, ws, b % tiles, (b / tiles) % p.H, b / (tiles * p.H), flags);
   } else {
-    // the prep work uses 8 warps; the ninth publishes the finished items' flags (the tenth and
-    // eleventh, which discard and load records in the state CTAs, have nothing to do here)
+    // the prep work uses 8 warps; the ninth publishes the finished items' flags (the others,
+    // which load and discard records in the state CTAs, have nothing to do here)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     PrepMisc* misc = reinterpret_cast<PrepMisc*>(sm + P_MISC);
