@@ -22,10 +22,11 @@
 // Kernel 1 (prep) computes the state-independent factors of every (chunk, head) in parallel
 // (persistent CTAs, one item at a time, the next item's loads in flight) and writes them to a
 // workspace record. Kernel 2 (state) walks each range's chunks in order for one (range, head,
-// 128-column tile of the state) with the transposed state S^T in TMEM: per chunk one N = 128
-// product X^T = S^T [W; Q'']^T, the U update and the outputs on CUDA cores, one N = 128
-// product Y^T = U^T Kb', and the state update, with the records streamed in by TMA two chunks
-// ahead. In package mode kernel 2 runs the same chunks on the M or the D half of the
+// 128-column tile of the state) with the transposed state S^T in two TMEM buffers: per chunk
+// one N = 128 product X^T = S^T [W; Q'']^T, the U update and the outputs on CUDA cores, the
+// decayed state S^T Diag(e^gamma_C) written into the other buffer next to X, and one N = 128
+// product U^T Kb' accumulated onto it, with the records streamed in by TMA two chunks ahead.
+// In package mode kernel 2 runs the same chunks on the M or the D half of the
 // augmented state [M | D] (identity / zero start; M columns see zero values) and writes no
 // outputs. A fused cooperative launch runs both kernels' work side by side for few walks.
 //
@@ -1253,7 +1254,7 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
     auto load_u0 = [&](int j, float4* u0) {
       const int64_t item = (int64_t)(slot0 + j) * H + h;
       if (flags) {
-        // The issuer acquired the record's flag before its arrive on this chunk's stage
+        // The loading warp acquired the record's flag before its arrive on this chunk's stage
         // barrier (a release): acquiring that phase orders these loads after the record.
         if (!mbar_wait_or(&misc->full[j & 1], ((uint32_t)j >> 1) & 1u, &misc->abort))
           misc->abort = 1;
