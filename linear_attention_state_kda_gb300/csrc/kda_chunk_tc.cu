@@ -1023,15 +1023,20 @@ static_assert(sizeof(StateMisc) <= 256, "misc overflow");
 // With p.discard, warps 9 and 11 drop each chunk's record from L2 once the compute warps have
 // counted it consumed.
 // With `flags`, waits (acquire) for each item's record before reading it.
+// The walk of range ridx for (tile, head), in TMEM the caller allocated; ends on a CTA barrier
+// (the caller then reads misc->abort). The barriers are initialised afresh for each range.
 // kDeferOut: store a chunk's outputs during the next chunk's X product (the standalone walk,
 // which reads its records from memory: ~15% faster on a 256-chunk walk) or at once (the fused
 // launch, where the walk trails the prep CTAs and storing at once measured better). A template
 // parameter, so that each kernel carries one form and no registers for the other.
-template <bool kDeferOut>
-__device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMap& twq,
-                                          const CUtensorMap& tkbt, const CUtensorMap& tdec,
-                                          const Ws& ws, const int tile, const int h,
-                                          const int ridx, const uint32_t* flags) {
+// kMultiRange: the CTA walks further ranges after this one in TMEM the caller allocated, so
+// every asynchronous arrive on the barriers is waited for before they are initialised again;
+// otherwise the walk allocates and frees its TMEM itself.
+template <bool kDeferOut, bool kMultiRange>
+__device__ __forceinline__ void state_range(const ChunkParams& p, const CUtensorMap& twq,
+                                            const CUtensorMap& tkbt, const CUtensorMap& tdec,
+                                            const Ws& ws, const int tile, const int h,
+                                            const int ridx, const uint32_t* flags) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   StateMisc* misc = reinterpret_cast<StateMisc*>(sm + S_MISC);
@@ -1058,11 +1063,12 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
   const int nch = (t_end - t_begin + C - 1) / C;
   const int slot0 = t_begin / C + ridx;
 
-  if (warp == 0) {
+  if (!kMultiRange && warp == 0) {
     tmem_alloc(&misc->tmem_base, 512);
     tmem_relinquish();
   }
-  if (tid == 0) {
+  if (tid == 0) {  // (with kMultiRange every async arrive of the previous range has landed)
+    if (!kMultiRange) misc->abort = 0;
     mbar_init(&misc->full[0], 1);
     mbar_init(&misc->full[1], 1);
     mbar_init(&misc->s_ready, 8);
@@ -1075,7 +1081,6 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
     mbar_init(&misc->bar_x, 1);
     mbar_init(&misc->bar_y, 1);
     mbar_init(&misc->bar_drain, 1);
-    misc->abort = 0;
     misc->consumed = 0;
     fence_mbar_init();
   }
@@ -1136,6 +1141,9 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
         misc->abort = 1;
         mma_commit(&misc->bar_drain);
         mbar_wait(&misc->bar_drain, 0, 100000000ull);
+      } else if (kMultiRange) {  // the last two stage releases have arrived
+        for (int j = nch > 2 ? nch - 2 : 0; j < nch; ++j)
+          mbar_wait(&misc->empty[j & 1], ((uint32_t)j >> 1) & 1u, 100000000ull);
       }
     }
   } else if (loader) {
@@ -1414,8 +1422,9 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
     float* dst = nullptr;
     if (pkg) dst = mcols ? p.M + sh * DK * DK + n : p.D + sh * DK * DK + n;
     else if (p.final_state) dst = p.final_state + sh * DK * DK + n;
-    // the final state is in buffer nch & 1, complete with the last Y product
-    if (dst && nch > 0 &&
+    // the final state is in buffer nch & 1, complete with the last Y product (waited for even
+    // when not stored if a further range re-initialises the barrier)
+    if ((dst || kMultiRange) && nch > 0 &&
         !mbar_wait_relaxed_or(&misc->bar_y, (uint32_t)(nch - 1) & 1u, &misc->abort))
       dst = nullptr;
     tc_fence_after();
@@ -1429,9 +1438,33 @@ __device__ __forceinline__ void state_run(const ChunkParams& p, const CUtensorMa
       }
     }
   }
-  if (misc->abort && tid == 0 && p.status) atomicOr(p.status, KDA_STATUS_TIMEOUT);
+  if (!kMultiRange) {
+    if (misc->abort && tid == 0 && p.status) atomicOr(p.status, KDA_STATUS_TIMEOUT);
+    cta_sync();
+    if (warp == 0) tmem_dealloc(tbase, 512);
+  } else {
+    cta_sync();
+  }
+}
+
+// TMEM for a walk CTA: allocated once (all 512 columns), released at the end.
+__device__ __forceinline__ void state_tmem_alloc() {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  StateMisc* misc = reinterpret_cast<StateMisc*>(sm + S_MISC);
+  if ((threadIdx.x >> 5) == 0) {
+    tmem_alloc(&misc->tmem_base, 512);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 0) misc->abort = 0;
+}
+__device__ __forceinline__ void state_tmem_free(const ChunkParams& p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  StateMisc* misc = reinterpret_cast<StateMisc*>(sm + S_MISC);
+  if (misc->abort && threadIdx.x == 0 && p.status) atomicOr(p.status, KDA_STATUS_TIMEOUT);
   cta_sync();
-  if (warp == 0) tmem_dealloc(tbase, 512);
+  if ((threadIdx.x >> 5) == 0) tmem_dealloc(misc->tmem_base, 512);
 }
 
 __global__ void __launch_bounds__(kStateThreads, 1)
@@ -1440,7 +1473,7 @@ chunk_state_kernel(const __grid_constant__ ChunkParams p,
                    const __grid_constant__ CUtensorMap tkbt,
                    const __grid_constant__ CUtensorMap tdec, const Ws ws,
                    const uint32_t* flags) {
-  state_run<true>(p, twq, tkbt, tdec, ws, blockIdx.x, blockIdx.y, blockIdx.z, flags);
+  state_range<true, false>(p, twq, tkbt, tdec, ws, blockIdx.x, blockIdx.y, blockIdx.z, flags);
 }
 
 // ============================================================================ fused launch
@@ -1450,6 +1483,7 @@ chunk_state_kernel(const __grid_constant__ ChunkParams p,
 // (flags[item] = 1, release / acquire at gpu scope; every wait bounded). The serial state
 // walk then follows the parallel prep work instead of waiting for all of it.
 constexpr uint32_t F_SMEM = P_SMEM > S_SMEM ? P_SMEM : S_SMEM;
+constexpr int kFusedMaxRanges = 8;  // ranges one walk CTA may take in turn
 
 __global__ void __launch_bounds__(kStateThreads, 1)
 chunk_fused_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ CUtensorMap tmq,
@@ -1461,11 +1495,22 @@ chunk_fused_kernel(const __grid_constant__ ChunkParams p, const __grid_constant_
                    const __grid_constant__ CUtensorMap twq,
                    const __grid_constant__ CUtensorMap tkbt,
                    const __grid_constant__ CUtensorMap tdec, const Ws ws, const int n_items,
-                   const int n_state, uint32_t* flags) {
+                   const int n_state, const int ranges_per_walk, uint32_t* flags) {
   const int b = blockIdx.x;
   if (b < n_state) {
+    // walk CTA b: (tile, head) b % (tiles H), ranges_per_walk consecutive ranges
     const int tiles = p.package ? 2 : 1;
-    state_run<false>(p, twq, tkbt, tdec, ws, b % tiles, (b / tiles) % p.H, b / (tiles * p.H), flags);
+    const int r0 = b / (tiles * p.H) * ranges_per_walk;
+    const int r1 = min(r0 + ranges_per_walk, p.n_ranges);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const StateMisc* misc = reinterpret_cast<const StateMisc*>(sm + S_MISC);
+    state_tmem_alloc();
+    for (int r = r0; r < r1; ++r) {
+      state_range<false, true>(p, twq, tkbt, tdec, ws, b % tiles, (b / tiles) % p.H, r, flags);
+      if (misc->abort) break;  // read after the range's closing CTA barrier: uniform
+    }
+    state_tmem_free(p);
   } else {
     // the prep work uses 8 warps; the ninth publishes the finished items' flags (the others,
     // which load and discard records in the state CTAs, have nothing to do here)
@@ -1680,11 +1725,19 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
     return set_error(KDA_ERR_CUDA, std::string("tensor-core chunk path attribute: ") +
                                        cudaGetErrorString(e));
   const int tiles = p.package ? 2 : 1;
-  const int64_t n_state = (int64_t)tiles * p.n_ranges * p.H;
   const int sms = sm_count();
   // Few serial walks: run them next to the prep work in one cooperative launch (at most a
-  // quarter of the SMs walk, the rest prepare records).
-  if (do_prep && do_state && n_state * 4 <= sms && cooperative_ok()) {
+  // quarter of the SMs walk, the rest prepare records). Every (tile, head, range) its own walk
+  // CTA when they fit; else, for a few ranges (a few long sequences, whose serial walks would
+  // otherwise follow all of the prep work), one walk CTA per (tile, head) takes the ranges in
+  // order while the prep CTAs produce their records in that order.
+  const int64_t per_range = (int64_t)tiles * p.H;
+  int ranges_per_walk = 0;
+  if (per_range * p.n_ranges * 4 <= sms) ranges_per_walk = 1;
+  else if (p.n_ranges <= kFusedMaxRanges && per_range * 4 <= sms) ranges_per_walk = p.n_ranges;
+  const int64_t n_state =
+      ranges_per_walk ? per_range * ((p.n_ranges + ranges_per_walk - 1) / ranges_per_walk) : 0;
+  if (do_prep && do_state && ranges_per_walk > 0 && cooperative_ok()) {
     e = cudaMemsetAsync(flags, 0, (size_t)n_items * 4, s);
     if (e != cudaSuccess)
       return set_error(KDA_ERR_CUDA, std::string("tensor-core chunk path flags: ") +
@@ -1705,7 +1758,7 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     e = cudaLaunchKernelEx(&cfg, chunk_fused_kernel, pf, mq, mk, mv, mg, mb, swq, mwq, mkbt, mdec,
-                           ws, (int)n_items, (int)n_state, flags);
+                           ws, (int)n_items, (int)n_state, ranges_per_walk, flags);
     if (e == cudaSuccess) {
       count_launches(1);
       return check_launch("tensor-core chunk fused kernel");
