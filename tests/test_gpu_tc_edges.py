@@ -175,3 +175,29 @@ def test_single_token_and_single_chunk_sequences():
     _assert_o(f64(o), ro, "tiny sequences")
     _assert_s(f64(fin), rf, "tiny sequences")
     assert torch.equal(fin[1], x.init_state[1]) and torch.equal(fin[6], x.init_state[6])
+
+
+def test_few_sequences_walked_in_turn_by_one_cta_per_head():
+    """Six ragged sequences at 8 heads: 48 walks are more than a quarter of the SMs, so the fused
+    launch gives each head one walk CTA that takes the six ranges in turn (an empty one and a
+    one-token one among them) while the prep CTAs produce their records. Against the oracle on
+    all heads, and against the same walks run from two separate launches (prepare, then a
+    replay from the entry states), bit for bit."""
+    lens = [1000, 0, 1, 63, 130, 4097]
+    h8 = 8
+    x = inputs.make_prefill(lens, H=h8, dk=D, dv=D, dtype="bf16", seed=47, device=DEV,
+                            init_std=0.05)
+    assert tc_path(len(lens), x.T, h8)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    o, fin = kda.chunk_prefill(x.q, x.k, x.v, x.g, x.beta, cu_seqlens=x.cu_seqlens,
+                               init_state=x.init_state, scale=SCALE, status=status)
+    ws = kda.chunk_prepare(x.q, x.k, x.v, x.g, x.beta, x.cu_seqlens, scale=SCALE)
+    o2, fin2 = kda.segment_replay_prepared(ws, x.cu_seqlens, x.init_state, x.T, h8, D, D,
+                                           want_final=True)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    ro, rf = _forward_oracle(x, scale=SCALE)
+    _assert_o(f64(o), ro, "ranges in turn")
+    _assert_s(f64(fin), rf, "ranges in turn")
+    assert torch.equal(o, o2) and torch.equal(fin, fin2)
+    assert torch.equal(fin[1], x.init_state[1])  # the empty sequence
