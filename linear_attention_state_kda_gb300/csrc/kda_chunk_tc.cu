@@ -1485,6 +1485,10 @@ chunk_state_kernel(const __grid_constant__ ChunkParams p,
 constexpr uint32_t F_SMEM = P_SMEM > S_SMEM ? P_SMEM : S_SMEM;
 constexpr int kFusedMaxRanges = 8;  // ranges one walk CTA may take in turn
 
+// kLooped: a walk CTA takes ranges_per_walk ranges in turn; else exactly one (ranges_per_walk
+// is 1), walked as in the state kernel (a separate instance, so that the one-range launch
+// carries none of the multi-range bookkeeping).
+template <bool kLooped>
 __global__ void __launch_bounds__(kStateThreads, 1)
 chunk_fused_kernel(const __grid_constant__ ChunkParams p, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tmk,
@@ -1502,15 +1506,19 @@ chunk_fused_kernel(const __grid_constant__ ChunkParams p, const __grid_constant_
     const int tiles = p.package ? 2 : 1;
     const int r0 = b / (tiles * p.H) * ranges_per_walk;
     const int r1 = min(r0 + ranges_per_walk, p.n_ranges);
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const StateMisc* misc = reinterpret_cast<const StateMisc*>(sm + S_MISC);
-    state_tmem_alloc();
-    for (int r = r0; r < r1; ++r) {
-      state_range<false, true>(p, twq, tkbt, tdec, ws, b % tiles, (b / tiles) % p.H, r, flags);
-      if (misc->abort) break;  // read after the range's closing CTA barrier: uniform
+    if (kLooped) {
+      extern __shared__ uint8_t smem_raw[];
+      uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+      const StateMisc* misc = reinterpret_cast<const StateMisc*>(sm + S_MISC);
+      state_tmem_alloc();
+      for (int r = r0; r < r1; ++r) {
+        state_range<false, true>(p, twq, tkbt, tdec, ws, b % tiles, (b / tiles) % p.H, r, flags);
+        if (misc->abort) break;  // read after the range's closing CTA barrier: uniform
+      }
+      state_tmem_free(p);
+    } else if (r0 < r1) {
+      state_range<false, false>(p, twq, tkbt, tdec, ws, b % tiles, (b / tiles) % p.H, r0, flags);
     }
-    state_tmem_free(p);
   } else {
     // the prep work uses 8 warps; the ninth publishes the finished items' flags (the others,
     // which load and discard records in the state CTAs, have nothing to do here)
@@ -1719,7 +1727,10 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
     e = cudaFuncSetAttribute(chunk_state_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              S_SMEM);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(chunk_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(chunk_fused_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             F_SMEM);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(chunk_fused_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              F_SMEM);
   if (e != cudaSuccess)
     return set_error(KDA_ERR_CUDA, std::string("tensor-core chunk path attribute: ") +
@@ -1757,8 +1768,11 @@ kda_status launch_chunk_tc(const ChunkParams& p, kda_dtype dt, void* workspace, 
     attr[0].val.cooperative = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, chunk_fused_kernel, pf, mq, mk, mv, mg, mb, swq, mwq, mkbt, mdec,
-                           ws, (int)n_items, (int)n_state, ranges_per_walk, flags);
+    e = ranges_per_walk > 1
+            ? cudaLaunchKernelEx(&cfg, chunk_fused_kernel<true>, pf, mq, mk, mv, mg, mb, swq, mwq,
+                                 mkbt, mdec, ws, (int)n_items, (int)n_state, ranges_per_walk, flags)
+            : cudaLaunchKernelEx(&cfg, chunk_fused_kernel<false>, pf, mq, mk, mv, mg, mb, swq, mwq,
+                                 mkbt, mdec, ws, (int)n_items, (int)n_state, ranges_per_walk, flags);
     if (e == cudaSuccess) {
       count_launches(1);
       return check_launch("tensor-core chunk fused kernel");
