@@ -114,3 +114,26 @@ def test_full_conv_16k_sampled_channels():
     assert _rel(f64(out[:, sel]), ref) < TOL["bf16"]
     w = int(cv.write_slots[0])
     assert torch.equal(cv.state[w], cv.x[-3:])
+
+
+@pytest.mark.parametrize("dtype,W", [("bf16", 4), ("f32", 3)])
+def test_many_sequences_more_tiles_than_ctas(dtype, W):
+    """Two hundred ragged sequences (empty, shorter than the window, multiples of the tile,
+    a few hundred tokens), so that each persistent CTA takes many tiles in turn, holes in the
+    tile numbering between them: every output and every stored window against the oracle."""
+    rng = np.random.default_rng(71)
+    lens = [int(v) for v in rng.integers(0, 300, size=200)]
+    lens[:8] = [0, 1, 2, 3, 32, 64, 16, 0]
+    C = 1024
+    cv = inputs.make_conv(lens, C, W, dtype=dtype, seed=72 + W, device=DEV)
+    state0 = f64(cv.state)
+    out = kda.short_conv(cv.x, cv.weight, cv.cu_seqlens, silu=True, read_slots=cv.read_slots,
+                         write_slots=cv.write_slots, conv_state=cv.state)
+    torch.cuda.synchronize()
+    host = state0.copy()
+    ref, bad = oracle.short_conv(f64(cv.x), f64(cv.weight), _ids(cv.cu_seqlens), silu=True,
+                                 read_slots=_ids(cv.read_slots), write_slots=_ids(cv.write_slots),
+                                 pool=host)
+    assert bad == 0
+    assert _rel(f64(out), ref) < TOL[dtype]
+    assert np.array_equal(f64(cv.state), host)
