@@ -317,17 +317,23 @@ bool launch_w(int n_seqs, int total, const int32_t* cu, int C, const void* x, co
                      (uint32_t)S::ROWS))
     return false;
   constexpr size_t smem = (size_t)kStages * S::BYTES + 128;
-  // CTAs resident per SM at this shared-memory size (at most kCtasPerSm): every CTA of the
-  // persistent grid runs from the start
-  static const int per_sm = [] {
+  // CTAs resident per SM at this shared-memory size (at most kCtasPerSm), so that every CTA
+  // of the persistent grid runs from the start; the attribute and the query are per device,
+  // done on a device's first call (a repeated first call just does them again)
+  static int per_sm_of[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return false;
+  int per_sm = dev < 64 ? per_sm_of[dev] : 0;
+  if (per_sm <= 0) {
     int n = 0;
     if (cudaFuncSetAttribute(conv_kernel<W, T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem) != cudaSuccess ||
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, conv_kernel<W, T>, kThreads, smem) !=
             cudaSuccess)
-      return 0;
-    return n < kCtasPerSm ? n : kCtasPerSm;
-  }();
+      return false;
+    per_sm = n < kCtasPerSm ? n : kCtasPerSm;
+    if (dev < 64) per_sm_of[dev] = per_sm;
+  }
   if (per_sm <= 0) return false;
   const int64_t tiles = (int64_t)total / S::R + n_seqs;
   const int64_t ncb = (C + kCols - 1) / kCols;
