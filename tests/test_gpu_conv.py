@@ -137,3 +137,23 @@ def test_many_sequences_more_tiles_than_ctas(dtype, W):
     assert bad == 0
     assert _rel(f64(out), ref) < TOL[dtype]
     assert np.array_equal(f64(cv.state), host)
+
+
+def test_more_channel_blocks_than_ctas():
+    """240,000 channels: 469 blocks of 512 channels (the last one 384 wide), more than the
+    persistent grid's CTAs, so that a CTA changes channel block from one tile to the next and
+    reloads its taps: outputs and stored windows against the oracle."""
+    lens = [40, 30]
+    C, W = 240000, 4
+    cv = inputs.make_conv(lens, C, W, seed=77, device=DEV)
+    state0 = f64(cv.state)
+    out = kda.short_conv(cv.x, cv.weight, cv.cu_seqlens, silu=True, read_slots=cv.read_slots,
+                         write_slots=cv.write_slots, conv_state=cv.state)
+    torch.cuda.synchronize()
+    host = state0.copy()
+    ref, bad = oracle.short_conv(f64(cv.x), f64(cv.weight), _ids(cv.cu_seqlens), silu=True,
+                                 read_slots=_ids(cv.read_slots), write_slots=_ids(cv.write_slots),
+                                 pool=host)
+    assert bad == 0
+    assert _rel(f64(out), ref) < TOL["bf16"]
+    assert np.array_equal(f64(cv.state), host)
