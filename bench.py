@@ -46,7 +46,7 @@ DECODE_BYTES_PER_ROW_HEAD = 2 * STATE_BYTES + 3 * D * 2 + D * 4 + 4 + D * 2
 # ncu capture summarised in profiles/, and the SHA-256 prefix of the chunk kernels' source it
 # was taken on: once that source changes the figure no longer describes the kernel that runs,
 # and the roofline object reports traffic as null until a new capture replaces both.
-TRAFFIC_PREFILL_16K = 911.9e6  # mean of 3 launches: 704.7 MB read + 207.2 MB written
+TRAFFIC_PREFILL_16K = 929.2e6  # mean of 6 launches in two captures: 710.3 MB read + 218.9 written
 TRAFFIC_SOURCE_SHA = "bbf7cd0786738437"
 CHUNK_SOURCE = os.path.join(ROOT, "linear_attention_state_kda_gb300", "csrc", "kda_chunk_tc.cu")
 
