@@ -608,11 +608,14 @@ def run_profile_case(args):
         sso8 = torch.tensor([0, 8], dtype=torch.int32, device=dev)
         M8, D8 = kda.segment_package(x.k, x.v, x.g, x.beta, offs8)
         si8, _ = kda.package_scan(M8, D8, sso8, 8)
+        # the replay as the bench's segment path runs it: a walk over records prepared once
+        # (the one-call kda_segment_replay takes the fused launch at this size)
+        ws_r = kda.chunk_prepare(x.q, x.k, x.v, x.g, x.beta, offs) if case == "replay" else None
         fns = {
             "prefill": [lambda: kda.chunk_prefill(x.q, x.k, x.v, x.g, x.beta)],
             "package": [lambda: kda.segment_package(x.k, x.v, x.g, x.beta, offs, M=M, D=Dp)],
             "scan": [lambda: kda.package_scan(M8, D8, sso8, 8, seg_init=si8)],
-            "replay": [lambda: kda.segment_replay(x.q, x.k, x.v, x.g, x.beta, offs, si)],
+            "replay": [lambda: kda.segment_replay_prepared(ws_r, offs, si, 4096, 32, D, D)],
         }[case]
     torch.cuda.synchronize()
     for _ in range(args.launches):
